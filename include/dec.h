@@ -1,0 +1,169 @@
+/*
+ * dec.h — C ABI of the batch-1 decode library (libtld_gb300.so).
+ *
+ * One decode step runs one token through a stack of Llama-style decoder layers
+ * with a KV cache that grows by one row per step.  The per-layer op chain is
+ * the one listed on "RDNA4 Decode Kernel Fusion: Pipeline Barriers, Not
+ * Launches, Are the Win", section "Decode is where the bubble has nowhere to
+ * go": input RMSNorm and weight multiply, QKV projection, RoPE on q and k,
+ * attention against the KV cache, output projection, post-attention RMSNorm
+ * and multiply, gate and up projections, SwiGLU, down projection.  The fused
+ * plan runs it as five kernels per layer (the fusions of that page's FAQ and
+ * of section "Fusion removes the barrier by removing the write"); the unfused
+ * plan keeps one kernel per op as the ablation ("Backend-Specific Kernel
+ * Fusion", section "A practical engineering example": keep the old route).
+ * Per step only the position advances; a CUDA graph of the whole token is
+ * captured once and replayed ("Vulkan Command Buffer Reuse vs CUDA Graphs:
+ * RDNA4 Decode Overhead", section "Why NVIDIA got a free 14 percent").
+ *
+ * Conventions for every call:
+ *   - returns DEC_OK (0) or a negative DEC_ERR_* code; the message of the last
+ *     failure is kept in the handle (dec_last_error);
+ *   - arguments are validated on the host, synchronously, before any work is
+ *     queued; no call aborts or exits the process;
+ *   - pointers marked "host or device" may point to either (CUDA unified
+ *     addressing decides); pointers marked "device" must be device memory;
+ *   - all calls on one handle must come from one host thread at a time.
+ */
+#ifndef TLD_GB300_DEC_H
+#define TLD_GB300_DEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* dec_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+enum dec_status {
+  DEC_OK = 0,
+  DEC_ERR_ARG = -1,    /* null pointer, bad enum, wrong byte count */
+  DEC_ERR_SHAPE = -2,  /* model shape this library does not support */
+  DEC_ERR_STATE = -3,  /* step before every weight / KV row is loaded */
+  DEC_ERR_POS = -4,    /* pos differs from the current KV length */
+  DEC_ERR_CTX = -5,    /* pos or KV length reaches max_ctx */
+  DEC_ERR_CUDA = -6,   /* a CUDA runtime call failed (message kept) */
+  DEC_ERR_OOM = -7,    /* device allocation failed */
+  DEC_ERR_DEVICE = -8  /* a kernel gave up a bounded wait and raised its error flag */
+};
+
+enum dec_weight_fmt {
+  DEC_W_BF16 = 0,  /* bf16 matrices [out][in], row-major (K contiguous) */
+  DEC_W_Q4B32 = 1  /* int4 in blocks of 32 along K + one fp16 scale per block;
+                      the GEMV inputs are quantized to int8 per 32-block */
+};
+
+enum dec_flags {
+  DEC_PLAN_FUSED = 0,    /* five kernels per layer (default) */
+  DEC_PLAN_UNFUSED = 1,  /* one kernel per op: the ablation / reference chain */
+  DEC_NO_GRAPH = 2       /* launch eagerly instead of replaying a CUDA graph */
+};
+
+/* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
+ * [hidden]) and the seven matrices (bf16 [out][in]).  Q4 models load the norm
+ * vectors, the seven matrices as packed nibbles ([out][in/32] blocks of 16
+ * bytes: element 2i in the low nibble and 2i+1 in the high nibble of byte i of
+ * the block, each stored as q + 8 in [0, 15]) and, under id + DEC_T_SCALES,
+ * their fp16 scales ([out][in/32]). */
+enum dec_tensor {
+  DEC_T_ATTN_NORM = 0, /* [hidden] */
+  DEC_T_WQ = 1,        /* [n_q_heads*head_dim][hidden] */
+  DEC_T_WK = 2,        /* [n_kv_heads*head_dim][hidden] */
+  DEC_T_WV = 3,        /* [n_kv_heads*head_dim][hidden] */
+  DEC_T_WO = 4,        /* [hidden][n_q_heads*head_dim] */
+  DEC_T_FFN_NORM = 5,  /* [hidden] */
+  DEC_T_WGATE = 6,     /* [ffn][hidden] */
+  DEC_T_WUP = 7,       /* [ffn][hidden] */
+  DEC_T_WDOWN = 8,     /* [hidden][ffn] */
+  DEC_T_SCALES = 16    /* add to WQ..WDOWN for the Q4 scales */
+};
+
+typedef struct dec_model_desc {
+  int32_t n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn;
+  float rms_eps;      /* RMSNorm epsilon, inside the square root */
+  float rope_theta;   /* RoPE base: angle of pair i at position p = p * theta^(-2i/head_dim) */
+  int32_t max_ctx;    /* KV cache capacity in positions */
+  int32_t weight_fmt; /* enum dec_weight_fmt */
+  int32_t flags;      /* enum dec_flags, OR-ed */
+} dec_model_desc;
+
+typedef struct dec_info {
+  int32_t kernels_per_layer;  /* launches per layer of the chosen plan */
+  int32_t kernels_per_token;  /* launches per dec_step */
+  int32_t n_sm;               /* SMs the grids are sized for */
+  int32_t kv_len;             /* current KV length (next pos) */
+  int64_t weight_bytes;       /* device bytes of all layers' weights as stored */
+  int64_t kv_bytes;           /* device bytes of the KV cache (both K and V) */
+  int64_t workspace_bytes;    /* device bytes of activations + split-K workspace */
+} dec_info;
+
+typedef struct dec_handle dec_handle; /* opaque */
+
+/* Validates the shape and allocates every device buffer (weights, KV cache,
+ * workspaces) on the current CUDA device.  Supported: head_dim 64 or 128,
+ * n_q_heads a multiple of n_kv_heads, hidden and ffn multiples of 8 (of 32
+ * for DEC_W_Q4B32), 1 <= max_ctx <= 65536.  *out is NULL on failure. */
+int dec_create(const dec_model_desc* desc, dec_handle** out);
+
+/* Copies one tensor of one layer (host or device src, `bytes` long, layout as
+ * in enum dec_tensor) into library-owned device memory, repacking it into the
+ * kernels' tiled layout.  Blocks until done.  The caller keeps src. */
+int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size_t bytes);
+
+/* Loads the first n_pos cache rows of one layer: k and v are host or device
+ * bf16 [n_kv_heads][n_pos][head_dim] (k already rotated by RoPE at its own
+ * position, v raw).  Sets that layer's KV length to n_pos.  Blocks until done
+ * and waits for all queued work of the device first. */
+int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16, int n_pos);
+
+/* Rewinds every layer's KV length to n_pos (<= the current length); rows past
+ * it are overwritten by later steps.  Waits for the device first. */
+int dec_truncate_kv(dec_handle* h, int n_pos);
+
+/* One decode step, queued on `stream`, returns after enqueue.
+ * token_embedding: device fp32 [hidden], the stack's input at this position.
+ * out_hidden: device fp32 [hidden], the last layer's output (no final norm,
+ * no LM head).  pos must equal the current KV length (strictly sequential);
+ * every layer appends its k, v at row pos and attends to rows 0..pos; after
+ * the call the KV length is pos + 1.  Neither buffer may be written by other
+ * work until the step has run. */
+int dec_step(dec_handle* h, const float* token_embedding, int pos, float* out_hidden,
+             dec_stream_t stream);
+
+/* Debug taps (both may be NULL): per_layer_out, device fp32 [n_layers][hidden],
+ * receives every layer's output at each step; qact_tap (DEC_W_Q4B32 only),
+ * device int8 [n_layers][4][max(hidden, ffn, n_q_heads*head_dim)], receives
+ * the int8 inputs of the q, o, gate and down projections, and qscale_tap,
+ * device fp32 [n_layers][4][max(...)/32], their block scales.  Setting taps
+ * discards the captured graph; it is recaptured at the next step. */
+int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qscale_tap);
+
+/* Waits for `stream` and reports DEC_ERR_DEVICE if any kernel raised its
+ * error flag (a bounded wait ran out); the flag is cleared. */
+int dec_sync_status(dec_handle* h, dec_stream_t stream);
+
+/* Fills *info; never fails on a valid handle. */
+int dec_get_info(const dec_handle* h, dec_info* info);
+
+/* Launches `count` times the fused plan's kernel `kernel` (0 = norm+QKV+RoPE+
+ * append, 1 = attention, 2 = o-proj+residual, 3 = norm+gate/up+SwiGLU,
+ * 4 = down+residual) for layers first_layer, first_layer+1, ... (mod
+ * n_layers), back to back on `stream`, on the activations the last step left.
+ * For timing one kernel alone; the KV length does not change and the next
+ * dec_step overwrites whatever these launches wrote. */
+int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream);
+
+/* Frees every device buffer and the graph; accepts NULL and partially
+ * created handles.  Waits for the device first. */
+int dec_destroy(dec_handle* h);
+
+/* Message of the last failed call on h ("" if none); h may be NULL, in which
+ * case the message of the last failed dec_create of this thread is returned. */
+const char* dec_last_error(const dec_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TLD_GB300_DEC_H */

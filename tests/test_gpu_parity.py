@@ -1,0 +1,142 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle on the
+same seeded inputs, per layer and per step (max|err| <= 2e-2, rel-L2 <= 5e-3),
+plus plan equivalence, determinism and graph / eager agreement."""
+import numpy as np
+import pytest
+
+from harness import assert_close, oracle_stack, run_gpu, run_oracle
+from transformer_layer_decode_gb300 import dec, synth, workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+def _check(w, steps, *, unfused=False, graph=True, max_ctx=None):
+    max_ctx = max_ctx or w.prefill + steps + 2
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=unfused, graph=graph,
+                                    keep_host=True)
+    xs = workload.step_inputs(w, steps)
+    got = run_gpu(d, w, xs)
+    d.close()
+    ref = run_oracle(oracle_stack(w, host, max_ctx), w, xs)
+    worst = (0.0, 0.0)
+    for s in range(steps):
+        for l in range(w.n_layers):
+            a, r = assert_close(got[s, l], ref[s, l], f"{w.name} step {s} layer {l}")
+            worst = (max(worst[0], a), max(worst[1], r))
+    return got, worst
+
+
+def test_layer_h512_single_step():
+    """One layer, hidden 512, GQA 8/2, d 64, F 1408, decode at pos 127."""
+    _check(synth.WORKLOADS["layer_h512"], 1)
+
+
+SMALL = {
+    # ragged K tiles (264 = 256 + 8; 1000 = 3*256 + 232), GQA 2, empty prefill (KV length 1)
+    "ragged_g2_empty": synth.Workload("ragged_g2_empty", 2, 264, 4, 2, 64, 1000, prefill=0, steps=3),
+    # MHA, head_dim 128, prefill not a multiple of the chunk
+    "mha_d128": synth.Workload("mha_d128", 2, 512, 4, 4, 128, 1408, prefill=45, steps=3),
+    # GQA 8, fewer rows than SMs
+    "g8_d64": synth.Workload("g8_d64", 1, 256, 16, 2, 64, 512, prefill=200, steps=2),
+    # GQA 4, d 128, context spanning many chunks and CTAs
+    "g4_d128_long": synth.Workload("g4_d128_long", 1, 1024, 8, 2, 128, 2816, prefill=1500, steps=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused"])
+def test_small_shapes(name, mode):
+    _check(SMALL[name], SMALL[name].steps, unfused=(mode == "unfused"),
+           graph=(mode != "fused_eager"))
+
+
+def test_stack16_h2048_all_steps():
+    """16-layer 1B-shape stack, 64 steps from pos 1023, every layer at every step."""
+    w = synth.WORKLOADS["stack16_h2048"]
+    _, worst = _check(w, w.steps)
+    print("stack16 worst max|err| %.3e rel-L2 %.3e" % worst)
+
+
+def test_plans_agree_and_are_deterministic():
+    w = SMALL["mha_d128"]
+    xs = workload.step_inputs(w, 3)
+    outs = {}
+    for key, kw in {"graph": {}, "graph2": {}, "eager": {"graph": False},
+                    "unfused": {"unfused": True}}.items():
+        d, _ = workload.make_decoder(w, max_ctx=64, **kw)
+        outs[key] = run_gpu(d, w, xs)
+        d.close()
+    assert np.array_equal(outs["graph"], outs["graph2"]), "fused plan not run-to-run identical"
+    assert np.array_equal(outs["graph"], outs["eager"]), "graph replay differs from eager launch"
+    for s in range(3):
+        for l in range(w.n_layers):
+            assert_close(outs["graph"][s, l], outs["unfused"][s, l], f"fused vs unfused {s},{l}")
+
+
+def test_residual_wiring_zero_projections():
+    """Wo = 0 and Wd = 0: every layer returns its input exactly."""
+    w = SMALL["mha_d128"]
+    d = dec.Decoder(workload.shape_of(w, 64))
+    for l in range(w.n_layers):
+        lw = synth.layer_weights(w, l)
+        lw.mats[synth.T_WO][:] = 0
+        lw.mats[synth.T_WDOWN][:] = 0
+        workload.load_layer(d, w, l, lw)
+        k, v = synth.kv_bf16(w, l, w.prefill)
+        d.load_kv(l, k, v)
+    xs = workload.step_inputs(w, 2)
+    got = run_gpu(d, w, xs)
+    d.close()
+    for s in range(2):
+        for l in range(w.n_layers):
+            assert np.array_equal(got[s, l], xs[s])
+
+
+def test_io_pointers_can_change_between_steps():
+    """The captured graph is re-pointed when the caller passes new buffers."""
+    w = SMALL["ragged_g2_empty"]
+    xs = workload.step_inputs(w, 3)
+    d_ref, _ = workload.make_decoder(w, max_ctx=16, graph=False)
+    ref = run_gpu(d_ref, w, xs, taps=False)
+    d_ref.close()
+    d, _ = workload.make_decoder(w, max_ctx=16)
+    outs = []
+    for s in range(3):
+        emb = torch.from_numpy(xs[s]).cuda()          # a fresh buffer every step
+        out = torch.full((w.hidden,), float("nan"), device="cuda")
+        d.step(emb, s, out)
+        d.sync_status()
+        outs.append(out.cpu().numpy())
+    d.close()
+    assert np.array_equal(np.stack(outs), ref)
+
+
+def test_step_errors_on_gpu():
+    w = SMALL["ragged_g2_empty"]
+    d, _ = workload.make_decoder(w, max_ctx=4)
+    emb = torch.zeros(w.hidden, device="cuda")
+    out = torch.zeros(w.hidden, device="cuda")
+    with pytest.raises(dec.DecError) as e:
+        d.step(emb, 1, out)                      # pos != KV length
+    assert e.value.code == dec.DEC_ERR_POS
+    for p in range(4):
+        d.step(emb, p, out)
+    with pytest.raises(dec.DecError) as e:
+        d.step(emb, 4, out)                      # cache full
+    assert e.value.code == dec.DEC_ERR_CTX
+    d.truncate_kv(1)
+    d.step(emb, 1, out)
+    d.sync_status()
+    with pytest.raises(dec.DecError) as e:
+        d.load_weights(0, dec.DEC_T_WQ, np.zeros(7, np.uint16))   # wrong size
+    assert e.value.code == dec.DEC_ERR_ARG
+    d.close()
+    fresh = dec.Decoder(workload.shape_of(w, 4))
+    with pytest.raises(dec.DecError) as e:
+        fresh.step(emb, 0, out)                  # weights missing
+    assert e.value.code == dec.DEC_ERR_STATE
+    fresh.close()

@@ -1,0 +1,736 @@
+// C ABI of the decode library: validation, device memory, the per-layer launch
+// plan (fused or unfused), and the whole-token CUDA graph whose only
+// per-step change is the step position held in device memory ("Vulkan Command
+// Buffer Reuse vs CUDA Graphs: RDNA4 Decode Overhead", section "Why NVIDIA got
+// a free 14 percent": capture once, patch the few per-token parameters).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "../../include/dec.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace tld;
+
+namespace {
+
+constexpr int kNumMats = 7;  // q k v o gate up down
+constexpr size_t kSmemBudget = 110 * 1024;  // two CTAs per SM (next kernel's prefetch)
+
+struct Tiled {  // one fused-plan matrix in the tiled layout
+  uint8_t* w = nullptr;
+  int N = 0, K = 0, ktiles = 0, kw_last = 0, n_rb = 0, nstages = 0, max_rb_local = 0;
+  int64_t ntiles = 0;
+  size_t smem = 0;
+};
+
+struct LayerDev {
+  uint16_t* attn_norm = nullptr;
+  uint16_t* ffn_norm = nullptr;
+  Tiled qkv, o, gu, down;                       // fused plan
+  uint16_t* mats[kNumMats] = {};                // unfused plan: row-major bf16
+  uint16_t* kc = nullptr;
+  uint16_t* vc = nullptr;
+  uint32_t loaded = 0;                          // bit per tensor id
+  int kv_len = 0;
+};
+
+thread_local std::string g_create_error;
+
+}  // namespace
+
+struct dec_handle {
+  dec_model_desc d{};
+  int n_sm = 0, G = 0;
+  bool fused = true, graph = true;
+  std::vector<LayerDev> layers;
+  std::vector<void*> allocs;
+  // activations / workspace
+  float *X = nullptr, *h1 = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
+  float *n1 = nullptr, *k = nullptr, *v = nullptr, *g = nullptr, *u = nullptr, *y = nullptr;
+  float* gpart = nullptr;
+  int* gcount = nullptr;
+  float* apart = nullptr;
+  int* acount = nullptr;
+  int* d_pos = nullptr;
+  int* d_err = nullptr;
+  float2* rope = nullptr;
+  uint16_t* staging = nullptr;
+  size_t staging_bytes = 0;
+  size_t attn_smem = 0;
+  int attn_nstages = 0;
+  int kv_len = 0;
+  int64_t weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
+  // taps
+  float* tap = nullptr;
+  int8_t* qtap = nullptr;
+  float* qstap = nullptr;
+  // graph
+  cudaStream_t cap_stream = nullptr;
+  cudaGraph_t graph_g = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  cudaGraphNode_t first_node = nullptr, last_node = nullptr;
+  const float* cap_emb = nullptr;
+  float* cap_out = nullptr;
+  std::string err;
+};
+
+namespace {
+
+int fail(dec_handle* h, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf;
+  else g_create_error = buf;
+  return code;
+}
+
+int cuda_fail(dec_handle* h, cudaError_t e, const char* what) {
+  return fail(h, DEC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define TLD_CUDA(h, call)                                    \
+  do {                                                       \
+    cudaError_t e_ = (call);                                 \
+    if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
+  } while (0)
+
+template <class T>
+int dev_alloc(dec_handle* h, T** p, size_t bytes, int64_t* account) {
+  void* v = nullptr;
+  cudaError_t e = cudaMalloc(&v, bytes < 16 ? 16 : bytes);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return fail(h, DEC_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  }
+  h->allocs.push_back(v);
+  if (account) *account += (int64_t)bytes;
+  *p = static_cast<T*>(v);
+  return DEC_OK;
+}
+
+// Plans the split of one tiled matrix over the grid.
+void plan_tiled(Tiled& t, int N, int K, int n_sm) {
+  t.N = N;
+  t.K = K;
+  t.ktiles = (K + kTileK - 1) / kTileK;
+  t.kw_last = K - kTileK * (t.ktiles - 1);
+  t.n_rb = N / kTileR;
+  t.ntiles = (int64_t)t.n_rb * t.ktiles;
+  int mx = 1;
+  for (int b = 0; b < n_sm; ++b) {
+    const int64_t a0 = split_begin(t.ntiles, n_sm, b), a1 = split_begin(t.ntiles, n_sm, b + 1);
+    if (a1 <= a0) continue;
+    const int span = (int)((a1 - 1) / t.ktiles - a0 / t.ktiles + 1);
+    if (span > mx) mx = span;
+  }
+  t.max_rb_local = mx;
+  const size_t fixed = gemv_smem_bytes(K, 0, mx);
+  int ns = (int)((kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kStageBytes);
+  if (ns < 2) ns = 2;
+  if (ns > 8) ns = 8;
+  t.nstages = ns;
+  t.smem = gemv_smem_bytes(K, ns, mx);
+}
+
+int max_k(const dec_model_desc& d) {
+  int m = d.hidden;
+  if (d.ffn > m) m = d.ffn;
+  if (d.n_q_heads * d.head_dim > m) m = d.n_q_heads * d.head_dim;
+  return m;
+}
+
+void mat_shape(const dec_model_desc& d, int tensor, int* N, int* K) {
+  const int H = d.hidden, hd = d.head_dim, F = d.ffn;
+  switch (tensor) {
+    case DEC_T_WQ: *N = d.n_q_heads * hd; *K = H; break;
+    case DEC_T_WK: *N = d.n_kv_heads * hd; *K = H; break;
+    case DEC_T_WV: *N = d.n_kv_heads * hd; *K = H; break;
+    case DEC_T_WO: *N = H; *K = d.n_q_heads * hd; break;
+    case DEC_T_WGATE: *N = F; *K = H; break;
+    case DEC_T_WUP: *N = F; *K = H; break;
+    case DEC_T_WDOWN: *N = H; *K = F; break;
+    default: *N = *K = 0;
+  }
+}
+
+uint32_t required_mask(const dec_model_desc& d) {
+  uint32_t m = (1u << DEC_T_ATTN_NORM) | (1u << DEC_T_FFN_NORM);
+  for (int t = DEC_T_WQ; t <= DEC_T_WDOWN; ++t) {
+    if (t == DEC_T_FFN_NORM) continue;
+    m |= 1u << t;
+    if (d.weight_fmt == DEC_W_Q4B32) m |= 1u << (t + DEC_T_SCALES);
+  }
+  return m;
+}
+
+void drop_graph(dec_handle* h) {
+  if (h->exec) cudaGraphExecDestroy(h->exec);
+  if (h->graph_g) cudaGraphDestroy(h->graph_g);
+  h->exec = nullptr;
+  h->graph_g = nullptr;
+  h->first_node = h->last_node = nullptr;
+}
+
+// ---- the fused plan ------------------------------------------------------------
+
+GemvParams gemv_base(const dec_handle* h, const Tiled& t) {
+  GemvParams p{};
+  p.w = t.w;
+  p.K = t.K;
+  p.ktiles = t.ktiles;
+  p.kw_last = t.kw_last;
+  p.n_rb = t.n_rb;
+  p.ntiles = t.ntiles;
+  p.nstages = t.nstages;
+  p.max_rb_local = t.max_rb_local;
+  p.eps = h->d.rms_eps;
+  p.part = h->gpart;
+  p.counters = h->gcount;
+  p.err = h->d_err;
+  p.nq = h->d.n_q_heads;
+  p.nkv = h->d.n_kv_heads;
+  p.hd = h->d.head_dim;
+  p.max_ctx = h->d.max_ctx;
+  p.pos = h->d_pos;
+  p.rope = h->rope;
+  return p;
+}
+
+GemvParams k1_params(const dec_handle* h, int l, const float* x_in, bool first) {
+  const LayerDev& L = h->layers[l];
+  GemvParams p = gemv_base(h, L.qkv);
+  p.x = x_in;
+  p.norm_w = L.attn_norm;
+  p.x_copy = first ? h->X : nullptr;
+  p.q_out = h->q;
+  p.kc = L.kc;
+  p.vc = L.vc;
+  return p;
+}
+
+AttnParams k2_params(const dec_handle* h, int l) {
+  const LayerDev& L = h->layers[l];
+  AttnParams p{};
+  p.kc = L.kc;
+  p.vc = L.vc;
+  p.q = h->q;
+  p.o = h->o;
+  p.part = h->apart;
+  p.counters = h->acount;
+  p.pos = h->d_pos;
+  p.err = h->d_err;
+  p.nkv = h->d.n_kv_heads;
+  p.max_ctx = h->d.max_ctx;
+  p.nstages = h->attn_nstages;
+  p.scale = (float)(1.0 / std::sqrt((double)h->d.head_dim));
+  return p;
+}
+
+GemvParams k3_params(const dec_handle* h, int l) {
+  GemvParams p = gemv_base(h, h->layers[l].o);
+  p.x = h->o;
+  p.resid = h->X;
+  p.out = h->h1;
+  return p;
+}
+
+GemvParams k4_params(const dec_handle* h, int l) {
+  const LayerDev& L = h->layers[l];
+  GemvParams p = gemv_base(h, L.gu);
+  p.x = h->h1;
+  p.norm_w = L.ffn_norm;
+  p.a_out = h->a;
+  return p;
+}
+
+GemvParams k5_params(const dec_handle* h, int l, float* out, bool last_of_step) {
+  GemvParams p = gemv_base(h, h->layers[l].down);
+  p.x = h->a;
+  p.resid = h->h1;
+  p.out = out;
+  p.tap = h->tap ? h->tap + (size_t)l * h->d.hidden : nullptr;
+  p.pos_advance = last_of_step ? h->d_pos : nullptr;
+  return p;
+}
+
+cudaGraphNode_t last_captured_node(cudaStream_t s) {
+  cudaStreamCaptureStatus st;
+  const cudaGraphNode_t* deps = nullptr;
+  size_t n = 0;
+  if (cudaStreamGetCaptureInfo(s, &st, nullptr, nullptr, &deps, nullptr, &n) != cudaSuccess ||
+      st != cudaStreamCaptureStatusActive || n == 0)
+    return nullptr;
+  return deps[n - 1];
+}
+
+int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, float* out,
+                         bool in_step, cudaStream_t s) {
+  const int nb = h->n_sm;
+  const LayerDev& L = h->layers[l];
+  const bool first = in_step && l == 0;
+  const bool last = l == h->d.n_layers - 1;
+  cudaError_t e = cudaSuccess;
+  switch (kernel) {
+    case 0:
+      e = launch_gemv(PRO_NORM, EPI_QKV, k1_params(h, l, first ? emb : h->X, first), nb,
+                      L.qkv.smem, s);
+      break;
+    case 1:
+      e = launch_attn(h->d.head_dim, h->G, k2_params(h, l), nb, h->attn_smem, s);
+      break;
+    case 2:
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, k3_params(h, l), nb, L.o.smem, s);
+      break;
+    case 3:
+      e = launch_gemv(PRO_NORM, EPI_SWIGLU, k4_params(h, l), nb, L.gu.smem, s);
+      break;
+    case 4:
+      e = launch_gemv(PRO_PLAIN, EPI_RESID,
+                      k5_params(h, l, (in_step && last) ? out : h->X, in_step && last), nb,
+                      L.down.smem, s);
+      break;
+    default:
+      return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+  return DEC_OK;
+}
+
+int enqueue_unfused_layer(dec_handle* h, int l, const float* x_in, float* out, bool last,
+                          cudaStream_t s) {
+  const dec_model_desc& d = h->d;
+  const LayerDev& L = h->layers[l];
+  const int H = d.hidden, hd = d.head_dim, F = d.ffn, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  float* tap = h->tap ? h->tap + (size_t)l * H : nullptr;
+#define TLD_U(call)                                        \
+  do {                                                     \
+    cudaError_t e_ = (call);                               \
+    if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
+  } while (0)
+  TLD_U(unf::rms_scale(x_in, H, d.rms_eps, h->n1, s));
+  TLD_U(unf::mul(h->n1, L.attn_norm, H, s));
+  TLD_U(unf::gemv(L.mats[0], nq * hd, H, h->n1, h->q, s));
+  TLD_U(unf::gemv(L.mats[1], nkv * hd, H, h->n1, h->k, s));
+  TLD_U(unf::gemv(L.mats[2], nkv * hd, H, h->n1, h->v, s));
+  TLD_U(unf::rope(h->q, h->k, nq, nkv, hd, h->d_pos, h->rope, s));
+  TLD_U(unf::kv_append(h->k, h->v, nkv, hd, d.max_ctx, h->d_pos, L.kc, L.vc, s));
+  TLD_U(unf::attention(h->q, L.kc, L.vc, nq, nkv, hd, d.max_ctx, h->d_pos, h->o, s));
+  TLD_U(unf::gemv(L.mats[3], H, nq * hd, h->o, h->y, s));
+  TLD_U(unf::add(x_in, h->y, h->h1, nullptr, H, nullptr, s));
+  TLD_U(unf::rms_scale(h->h1, H, d.rms_eps, h->n1, s));
+  TLD_U(unf::mul(h->n1, L.ffn_norm, H, s));
+  TLD_U(unf::gemv(L.mats[4], F, H, h->n1, h->g, s));
+  TLD_U(unf::gemv(L.mats[5], F, H, h->n1, h->u, s));
+  TLD_U(unf::swiglu(h->g, h->u, h->a, F, s));
+  TLD_U(unf::gemv(L.mats[6], H, F, h->a, h->y, s));
+  TLD_U(unf::add(h->h1, h->y, out, tap, H, last ? h->d_pos : nullptr, s));
+#undef TLD_U
+  return DEC_OK;
+}
+constexpr int kUnfusedKernelsPerLayer = 17;
+
+// Queues one whole token.  Records the first and last kernel nodes when capturing.
+int enqueue_step(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing) {
+  const int Lc = h->d.n_layers;
+  if (!h->fused) {
+    for (int l = 0; l < Lc; ++l) {
+      // the unfused chain ping-pongs the residual stream through X
+      const float* xin = (l == 0) ? emb : h->X;
+      float* xout = (l == Lc - 1) ? out : h->X;
+      int rc = enqueue_unfused_layer(h, l, xin, xout, l == Lc - 1, s);
+      if (rc) return rc;
+    }
+    return DEC_OK;
+  }
+  for (int l = 0; l < Lc; ++l) {
+    for (int k = 0; k < 5; ++k) {
+      int rc = enqueue_fused_kernel(h, k, l, emb, out, true, s);
+      if (rc) return rc;
+      if (capturing && l == 0 && k == 0) h->first_node = last_captured_node(s);
+      if (capturing && l == Lc - 1 && k == 4) h->last_node = last_captured_node(s);
+    }
+  }
+  return DEC_OK;
+}
+
+int capture(dec_handle* h, const float* emb, float* out) {
+  drop_graph(h);
+  if (!h->cap_stream) TLD_CUDA(h, cudaStreamCreateWithFlags(&h->cap_stream, cudaStreamNonBlocking));
+  TLD_CUDA(h, cudaStreamBeginCapture(h->cap_stream, cudaStreamCaptureModeThreadLocal));
+  int rc = enqueue_step(h, emb, out, h->cap_stream, true);
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaStreamEndCapture(h->cap_stream, &g);
+  if (rc) {
+    if (g) cudaGraphDestroy(g);
+    return rc;
+  }
+  if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
+  h->graph_g = g;
+  TLD_CUDA(h, cudaGraphInstantiate(&h->exec, g, 0));
+  if (h->fused && (!h->first_node || !h->last_node))
+    return fail(h, DEC_ERR_CUDA, "could not locate the captured kernel nodes");
+  h->cap_emb = emb;
+  h->cap_out = out;
+  return DEC_OK;
+}
+
+// Points the captured graph at new input / output buffers.
+int patch_io(dec_handle* h, const float* emb, float* out) {
+  if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
+  if (emb != h->cap_emb) {
+    GemvParams p = k1_params(h, 0, emb, true);
+    void* args[] = {&p};
+    cudaKernelNodeParams kp{};
+    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_NORM, EPI_QKV));
+    kp.gridDim = dim3(h->n_sm);
+    kp.blockDim = dim3(kThreads);
+    kp.sharedMemBytes = (unsigned)h->layers[0].qkv.smem;
+    kp.kernelParams = args;
+    TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->first_node, &kp));
+    h->cap_emb = emb;
+  }
+  if (out != h->cap_out) {
+    const int l = h->d.n_layers - 1;
+    GemvParams p = k5_params(h, l, out, true);
+    void* args[] = {&p};
+    cudaKernelNodeParams kp{};
+    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_PLAIN, EPI_RESID));
+    kp.gridDim = dim3(h->n_sm);
+    kp.blockDim = dim3(kThreads);
+    kp.sharedMemBytes = (unsigned)h->layers[l].down.smem;
+    kp.kernelParams = args;
+    TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->last_node, &kp));
+    h->cap_out = out;
+  }
+  return DEC_OK;
+}
+
+int set_device_pos(dec_handle* h, int pos) {
+  TLD_CUDA(h, cudaMemcpy(h->d_pos, &pos, sizeof(int), cudaMemcpyHostToDevice));
+  return DEC_OK;
+}
+
+}  // namespace
+
+// ---- C ABI ----------------------------------------------------------------------
+
+extern "C" {
+
+int dec_create(const dec_model_desc* desc, dec_handle** out) {
+  if (!out) return fail(nullptr, DEC_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  if (!desc) return fail(nullptr, DEC_ERR_ARG, "desc is NULL");
+  const dec_model_desc d = *desc;
+  if (d.n_layers < 1 || d.hidden < 1 || d.n_q_heads < 1 || d.n_kv_heads < 1 || d.ffn < 1 ||
+      d.max_ctx < 1 || !(d.rms_eps >= 0.f) || !(d.rope_theta > 0.f))
+    return fail(nullptr, DEC_ERR_ARG, "non-positive size or bad eps/theta in the model desc");
+  if (d.head_dim != 64 && d.head_dim != 128)
+    return fail(nullptr, DEC_ERR_SHAPE, "head_dim %d unsupported (64 or 128)", d.head_dim);
+  if (d.n_q_heads % d.n_kv_heads)
+    return fail(nullptr, DEC_ERR_SHAPE, "n_q_heads %% n_kv_heads != 0");
+  const int G = d.n_q_heads / d.n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8)
+    return fail(nullptr, DEC_ERR_SHAPE, "GQA group %d unsupported (1, 2, 4 or 8)", G);
+  if (d.hidden % 8 || d.ffn % 8)
+    return fail(nullptr, DEC_ERR_SHAPE, "hidden and ffn must be multiples of 8");
+  if (d.max_ctx > 65536) return fail(nullptr, DEC_ERR_SHAPE, "max_ctx > 65536");
+  if (d.weight_fmt != DEC_W_BF16 && d.weight_fmt != DEC_W_Q4B32)
+    return fail(nullptr, DEC_ERR_ARG, "unknown weight_fmt %d", d.weight_fmt);
+  if (d.weight_fmt == DEC_W_Q4B32)
+    return fail(nullptr, DEC_ERR_SHAPE, "int4 weights are not built in this library yet");
+  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH))
+    return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
+
+  dec_handle* h = new (std::nothrow) dec_handle();
+  if (!h) return fail(nullptr, DEC_ERR_OOM, "host allocation failed");
+  h->d = d;
+  h->G = G;
+  h->fused = !(d.flags & DEC_PLAN_UNFUSED);
+  h->graph = !(d.flags & DEC_NO_GRAPH);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = set_smem_limits();
+  if (e != cudaSuccess) {
+    g_create_error = std::string("CUDA device query: ") + cudaGetErrorString(e);
+    delete h;
+    return DEC_ERR_CUDA;
+  }
+  const int H = d.hidden, hd = d.head_dim, F = d.ffn, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  int rc = DEC_OK;
+  auto A = [&](auto** p, size_t bytes, int64_t* acct) {
+    if (rc == DEC_OK) rc = dev_alloc(h, p, bytes, acct);
+  };
+  h->layers.resize(d.n_layers);
+  for (int l = 0; l < d.n_layers; ++l) {
+    LayerDev& L = h->layers[l];
+    A(&L.attn_norm, 2 * (size_t)H, &h->weight_bytes);
+    A(&L.ffn_norm, 2 * (size_t)H, &h->weight_bytes);
+    if (h->fused) {
+      plan_tiled(L.qkv, (nq + 2 * nkv) * hd, H, h->n_sm);
+      plan_tiled(L.o, H, nq * hd, h->n_sm);
+      plan_tiled(L.gu, 2 * F, H, h->n_sm);
+      plan_tiled(L.down, H, F, h->n_sm);
+      for (Tiled* t : {&L.qkv, &L.o, &L.gu, &L.down})
+        A(&t->w, 2 * (size_t)t->N * t->K, &h->weight_bytes);
+    } else {
+      for (int m = 0; m < kNumMats; ++m) {
+        int N, K;
+        mat_shape(d, DEC_T_WQ + (m < 4 ? m : m + 1), &N, &K);
+        A(&L.mats[m], 2 * (size_t)N * K, &h->weight_bytes);
+      }
+    }
+    A(&L.kc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
+    A(&L.vc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
+  }
+  const int km = max_k(d);
+  int max_rb = 1;
+  if (h->fused)
+    for (const Tiled* t : {&h->layers[0].qkv, &h->layers[0].o, &h->layers[0].gu,
+                           &h->layers[0].down})
+      if (t->n_rb > max_rb) max_rb = t->n_rb;
+  A(&h->X, 4 * (size_t)H, &h->ws_bytes);
+  A(&h->h1, 4 * (size_t)H, &h->ws_bytes);
+  A(&h->q, 4 * (size_t)nq * hd, &h->ws_bytes);
+  A(&h->o, 4 * (size_t)nq * hd, &h->ws_bytes);
+  A(&h->a, 4 * (size_t)F, &h->ws_bytes);
+  A(&h->n1, 4 * (size_t)H, &h->ws_bytes);
+  A(&h->k, 4 * (size_t)nkv * hd, &h->ws_bytes);
+  A(&h->v, 4 * (size_t)nkv * hd, &h->ws_bytes);
+  A(&h->g, 4 * (size_t)F, &h->ws_bytes);
+  A(&h->u, 4 * (size_t)F, &h->ws_bytes);
+  A(&h->y, 4 * (size_t)km, &h->ws_bytes);
+  A(&h->gpart, 4 * (size_t)h->n_sm * 2 * kTileR, &h->ws_bytes);
+  A(&h->gcount, 4 * (size_t)max_rb, &h->ws_bytes);
+  A(&h->apart, 4 * (size_t)h->n_sm * 2 * G * (hd + 2), &h->ws_bytes);
+  A(&h->acount, 4 * (size_t)nkv, &h->ws_bytes);
+  A(&h->d_pos, 16, &h->ws_bytes);
+  A(&h->d_err, 16, &h->ws_bytes);
+  A(&h->rope, sizeof(float2) * (size_t)d.max_ctx * (hd / 2), &h->ws_bytes);
+  if (rc) {
+    dec_destroy(h);
+    g_create_error = "device allocation failed";
+    return rc;
+  }
+  // zero counters / flags / position; fill the RoPE table in double
+  e = cudaMemset(h->gcount, 0, 4 * (size_t)max_rb);
+  if (e == cudaSuccess) e = cudaMemset(h->acount, 0, 4 * (size_t)nkv);
+  if (e == cudaSuccess) e = cudaMemset(h->d_pos, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 16);
+  if (e == cudaSuccess) {
+    std::vector<float2> tab((size_t)d.max_ctx * (hd / 2));
+    for (int p = 0; p < d.max_ctx; ++p)
+      for (int i = 0; i < hd / 2; ++i) {
+        const double ang = (double)p * std::pow((double)d.rope_theta, -2.0 * i / hd);
+        tab[(size_t)p * (hd / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+      }
+    e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  }
+  if (e != cudaSuccess) {
+    g_create_error = std::string("initialising device buffers: ") + cudaGetErrorString(e);
+    dec_destroy(h);
+    return DEC_ERR_CUDA;
+  }
+  h->attn_nstages = 4;
+  h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+  *out = h;
+  return DEC_OK;
+}
+
+int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size_t bytes) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!src) return fail(h, DEC_ERR_ARG, "src is NULL");
+  const dec_model_desc& d = h->d;
+  if (layer < 0 || layer >= d.n_layers) return fail(h, DEC_ERR_ARG, "layer %d out of range", layer);
+  LayerDev& L = h->layers[layer];
+  if (tensor == DEC_T_ATTN_NORM || tensor == DEC_T_FFN_NORM) {
+    if (bytes != 2 * (size_t)d.hidden)
+      return fail(h, DEC_ERR_ARG, "norm vector: %zu bytes, expected %zu", bytes, 2 * (size_t)d.hidden);
+    TLD_CUDA(h, cudaMemcpy(tensor == DEC_T_ATTN_NORM ? L.attn_norm : L.ffn_norm, src, bytes,
+                           cudaMemcpyDefault));
+    L.loaded |= 1u << tensor;
+    return DEC_OK;
+  }
+  int N, K;
+  mat_shape(d, tensor, &N, &K);
+  if (N == 0) return fail(h, DEC_ERR_ARG, "tensor id %d invalid for this weight format", tensor);
+  const size_t want = 2 * (size_t)N * K;
+  if (bytes != want) return fail(h, DEC_ERR_ARG, "tensor %d: %zu bytes, expected %zu", tensor, bytes, want);
+  if (!h->fused) {
+    const int m = tensor <= DEC_T_WO ? tensor - DEC_T_WQ : tensor - DEC_T_WQ - 1;
+    TLD_CUDA(h, cudaMemcpy(L.mats[m], src, bytes, cudaMemcpyDefault));
+    L.loaded |= 1u << tensor;
+    return DEC_OK;
+  }
+  if (h->staging_bytes < want) {
+    if (h->staging) {
+      cudaFree(h->staging);
+      for (auto& p : h->allocs)
+        if (p == h->staging) p = nullptr;
+    }
+    h->staging = nullptr;
+    h->staging_bytes = 0;
+    int rc = dev_alloc(h, &h->staging, want, nullptr);
+    if (rc) return rc;
+    h->staging_bytes = want;
+  }
+  TLD_CUDA(h, cudaMemcpy(h->staging, src, bytes, cudaMemcpyDefault));
+  const int hd = d.head_dim;
+  cudaError_t e;
+  switch (tensor) {
+    case DEC_T_WQ: e = launch_repack_bf16(h->staging, N, K, L.qkv.w, 0, 1, hd, 0); break;
+    case DEC_T_WK:
+      e = launch_repack_bf16(h->staging, N, K, L.qkv.w, d.n_q_heads * hd, 1, hd, 0);
+      break;
+    case DEC_T_WV:
+      e = launch_repack_bf16(h->staging, N, K, L.qkv.w, (d.n_q_heads + d.n_kv_heads) * hd, 0, hd, 0);
+      break;
+    case DEC_T_WO: e = launch_repack_bf16(h->staging, N, K, L.o.w, 0, 0, hd, 0); break;
+    case DEC_T_WGATE: e = launch_repack_bf16(h->staging, N, K, L.gu.w, 0, 2, hd, 0); break;
+    case DEC_T_WUP: e = launch_repack_bf16(h->staging, N, K, L.gu.w, 1, 2, hd, 0); break;
+    default: e = launch_repack_bf16(h->staging, N, K, L.down.w, 0, 0, hd, 0); break;
+  }
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "weight repack");
+  L.loaded |= 1u << tensor;
+  return DEC_OK;
+}
+
+int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16, int n_pos) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  const dec_model_desc& d = h->d;
+  if (layer < 0 || layer >= d.n_layers) return fail(h, DEC_ERR_ARG, "layer %d out of range", layer);
+  if (n_pos < 0) return fail(h, DEC_ERR_ARG, "n_pos < 0");
+  if (n_pos >= d.max_ctx) return fail(h, DEC_ERR_CTX, "n_pos %d leaves no room (max_ctx %d)", n_pos, d.max_ctx);
+  if (n_pos > 0 && (!k_bf16 || !v_bf16)) return fail(h, DEC_ERR_ARG, "k or v is NULL");
+  TLD_CUDA(h, cudaDeviceSynchronize());
+  LayerDev& L = h->layers[layer];
+  if (n_pos > 0) {
+    const size_t row = 2 * (size_t)n_pos * d.head_dim, pitch = 2 * (size_t)d.max_ctx * d.head_dim;
+    TLD_CUDA(h, cudaMemcpy2D(L.kc, pitch, k_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
+    TLD_CUDA(h, cudaMemcpy2D(L.vc, pitch, v_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
+  }
+  L.kv_len = n_pos;
+  h->kv_len = n_pos;
+  return set_device_pos(h, n_pos);
+}
+
+int dec_truncate_kv(dec_handle* h, int n_pos) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  for (const LayerDev& L : h->layers)
+    if (n_pos < 0 || n_pos > L.kv_len)
+      return fail(h, DEC_ERR_POS, "truncate to %d beyond a layer's KV length %d", n_pos, L.kv_len);
+  TLD_CUDA(h, cudaDeviceSynchronize());
+  for (LayerDev& L : h->layers) L.kv_len = n_pos;
+  h->kv_len = n_pos;
+  return set_device_pos(h, n_pos);
+}
+
+int dec_step(dec_handle* h, const float* emb, int pos, float* out, dec_stream_t stream) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!emb || !out) return fail(h, DEC_ERR_ARG, "token_embedding or out_hidden is NULL");
+  const uint32_t need = required_mask(h->d);
+  for (int l = 0; l < h->d.n_layers; ++l) {
+    const LayerDev& L = h->layers[l];
+    if ((L.loaded & need) != need)
+      return fail(h, DEC_ERR_STATE, "layer %d: weights not all loaded (mask 0x%x of 0x%x)", l,
+                  L.loaded & need, need);
+    if (L.kv_len != h->kv_len)
+      return fail(h, DEC_ERR_STATE, "layer %d KV length %d differs from %d", l, L.kv_len, h->kv_len);
+  }
+  if (pos != h->kv_len) return fail(h, DEC_ERR_POS, "pos %d != KV length %d", pos, h->kv_len);
+  if (pos >= h->d.max_ctx) return fail(h, DEC_ERR_CTX, "pos %d >= max_ctx %d", pos, h->d.max_ctx);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int rc;
+  if (h->graph) {
+    rc = h->exec ? patch_io(h, emb, out) : capture(h, emb, out);
+    if (rc) return rc;
+    cudaError_t e = cudaGraphLaunch(h->exec, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "cudaGraphLaunch");
+  } else {
+    rc = enqueue_step(h, emb, out, s, false);
+    if (rc) return rc;
+  }
+  h->kv_len = pos + 1;
+  for (LayerDev& L : h->layers) L.kv_len = pos + 1;
+  return DEC_OK;
+}
+
+int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qscale_tap) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if ((qact_tap || qscale_tap) && h->d.weight_fmt != DEC_W_Q4B32)
+    return fail(h, DEC_ERR_ARG, "int8 activation taps need DEC_W_Q4B32");
+  h->tap = per_layer_out;
+  h->qtap = qact_tap;
+  h->qstap = qscale_tap;
+  drop_graph(h);
+  return DEC_OK;
+}
+
+int dec_sync_status(dec_handle* h, dec_stream_t stream) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  TLD_CUDA(h, cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+  int flag = 0;
+  TLD_CUDA(h, cudaMemcpy(&flag, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (flag) {
+    TLD_CUDA(h, cudaMemset(h->d_err, 0, sizeof(int)));
+    return fail(h, DEC_ERR_DEVICE, "a kernel gave up a bounded wait (flags 0x%x)", flag);
+  }
+  return DEC_OK;
+}
+
+int dec_get_info(const dec_handle* h, dec_info* info) {
+  if (!h || !info) return DEC_ERR_ARG;
+  info->kernels_per_layer = h->fused ? 5 : kUnfusedKernelsPerLayer;
+  info->kernels_per_token = info->kernels_per_layer * h->d.n_layers;
+  info->n_sm = h->n_sm;
+  info->kv_len = h->kv_len;
+  info->weight_bytes = h->weight_bytes;
+  info->kv_bytes = h->kv_bytes;
+  info->workspace_bytes = h->ws_bytes;
+  return DEC_OK;
+}
+
+int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!h->fused) return fail(h, DEC_ERR_STATE, "kernel launches need the fused plan");
+  if (kernel < 0 || kernel > 4 || count < 0 || first_layer < 0 || first_layer >= h->d.n_layers)
+    return fail(h, DEC_ERR_ARG, "bad kernel / layer / count");
+  const uint32_t need = required_mask(h->d);
+  for (const LayerDev& L : h->layers)
+    if ((L.loaded & need) != need) return fail(h, DEC_ERR_STATE, "weights not all loaded");
+  if (h->kv_len >= h->d.max_ctx) return fail(h, DEC_ERR_CTX, "KV cache full");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  for (int i = 0; i < count; ++i) {
+    int rc = enqueue_fused_kernel(h, kernel, (first_layer + i) % h->d.n_layers, nullptr, nullptr,
+                                  false, s);
+    if (rc) return rc;
+  }
+  return DEC_OK;
+}
+
+int dec_destroy(dec_handle* h) {
+  if (!h) return DEC_OK;
+  cudaDeviceSynchronize();
+  drop_graph(h);
+  if (h->cap_stream) cudaStreamDestroy(h->cap_stream);
+  for (void* p : h->allocs)
+    if (p) cudaFree(p);
+  delete h;
+  return DEC_OK;
+}
+
+const char* dec_last_error(const dec_handle* h) {
+  return h ? h->err.c_str() : g_create_error.c_str();
+}
+
+}  // extern "C"

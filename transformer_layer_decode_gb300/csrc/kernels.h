@@ -1,0 +1,129 @@
+// Parameter blocks and launchers of the decode kernels (host + device view).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace tld {
+
+// Balanced contiguous split of `total` units over `parts`: part p owns
+// [split_begin(p), split_begin(p+1)).
+__host__ __device__ inline int64_t split_begin(int64_t total, int parts, int p) {
+  return total * p / parts;
+}
+// The part owning unit u (inverse of split_begin).
+__host__ __device__ inline int split_owner(int64_t total, int parts, int64_t u) {
+  return (int)(((u + 1) * parts - 1) / total);
+}
+
+// ---- tiled weight layout ----------------------------------------------------
+// A [N][K] matrix is stored as row blocks of kTileR rows; each row block is a
+// run of k-tiles of kTileK columns (the last one kw = K - kTileK*(ktiles-1)
+// wide), each k-tile row-major inside.  Tiles are consecutive in memory in
+// (row block, k-tile) order, so any range of tiles is one contiguous run of
+// bytes: a CTA that owns tiles [t0, t1) streams exactly one slab.
+constexpr int kTileR = 4;
+constexpr int kTileK = 256;
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
+constexpr int kStageTiles = kConsumerWarps;          // one tile per consumer warp per stage
+constexpr int kStageBytes = kStageTiles * kTileR * kTileK * 2;  // 16 KB
+
+__host__ __device__ inline int64_t tile_byte_offset(int64_t t, int ktiles, int K) {
+  int64_t rb = t / ktiles, kt = t - rb * ktiles;
+  return rb * (int64_t)kTileR * K * 2 + kt * (int64_t)kTileR * kTileK * 2;
+}
+
+// Element (row r, col k) of a [N][K] matrix inside the tiled layout.
+__host__ __device__ inline int64_t tiled_elem_offset(int64_t r, int64_t k, int K) {
+  int ktiles = (K + kTileK - 1) / kTileK;
+  int64_t kt = k / kTileK;
+  int kw = (kt == ktiles - 1) ? K - kTileK * (ktiles - 1) : kTileK;
+  return (r / kTileR) * (int64_t)kTileR * K + kt * (int64_t)kTileR * kTileK +
+         (r % kTileR) * kw + (k - kt * kTileK);
+}
+
+enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
+enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+
+struct GemvParams {
+  const uint8_t* w;  // tiled weights
+  int K, ktiles, kw_last, n_rb;
+  int64_t ntiles;
+  int nstages, max_rb_local;
+  // prologue
+  const float* x;          // input vector [K]
+  const uint16_t* norm_w;  // bf16 [K] (PRO_NORM)
+  float eps;
+  float* x_copy;           // if set, CTA 0 also copies x here
+  // split row blocks
+  float* part;    // [grid][2][kTileR]
+  int* counters;  // [n_rb], zero between launches
+  int* err;
+  // EPI_QKV: rows are q (pair-interleaved per head), k (same), v
+  int nq, nkv, hd, max_ctx;
+  const int* pos;       // device step position
+  const float2* rope;   // [max_ctx][hd/2] (cos, sin)
+  float* q_out;         // [nq*hd]
+  uint16_t* kc;         // layer cache [nkv][max_ctx][hd]
+  uint16_t* vc;
+  // EPI_RESID
+  const float* resid;
+  float* out;
+  float* tap;
+  int* pos_advance;     // if set, CTA 0 adds 1 here (end of a step)
+  // EPI_SWIGLU: rows interleave gate and up
+  float* a_out;
+};
+
+struct AttnParams {
+  const uint16_t* kc;  // layer cache [nkv][max_ctx][hd]
+  const uint16_t* vc;
+  const float* q;      // [nq*hd] rotated
+  float* o;            // [nq*hd]
+  float* part;         // [grid][2][G][hd+2]
+  int* counters;       // [nkv]
+  const int* pos;
+  int* err;
+  int nkv, max_ctx, nstages;
+  float scale;
+};
+
+// Shared memory the fused kernels need.
+size_t gemv_smem_bytes(int K, int nstages, int max_rb_local);
+size_t attn_smem_bytes(int hd, int G, int nstages);
+
+// Launch with programmatic stream serialization (the kernel may start while
+// the previous one on the stream finishes; it waits before reading its inputs).
+cudaError_t launch_gemv(int pro, int epi, const GemvParams& p, int grid, size_t smem,
+                        cudaStream_t s);
+cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
+                        cudaStream_t s);
+const void* gemv_kernel_ptr(int pro, int epi);
+const void* attn_kernel_ptr(int hd, int G);
+cudaError_t set_smem_limits();
+
+// Load-time repack of a row-major [rows][K] bf16 block into the tiled layout
+// of a matrix with K columns, source row s going to tiled row map(s):
+//   map = dst_row0 + s                                  (kind 0, plain)
+//   q/k heads: dst_row0 + rope pair interleave          (kind 1)
+//   gate/up:   dst_row0 + 2*s (+1 for up via dst_row0)  (kind 2)
+cudaError_t launch_repack_bf16(const uint16_t* src, int rows, int K, uint8_t* dst_tiled,
+                               int dst_row0, int kind, int hd, cudaStream_t s);
+
+// ---- the unfused plan: one kernel per op -------------------------------------
+namespace unf {
+cudaError_t rms_scale(const float* x, int H, float eps, float* n, cudaStream_t s);
+cudaError_t mul(float* n, const uint16_t* w, int H, cudaStream_t s);
+cudaError_t gemv(const uint16_t* W, int N, int K, const float* x, float* y, cudaStream_t s);
+cudaError_t rope(float* q, float* k, int nq, int nkv, int hd, const int* pos, const float2* tab,
+                 cudaStream_t s);
+cudaError_t kv_append(const float* k, const float* v, int nkv, int hd, int max_ctx, const int* pos,
+                      uint16_t* kc, uint16_t* vc, cudaStream_t s);
+cudaError_t attention(const float* q, const uint16_t* kc, const uint16_t* vc, int nq, int nkv,
+                      int hd, int max_ctx, const int* pos, float* o, cudaStream_t s);
+cudaError_t add(const float* a, const float* b, float* out, float* tap, int n, int* pos_advance,
+                cudaStream_t s);
+cudaError_t swiglu(const float* g, const float* u, float* a, int F, cudaStream_t s);
+}  // namespace unf
+
+}  // namespace tld

@@ -1,0 +1,192 @@
+"""ctypes binding of the decode library's C ABI (include/dec.h).
+
+Argument marshalling only: every step of the decode runs in the library's
+CUDA kernels.  PyTorch provides device memory and streams.  If the library has
+not been built, :func:`load_library` raises; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtld_gb300.so")
+
+# enum values of dec.h
+DEC_OK, DEC_ERR_ARG, DEC_ERR_SHAPE, DEC_ERR_STATE = 0, -1, -2, -3
+DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6, -7, -8
+DEC_W_BF16, DEC_W_Q4B32 = 0, 1
+DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH = 0, 1, 2
+DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
+DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
+
+KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
+                "norm_gateup_swiglu", "down_residual")
+
+EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_truncate_kv", "dec_step",
+            "dec_set_tap", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
+            "dec_destroy", "dec_last_error")
+
+
+class DecError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{msg} (code {code})")
+        self.code = code
+
+
+class ModelDesc(ctypes.Structure):
+    _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("n_q_heads", ctypes.c_int32), ("n_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("ffn", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float),
+                ("max_ctx", ctypes.c_int32), ("weight_fmt", ctypes.c_int32),
+                ("flags", ctypes.c_int32)]
+
+
+class Info(ctypes.Structure):
+    _fields_ = [("kernels_per_layer", ctypes.c_int32), ("kernels_per_token", ctypes.c_int32),
+                ("n_sm", ctypes.c_int32), ("kv_len", ctypes.c_int32),
+                ("weight_bytes", ctypes.c_int64), ("kv_bytes", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libtld_gb300.so (built by ``build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"decode library not built: {path} is missing "
+                           "(run transformer_layer_decode_gb300.build.build())")
+    L = ctypes.CDLL(path)
+    vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sig = {
+        "dec_create": [ctypes.POINTER(ModelDesc), ctypes.POINTER(vp)],
+        "dec_load_weights": [vp, i32, i32, vp, sz],
+        "dec_load_kv": [vp, i32, vp, vp, i32],
+        "dec_truncate_kv": [vp, i32],
+        "dec_step": [vp, vp, i32, vp, vp],
+        "dec_set_tap": [vp, vp, vp, vp],
+        "dec_sync_status": [vp, vp],
+        "dec_get_info": [vp, ctypes.POINTER(Info)],
+        "dec_launch_kernel": [vp, i32, i32, i32, vp],
+        "dec_destroy": [vp],
+    }
+    for name, args in sig.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = i32
+    L.dec_last_error.argtypes = [vp]
+    L.dec_last_error.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _ptr(x) -> int | None:
+    """Address of a torch tensor, numpy array or raw int pointer (None passes NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if isinstance(x, np.ndarray):
+        assert x.flags.c_contiguous, "arrays must be C-contiguous"
+        return x.ctypes.data
+    if hasattr(x, "data_ptr"):
+        assert x.is_contiguous(), "tensors must be contiguous"
+        return x.data_ptr()
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _nbytes(x) -> int:
+    if isinstance(x, np.ndarray):
+        return x.nbytes
+    return x.numel() * x.element_size()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+@dataclass
+class Shape:
+    n_layers: int
+    hidden: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ffn: int
+    max_ctx: int
+    rms_eps: float = 1e-6
+    rope_theta: float = 1e4
+    weight_fmt: int = DEC_W_BF16
+
+
+class Decoder:
+    """One decode handle: weights, KV cache and the captured step graph."""
+
+    def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True):
+        self.lib = load_library()
+        self.shape = shape
+        flags = (DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
+        self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
+                              shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
+                              shape.max_ctx, shape.weight_fmt, flags)
+        h = ctypes.c_void_p()
+        rc = self.lib.dec_create(ctypes.byref(self.desc), ctypes.byref(h))
+        if rc != DEC_OK:
+            raise DecError(rc, self.lib.dec_last_error(None).decode())
+        self.h = h
+
+    def _check(self, rc: int):
+        if rc != DEC_OK:
+            raise DecError(rc, self.lib.dec_last_error(self.h).decode())
+
+    def load_weights(self, layer: int, tensor: int, src):
+        self._check(self.lib.dec_load_weights(self.h, layer, tensor, _ptr(src), _nbytes(src)))
+
+    def load_kv(self, layer: int, k, v, n_pos: int | None = None):
+        n = k.shape[1] if n_pos is None else n_pos
+        self._check(self.lib.dec_load_kv(self.h, layer, _ptr(k), _ptr(v), n))
+
+    def truncate_kv(self, n_pos: int):
+        self._check(self.lib.dec_truncate_kv(self.h, n_pos))
+
+    def step(self, emb, pos: int, out, stream=None):
+        self._check(self.lib.dec_step(self.h, _ptr(emb), pos, _ptr(out), _stream_handle(stream)))
+
+    def set_tap(self, per_layer_out=None, qact=None, qscale=None):
+        self._check(self.lib.dec_set_tap(self.h, _ptr(per_layer_out), _ptr(qact), _ptr(qscale)))
+
+    def sync_status(self, stream=None):
+        self._check(self.lib.dec_sync_status(self.h, _stream_handle(stream)))
+
+    def info(self) -> Info:
+        inf = Info()
+        self._check(self.lib.dec_get_info(self.h, ctypes.byref(inf)))
+        return inf
+
+    def launch_kernel(self, kernel: int, first_layer: int, count: int, stream=None):
+        self._check(self.lib.dec_launch_kernel(self.h, kernel, first_layer, count,
+                                               _stream_handle(stream)))
+
+    def close(self):
+        if getattr(self, "h", None):
+            self.lib.dec_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
