@@ -39,6 +39,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="stack32_h4096_mha")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="override the layer count (small profiling cases only)")
     return ap.parse_args()
 
 
@@ -430,6 +432,8 @@ def main():
     rank, world, local_rank = dist_env()
     from transformer_layer_decode_gb300 import synth
     w = synth.WORKLOADS[args.workload]
+    if args.layers:
+        w = w.small(n_layers=args.layers, name=f"{w.name}_{args.layers}layers")
     if args.impl == "reference":
         res = run_reference(args, w, rank, world)
     else:

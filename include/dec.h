@@ -58,7 +58,9 @@ enum dec_weight_fmt {
 enum dec_flags {
   DEC_PLAN_FUSED = 0,    /* five kernels per layer (default) */
   DEC_PLAN_UNFUSED = 1,  /* one kernel per op: the ablation / reference chain */
-  DEC_NO_GRAPH = 2       /* launch eagerly instead of replaying a CUDA graph */
+  DEC_NO_GRAPH = 2,      /* launch eagerly instead of replaying a CUDA graph */
+  DEC_NO_PDL = 4         /* fused plan: launch without programmatic dependent launch,
+                            so each kernel starts only after the previous one ends */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
@@ -139,6 +141,18 @@ int dec_step(dec_handle* h, const float* token_embedding, int pos, float* out_hi
  * device fp32 [n_layers][4][max(...)/32], their block scales.  Setting taps
  * discards the captured graph; it is recaptured at the next step. */
 int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qscale_tap);
+
+/* GPU timeline probe of the fused plan (NULL turns it off): buf is device
+ * uint64 [kernels_per_token][8]; at every step, launch i (layer * 5 + kernel)
+ * records, in %globaltimer nanoseconds as atomic min / max: [0] earliest CTA
+ * start, [1] latest CTA end, [2] / [3] earliest / latest return from
+ * griddepcontrol.wait, [4] latest arrival of a CTA's first stage, [5] / [6]
+ * earliest / latest end of a CTA's streaming loop, [7] earliest CTA end.
+ * The caller initialises the min slots (0, 2, 5, 7) to UINT64_MAX and the max
+ * slots (1, 3, 4, 6) to 0.
+ * Setting it discards the captured graph.  For measurement only ("RDNA4
+ * Decode Kernel Fusion", section "What I am building next": GPU timestamps). */
+int dec_set_timeline(dec_handle* h, uint64_t* buf);
 
 /* Waits for `stream` and reports DEC_ERR_DEVICE if any kernel raised its
  * error flag (a bounded wait ran out); the flag is cleared. */

@@ -29,6 +29,11 @@ static void check_split(int64_t total, int parts) {
     CHECK(a == prev, "contiguous");
     prev = b;
     for (int64_t u = a; u < b; ++u) CHECK(split_owner(total, parts, u) == p, "owner %ld", (long)u);
+    if (total * parts < (1LL << 31)) {
+      CHECK(split_begin32((int)total, parts, p) == a, "split_begin32");
+      for (int64_t u = a; u < b; ++u)
+        CHECK(split_owner32((int)total, parts, (int)u) == p, "owner32 %ld", (long)u);
+    }
   }
 }
 

@@ -13,7 +13,7 @@ namespace tld {
 // means something is broken; the kernel then raises the error flag and leaves.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-enum ErrBits : int { ERR_FULL_WAIT = 1, ERR_EMPTY_WAIT = 2, ERR_DRAIN = 4 };
+enum ErrBits : int { ERR_FULL_WAIT = 1, ERR_EMPTY_WAIT = 2, ERR_DRAIN = 4, ERR_SPLITS = 8 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -70,11 +70,64 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// L2 cache policies for bulk copies: the weight stream of the running kernel is
+// read once (evict first); prefetched data of the next kernel should stay.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// bulk_g2s with an L2 cache policy.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Ticket for the last-arrival pattern: release this thread's prior writes and
+// acquire the other arrivals' writes in one atomic.
+__device__ __forceinline__ int atomic_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // Programmatic dependent launch: wait for the preceding grid's completion and
 // memory, and let the following grid start its prologue early.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Timeline probe of one launch (ns, %globaltimer): [0] first CTA start,
+// [1] last CTA end, [2] / [3] first / last return from griddepcontrol.wait,
+// [4] last CTA to receive its first stage, [5] / [6] first / last CTA to end
+// its main loop, [7] first CTA end.
+__device__ __forceinline__ void tl_mark_min(uint64_t* tl, int i) {
+  if (tl) atomicMin(reinterpret_cast<unsigned long long*>(tl + i), (unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void tl_mark_max(uint64_t* tl, int i) {
+  if (tl) atomicMax(reinterpret_cast<unsigned long long*>(tl + i), (unsigned long long)globaltimer_ns());
 }
 
 __device__ __forceinline__ void named_barrier(int id, int nthreads) {

@@ -20,7 +20,6 @@ using namespace tld;
 namespace {
 
 constexpr int kNumMats = 7;  // q k v o gate up down
-constexpr size_t kSmemBudget = 110 * 1024;  // two CTAs per SM (next kernel's prefetch)
 
 struct Tiled {  // one fused-plan matrix in the tiled layout
   uint8_t* w = nullptr;
@@ -47,16 +46,15 @@ thread_local std::string g_create_error;
 struct dec_handle {
   dec_model_desc d{};
   int n_sm = 0, G = 0;
-  bool fused = true, graph = true;
+  bool fused = true, graph = true, pdl = true;
   std::vector<LayerDev> layers;
   std::vector<void*> allocs;
   // activations / workspace
   float *X = nullptr, *h1 = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
   float *n1 = nullptr, *k = nullptr, *v = nullptr, *g = nullptr, *u = nullptr, *y = nullptr;
-  float* gpart = nullptr;
-  int* gcount = nullptr;
-  float* apart = nullptr;
-  int* acount = nullptr;
+  float* apart = nullptr;  // attention partial records
+  int* acount = nullptr;   // attention arrivals per split head
+  int att_grid = 0;
   int* d_pos = nullptr;
   int* d_err = nullptr;
   float2* rope = nullptr;
@@ -67,6 +65,7 @@ struct dec_handle {
   int kv_len = 0;
   int64_t weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
   // taps
+  uint64_t* timeline = nullptr;
   float* tap = nullptr;
   int8_t* qtap = nullptr;
   float* qstap = nullptr;
@@ -117,7 +116,8 @@ int dev_alloc(dec_handle* h, T** p, size_t bytes, int64_t* account) {
   return DEC_OK;
 }
 
-// Plans the split of one tiled matrix over the grid.
+// Plans one tiled matrix: each CTA owns whole row blocks; the ring gets as
+// many 32 KB stages as the shared-memory budget leaves.
 void plan_tiled(Tiled& t, int N, int K, int n_sm) {
   t.N = N;
   t.K = K;
@@ -125,20 +125,13 @@ void plan_tiled(Tiled& t, int N, int K, int n_sm) {
   t.kw_last = K - kTileK * (t.ktiles - 1);
   t.n_rb = N / kTileR;
   t.ntiles = (int64_t)t.n_rb * t.ktiles;
-  int mx = 1;
-  for (int b = 0; b < n_sm; ++b) {
-    const int64_t a0 = split_begin(t.ntiles, n_sm, b), a1 = split_begin(t.ntiles, n_sm, b + 1);
-    if (a1 <= a0) continue;
-    const int span = (int)((a1 - 1) / t.ktiles - a0 / t.ktiles + 1);
-    if (span > mx) mx = span;
-  }
-  t.max_rb_local = mx;
-  const size_t fixed = gemv_smem_bytes(K, 0, mx);
-  int ns = (int)((kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kStageBytes);
-  if (ns < 2) ns = 2;
+  t.max_rb_local = (t.n_rb + n_sm - 1) / n_sm;
+  const size_t fixed = gemv_smem_bytes(K, 0, t.max_rb_local);
+  int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kStageBytes);
+  if (ns < 2) ns = 2;  // may then exceed the co-residency budget (large K)
   if (ns > 8) ns = 8;
   t.nstages = ns;
-  t.smem = gemv_smem_bytes(K, ns, mx);
+  t.smem = gemv_smem_bytes(K, ns, t.max_rb_local);
 }
 
 int max_k(const dec_model_desc& d) {
@@ -193,8 +186,6 @@ GemvParams gemv_base(const dec_handle* h, const Tiled& t) {
   p.nstages = t.nstages;
   p.max_rb_local = t.max_rb_local;
   p.eps = h->d.rms_eps;
-  p.part = h->gpart;
-  p.counters = h->gcount;
   p.err = h->d_err;
   p.nq = h->d.n_q_heads;
   p.nkv = h->d.n_kv_heads;
@@ -278,26 +269,39 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
   const LayerDev& L = h->layers[l];
   const bool first = in_step && l == 0;
   const bool last = l == h->d.n_layers - 1;
+  uint64_t* tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + kernel) : nullptr;
   cudaError_t e = cudaSuccess;
   switch (kernel) {
-    case 0:
-      e = launch_gemv(PRO_NORM, EPI_QKV, k1_params(h, l, first ? emb : h->X, first), nb,
-                      L.qkv.smem, s);
+    case 0: {
+      GemvParams p = k1_params(h, l, first ? emb : h->X, first);
+      p.tl = tl;
+      e = launch_gemv(PRO_NORM, EPI_QKV, p, nb, L.qkv.smem, s, h->pdl);
       break;
-    case 1:
-      e = launch_attn(h->d.head_dim, h->G, k2_params(h, l), nb, h->attn_smem, s);
+    }
+    case 1: {
+      AttnParams p = k2_params(h, l);
+      p.tl = tl;
+      e = launch_attn(h->d.head_dim, h->G, p, h->att_grid, h->attn_smem, s, h->pdl);
       break;
-    case 2:
-      e = launch_gemv(PRO_PLAIN, EPI_RESID, k3_params(h, l), nb, L.o.smem, s);
+    }
+    case 2: {
+      GemvParams p = k3_params(h, l);
+      p.tl = tl;
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, p, nb, L.o.smem, s, h->pdl);
       break;
-    case 3:
-      e = launch_gemv(PRO_NORM, EPI_SWIGLU, k4_params(h, l), nb, L.gu.smem, s);
+    }
+    case 3: {
+      GemvParams p = k4_params(h, l);
+      p.tl = tl;
+      e = launch_gemv(PRO_NORM, EPI_SWIGLU, p, nb, L.gu.smem, s, h->pdl);
       break;
-    case 4:
-      e = launch_gemv(PRO_PLAIN, EPI_RESID,
-                      k5_params(h, l, (in_step && last) ? out : h->X, in_step && last), nb,
-                      L.down.smem, s);
+    }
+    case 4: {
+      GemvParams p = k5_params(h, l, (in_step && last) ? out : h->X, in_step && last);
+      p.tl = tl;
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, p, nb, L.down.smem, s, h->pdl);
       break;
+    }
     default:
       return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
   }
@@ -388,6 +392,7 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
   if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
   if (emb != h->cap_emb) {
     GemvParams p = k1_params(h, 0, emb, true);
+    p.tl = h->timeline;
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
     kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_NORM, EPI_QKV));
@@ -401,6 +406,7 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
   if (out != h->cap_out) {
     const int l = h->d.n_layers - 1;
     GemvParams p = k5_params(h, l, out, true);
+    p.tl = h->timeline ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 4) : nullptr;
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
     kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_PLAIN, EPI_RESID));
@@ -447,7 +453,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return fail(nullptr, DEC_ERR_ARG, "unknown weight_fmt %d", d.weight_fmt);
   if (d.weight_fmt == DEC_W_Q4B32)
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights are not built in this library yet");
-  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH))
+  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -456,6 +462,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->G = G;
   h->fused = !(d.flags & DEC_PLAN_UNFUSED);
   h->graph = !(d.flags & DEC_NO_GRAPH);
+  h->pdl = !(d.flags & DEC_NO_PDL);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
@@ -466,6 +473,9 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return DEC_ERR_CUDA;
   }
   const int H = d.hidden, hd = d.head_dim, F = d.ffn, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  // attention grid: at most kMaxSplits - 1 CTAs per KV head, so a head is never
+  // split over more than kMaxSplits CTAs
+  h->att_grid = h->n_sm < (kMaxSplits - 1) * nkv ? h->n_sm : (kMaxSplits - 1) * nkv;
   int rc = DEC_OK;
   auto A = [&](auto** p, size_t bytes, int64_t* acct) {
     if (rc == DEC_OK) rc = dev_alloc(h, p, bytes, acct);
@@ -493,11 +503,6 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     A(&L.vc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
   }
   const int km = max_k(d);
-  int max_rb = 1;
-  if (h->fused)
-    for (const Tiled* t : {&h->layers[0].qkv, &h->layers[0].o, &h->layers[0].gu,
-                           &h->layers[0].down})
-      if (t->n_rb > max_rb) max_rb = t->n_rb;
   A(&h->X, 4 * (size_t)H, &h->ws_bytes);
   A(&h->h1, 4 * (size_t)H, &h->ws_bytes);
   A(&h->q, 4 * (size_t)nq * hd, &h->ws_bytes);
@@ -509,9 +514,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   A(&h->g, 4 * (size_t)F, &h->ws_bytes);
   A(&h->u, 4 * (size_t)F, &h->ws_bytes);
   A(&h->y, 4 * (size_t)km, &h->ws_bytes);
-  A(&h->gpart, 4 * (size_t)h->n_sm * 2 * kTileR, &h->ws_bytes);
-  A(&h->gcount, 4 * (size_t)max_rb, &h->ws_bytes);
-  A(&h->apart, 4 * (size_t)h->n_sm * 2 * G * (hd + 2), &h->ws_bytes);
+  A(&h->apart, 4 * (size_t)h->att_grid * 2 * G * (hd + 4), &h->ws_bytes);
   A(&h->acount, 4 * (size_t)nkv, &h->ws_bytes);
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
@@ -521,10 +524,10 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     g_create_error = "device allocation failed";
     return rc;
   }
-  // zero counters / flags / position; fill the RoPE table in double
-  e = cudaMemset(h->gcount, 0, 4 * (size_t)max_rb);
+  // zero the flags / position / partials; fill the RoPE table in double
+  e = cudaMemset(h->d_pos, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(h->apart, 0, 4 * (size_t)h->att_grid * 2 * G * (hd + 4));
   if (e == cudaSuccess) e = cudaMemset(h->acount, 0, 4 * (size_t)nkv);
-  if (e == cudaSuccess) e = cudaMemset(h->d_pos, 0, 16);
   if (e == cudaSuccess) e = cudaMemset(h->d_err, 0, 16);
   if (e == cudaSuccess) {
     std::vector<float2> tab((size_t)d.max_ctx * (hd / 2));
@@ -540,8 +543,12 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     dec_destroy(h);
     return DEC_ERR_CUDA;
   }
-  h->attn_nstages = 4;
-  h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+  {
+    const size_t fixed = attn_smem_bytes(hd, G, 0);
+    int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
+    h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+    h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+  }
   *out = h;
   return DEC_OK;
 }
@@ -672,6 +679,14 @@ int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qs
   h->tap = per_layer_out;
   h->qtap = qact_tap;
   h->qstap = qscale_tap;
+  drop_graph(h);
+  return DEC_OK;
+}
+
+int dec_set_timeline(dec_handle* h, uint64_t* buf) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (buf && !h->fused) return fail(h, DEC_ERR_STATE, "the timeline probe needs the fused plan");
+  h->timeline = buf;
   drop_graph(h);
   return DEC_OK;
 }

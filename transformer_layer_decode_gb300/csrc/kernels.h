@@ -11,6 +11,11 @@ __host__ __device__ inline int64_t split_begin(int64_t total, int parts, int p) 
   return total * p / parts;
 }
 // The part owning unit u (inverse of split_begin).
+// 32-bit forms, for total * parts < 2^31.
+__host__ __device__ inline int split_begin32(int total, int parts, int p) { return total * p / parts; }
+__host__ __device__ inline int split_owner32(int total, int parts, int u) {
+  return ((u + 1) * parts - 1) / total;
+}
 __host__ __device__ inline int split_owner(int64_t total, int parts, int64_t u) {
   return (int)(((u + 1) * parts - 1) / total);
 }
@@ -25,8 +30,22 @@ constexpr int kTileR = 4;
 constexpr int kTileK = 256;
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
-constexpr int kStageTiles = kConsumerWarps;          // one tile per consumer warp per stage
-constexpr int kStageBytes = kStageTiles * kTileR * kTileK * 2;  // 16 KB
+// Shared memory budget per CTA.  Above half of the SM's 228 KB, so two CTAs of
+// one kernel never share an SM; the next kernel (programmatic dependent launch)
+// then takes each SM as soon as its current CTA leaves and starts streaming.
+#ifndef TLD_SMEM_BUDGET_KB
+#define TLD_SMEM_BUDGET_KB 220
+#endif
+constexpr int kSmemBudget = TLD_SMEM_BUDGET_KB * 1024;
+constexpr int kAttnStageBytes = 32768;  // K chunk + V chunk, 16 KB each
+// Bytes of its slab each GEMV CTA pulls into L2 at launch (beyond its ring).
+constexpr int kL2PrefetchBytes = 256 * 1024;
+constexpr int kTimelineSlots = 8;  // u64 per launch of the timeline probe
+// Most attention CTAs one KV head may be split over (bounds the merge).
+constexpr int kMaxSplits = 32;
+constexpr int kStageTiles = 2 * kConsumerWarps;      // two tiles per consumer warp per stage
+constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
+constexpr int kStageBytes = kStageTiles * kTileR * kTileK * 2;  // 32 KB
 
 __host__ __device__ inline int64_t tile_byte_offset(int64_t t, int ktiles, int K) {
   int64_t rb = t / ktiles, kt = t - rb * ktiles;
@@ -55,9 +74,6 @@ struct GemvParams {
   const uint16_t* norm_w;  // bf16 [K] (PRO_NORM)
   float eps;
   float* x_copy;           // if set, CTA 0 also copies x here
-  // split row blocks
-  float* part;    // [grid][2][kTileR]
-  int* counters;  // [n_rb], zero between launches
   int* err;
   // EPI_QKV: rows are q (pair-interleaved per head), k (same), v
   int nq, nkv, hd, max_ctx;
@@ -73,6 +89,7 @@ struct GemvParams {
   int* pos_advance;     // if set, CTA 0 adds 1 here (end of a step)
   // EPI_SWIGLU: rows interleave gate and up
   float* a_out;
+  uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
 };
 
 struct AttnParams {
@@ -80,12 +97,13 @@ struct AttnParams {
   const uint16_t* vc;
   const float* q;      // [nq*hd] rotated
   float* o;            // [nq*hd]
-  float* part;         // [grid][2][G][hd+2]
-  int* counters;       // [nkv]
+  float* part;         // [grid][2][G][hd+4]: (acc, m, l) of split heads
+  int* counters;       // [nkv] arrivals per split head, zero between launches
   const int* pos;
   int* err;
   int nkv, max_ctx, nstages;
   float scale;
+  uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
 };
 
 // Shared memory the fused kernels need.
@@ -95,9 +113,9 @@ size_t attn_smem_bytes(int hd, int G, int nstages);
 // Launch with programmatic stream serialization (the kernel may start while
 // the previous one on the stream finishes; it waits before reading its inputs).
 cudaError_t launch_gemv(int pro, int epi, const GemvParams& p, int grid, size_t smem,
-                        cudaStream_t s);
+                        cudaStream_t s, bool pdl);
 cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
-                        cudaStream_t s);
+                        cudaStream_t s, bool pdl);
 const void* gemv_kernel_ptr(int pro, int epi);
 const void* attn_kernel_ptr(int hd, int G);
 cudaError_t set_smem_limits();

@@ -3,25 +3,25 @@
 // Five kernels per layer (the fusions of "RDNA4 Decode Kernel Fusion:
 // Pipeline Barriers, Not Launches, Are the Win", FAQ and section "Fusion
 // removes the barrier by removing the write"):
-//   K1 gemv<PRO_NORM,  EPI_QKV>    RMSNorm*w prologue, [Wq;Wk;Wv] GEMV, RoPE on
-//                                  q and k and the k/v append in the epilogue
-//   K2 attn_decode                 GQA split-KV attention + last-CTA combine
+//   K1 gemv<PRO_NORM,  EPI_QKV>    RMSNorm*w, [Wq;Wk;Wv] GEMV, RoPE on q and k
+//                                  and the k/v append in the epilogue
+//   K2 attn_decode                 GQA split-KV attention; a head split over
+//                                  CTAs is merged by the last one to finish
 //   K3 gemv<PRO_PLAIN, EPI_RESID>  Wo GEMV + residual add
-//   K4 gemv<PRO_NORM,  EPI_SWIGLU> RMSNorm*w prologue, interleaved gate/up GEMV,
+//   K4 gemv<PRO_NORM,  EPI_SWIGLU> RMSNorm*w, interleaved gate/up GEMV,
 //                                  silu(g)*u in the epilogue (g, u never stored)
 //   K5 gemv<PRO_PLAIN, EPI_RESID>  Wd GEMV + residual add
 //
 // Batch-1 projections are matrix-vector products: one flop per weight byte, so
-// they are bound by HBM, not by the tensor cores.  Each GEMV CTA owns one
-// contiguous slab of the tiled weight matrix (a balanced split of its tiles
-// over the grid) and streams it through a ring of 16 KB shared-memory stages
-// filled by 1-D bulk copies (TMA) issued by one producer thread; eight
-// consumer warps each take one 4-row x 256-column tile per stage, read the
-// input vector from shared memory and accumulate in fp32.  A row block cut by
-// the split is finished by the last CTA to arrive (atomic ticket, partials
-// summed in CTA order, so results are deterministic).  Weights do not depend
-// on the previous kernel, so the producer starts streaming before
-// griddepcontrol.wait; only the input vector waits for the previous kernel.
+// they are bound by HBM, not by the tensor cores.  Each GEMV CTA owns a
+// contiguous run of whole 4-row blocks of the tiled weight matrix, i.e. one
+// contiguous slab of bytes, and streams it through a ring of 32 KB
+// shared-memory stages filled by 1-D bulk copies (TMA) issued by one producer
+// thread.  Eight consumer warps each take two 4-row x 256-column tiles per
+// stage, copy them to registers, hand the stage back, and accumulate against
+// the input vector held in shared memory in fp32.  Because CTAs own whole rows,
+// no partial sums cross CTAs.  Weights do not depend on the previous kernel:
+// the producer starts streaming at launch, before griddepcontrol.wait.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -32,35 +32,35 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 // ---- shared memory layout of the GEMV kernel -------------------------------
 struct GemvSmem {
   int K, nstages, max_rb_local;
-  __host__ __device__ size_t stages_off() const { return 0; }
   __host__ __device__ size_t bars_off() const { return (size_t)nstages * kStageBytes; }
-  __host__ __device__ size_t xs_off() const { return bars_off() + 2 * 8 * (size_t)nstages; }
+  __host__ __device__ size_t xs_off() const { return bars_off() + 16 * (size_t)nstages; }
   __host__ __device__ size_t part_off() const { return xs_off() + 4 * (size_t)((K + 3) & ~3); }
   __host__ __device__ size_t red_off() const {
     return part_off() + 4 * (size_t)max_rb_local * kConsumerWarps * kTileR;
   }
-  __host__ __device__ size_t total() const { return red_off() + 4 * 32 + 16; }  // red[0..8]: warp sums + abort mark
+  __host__ __device__ size_t total() const { return red_off() + 4 * 32; }  // red: warp sums + abort mark
 };
 
 size_t gemv_smem_bytes(int K, int nstages, int max_rb_local) {
   return GemvSmem{K, nstages, max_rb_local}.total();
 }
 
-// Epilogue of one finished row block (4 tiled rows, values v).
+// Epilogue of one finished row block (kTileR tiled rows, values v).
 template <int EPI>
-__device__ __forceinline__ void gemv_epilogue(const GemvParams& p, int rb, const float v[4]) {
+__device__ __forceinline__ void gemv_epilogue(const GemvParams& p, int rb, const float v[kTileR]) {
   const int R0 = rb * kTileR;
   if (EPI == EPI_QKV) {
     const int hd = p.hd, half = hd / 2;
     const int qrows = p.nq * hd, krows = p.nkv * hd;
     const int pos = *p.pos;
     if (R0 < qrows + krows) {
+      // rows (2i, 2i+1) of a head hold dims i and i + hd/2: rotate the pair
       const bool is_q = R0 < qrows;
       const int local = is_q ? R0 : R0 - qrows;
-      const int head = local / hd, i0 = (local % hd) / 2;  // two rope pairs: i0, i0+1
+      const int head = local / hd, i0 = (local % hd) / 2;
       const float2* cs = p.rope + (size_t)pos * half;
 #pragma unroll
-      for (int pr = 0; pr < 2; ++pr) {
+      for (int pr = 0; pr < kTileR / 2; ++pr) {
         const int i = i0 + pr;
         const float a = v[2 * pr], b = v[2 * pr + 1];
         const float2 c = cs[i];
@@ -80,33 +80,47 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, int rb, const
       const int head = local / hd, j = local % hd;
       uint16_t* row = p.vc + ((size_t)head * p.max_ctx + pos) * hd;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) row[j + r] = f32_to_bf16_bits(v[r]);
+      for (int r = 0; r < kTileR; ++r) row[j + r] = f32_to_bf16_bits(v[r]);
     }
   } else if (EPI == EPI_RESID) {
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < kTileR; ++r) {
       const float y = p.resid[R0 + r] + v[r];
       p.out[R0 + r] = y;
       if (p.tap) p.tap[R0 + r] = y;
     }
-  } else {  // EPI_SWIGLU: tiled rows (g_j, u_j, g_j+1, u_j+1)
+  } else {  // EPI_SWIGLU: tiled rows alternate gate and up of the same output
     const int j = R0 / 2;
-    p.a_out[j] = silu_f(v[0]) * v[1];
-    p.a_out[j + 1] = silu_f(v[2]) * v[3];
+#pragma unroll
+    for (int pr = 0; pr < kTileR / 2; ++pr) p.a_out[j + pr] = silu_f(v[2 * pr]) * v[2 * pr + 1];
   }
 }
 
-// Reduce 4 per-lane row accumulators over the warp; lane 8r ends with row r.
+// A position in the tiled matrix, advanced without divisions.
+struct TileCursor {
+  int rb, kt;
+  __device__ __forceinline__ void advance(int n, int ktiles) {
+    kt += n;
+    while (kt >= ktiles) {
+      kt -= ktiles;
+      ++rb;
+    }
+  }
+  // byte offset of the tile from the matrix start
+  __device__ __forceinline__ int64_t offset(int K) const {
+    return (int64_t)rb * kTileR * K * 2 + (int64_t)kt * kTileR * kTileK * 2;
+  }
+};
+
+// Reduce 4 per-lane row accumulators over the warp: each butterfly step keeps
+// half of the rows and hands the other half to the partner lane; lane 8r ends
+// with the total of row r.
 __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
-  const bool hi = lane & 16;
-  float keep0 = hi ? a[2] : a[0], keep1 = hi ? a[3] : a[1];
-  const float send0 = hi ? a[0] : a[2], send1 = hi ? a[1] : a[3];
-  keep0 += __shfl_xor_sync(0xffffffffu, send0, 16);
-  keep1 += __shfl_xor_sync(0xffffffffu, send1, 16);
-  const bool b3 = lane & 8;
-  float k = b3 ? keep1 : keep0;
-  const float snd = b3 ? keep0 : keep1;
-  k += __shfl_xor_sync(0xffffffffu, snd, 8);
+  const bool h16 = lane & 16;
+  const float k0 = (h16 ? a[2] : a[0]) + __shfl_xor_sync(0xffffffffu, h16 ? a[0] : a[2], 16);
+  const float k1 = (h16 ? a[3] : a[1]) + __shfl_xor_sync(0xffffffffu, h16 ? a[1] : a[3], 16);
+  const bool h8 = lane & 8;
+  float k = (h8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
   k += __shfl_xor_sync(0xffffffffu, k, 4);
   k += __shfl_xor_sync(0xffffffffu, k, 2);
   k += __shfl_xor_sync(0xffffffffu, k, 1);
@@ -114,10 +128,10 @@ __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
 }
 
 template <int PRO, int EPI>
-__global__ void __launch_bounds__(kThreads, 2) gemv_fused(const GemvParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const GemvSmem L{p.K, p.nstages, p.max_rb_local};
-  uint8_t* stages = smem + L.stages_off();
+  uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off());
   uint64_t* empty = full + p.nstages;
   float* xs = reinterpret_cast<float*>(smem + L.xs_off());
@@ -126,8 +140,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fused(const GemvParams p) {
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = gridDim.x, b = blockIdx.x;
-  const int64_t t0 = split_begin(p.ntiles, nb, b), t1 = split_begin(p.ntiles, nb, b + 1);
-  const int nloc = (int)(t1 - t0);
+  if (tid == 0) tl_mark_min(p.tl, 0);
+  // whole row blocks [rb0, rb1) of this CTA = tiles [t0, t1)
+  const int rb0 = (int)split_begin(p.n_rb, nb, b), rb1 = (int)split_begin(p.n_rb, nb, b + 1);
+  const int nrb = rb1 - rb0;
+  const int64_t t0 = (int64_t)rb0 * p.ktiles;
+  const int nloc = nrb * p.ktiles;
   const int nst = (nloc + kStageTiles - 1) / kStageTiles;
 
   if (tid == 0) {
@@ -142,126 +160,201 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fused(const GemvParams p) {
   if (warp == kConsumerWarps) {
     // ---- producer: stream this CTA's slab (weights only: no wait needed) ----
     if (lane == 0) {
+      TileCursor cur{rb0, 0};
+      const int64_t end_off = (int64_t)rb1 * kTileR * p.K * 2;
+      const uint64_t pol_stream = policy_evict_first();
+      int slot = 0, phase = 0;
       for (int s = 0; s < nst; ++s) {
-        const int slot = s % p.nstages;
-        if (s >= p.nstages && !mbar_wait(&empty[slot], ((s / p.nstages) - 1) & 1)) {
+        if (s >= p.nstages && !mbar_wait(&empty[slot], phase ^ 1)) {
           raise_error(p.err, ERR_EMPTY_WAIT);
           break;
         }
-        const int64_t ta = t0 + (int64_t)s * kStageTiles;
-        const int64_t tb = min(ta + kStageTiles, t1);
-        const int64_t oa = tile_byte_offset(ta, p.ktiles, p.K);
-        const uint32_t bytes = (uint32_t)(tile_byte_offset(tb, p.ktiles, p.K) - oa);
+        const int64_t oa = cur.offset(p.K);
+        cur.advance(kStageTiles, p.ktiles);
+        const int64_t ob = (s == nst - 1) ? end_off : cur.offset(p.K);
+        const uint32_t bytes = (uint32_t)(ob - oa);
         mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s(stages + (size_t)slot * kStageBytes, p.w + oa, bytes, &full[slot]);
+        bulk_g2s_hint(stages + (size_t)slot * kStageBytes, p.w + oa, bytes, &full[slot], pol_stream);
+        if (++slot == p.nstages) {
+          slot = 0;
+          phase ^= 1;
+        }
       }
     }
     return;
   }
 
   // ---- consumers -------------------------------------------------------------
+  constexpr int NC = kConsumerWarps * 32;
+  const int K4 = p.K / 4;
+  // Before the wait: the RMSNorm weights (static) go to xs as fp32.
+  if (PRO == PRO_NORM) {
+    const uint2* w4 = reinterpret_cast<const uint2*>(p.norm_w);
+    for (int k4 = tid; k4 < K4; k4 += NC) {
+      const uint2 wb = w4[k4];
+      reinterpret_cast<float4*>(xs)[k4] =
+          make_float4(bf16lo(wb.x), bf16hi(wb.x), bf16lo(wb.y), bf16hi(wb.y));
+    }
+  }
+  for (int i = tid; i < p.max_rb_local * kConsumerWarps * kTileR; i += NC) part_s[i] = 0.f;
+  if (tid == 0) red[kConsumerWarps] = 0.f;
+
   pdl_wait();  // the input vector comes from the previous kernel
-  // Let the next kernel launch (and prefetch its weights) now.  Triggering only
-  // after this CTA's own wait keeps at most two kernels in flight and means that
+  if (tid == 0) {
+    tl_mark_min(p.tl, 2);
+    tl_mark_max(p.tl, 3);
+  }
+  // Let the next kernel launch (and start its weight stream) now.  Triggering
+  // only after this CTA's own wait keeps at most two kernels in flight and means
   // everything before the previous kernel is complete when the next one starts.
   pdl_trigger();
-  constexpr int NC = kConsumerWarps * 32;
-  if (tid == 0) red[kConsumerWarps] = 0.f;
+
   if (PRO == PRO_NORM) {
-    float ss = 0.f;
+    // RMSNorm is a per-vector scale: the projection runs on x*w and the scale
+    // 1/sqrt(mean(x^2)+eps) is applied to the finished rows.
     const float4* x4 = reinterpret_cast<const float4*>(p.x);
-    for (int k4 = tid; k4 < p.K / 4; k4 += NC) {
-      const float4 v = x4[k4];
-      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    float ss = 0.f;
+    constexpr int PB = 4;  // loads in flight per thread
+    for (int base = tid; base < K4; base += NC * PB) {
+      float4 v[PB];
+#pragma unroll
+      for (int u = 0; u < PB; ++u)
+        if (base + u * NC < K4) v[u] = x4[base + u * NC];
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        const int k4 = base + u * NC;
+        if (k4 < K4) {
+          ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+          float4 w = reinterpret_cast<float4*>(xs)[k4];
+          w.x *= v[u].x;
+          w.y *= v[u].y;
+          w.z *= v[u].z;
+          w.w *= v[u].w;
+          reinterpret_cast<float4*>(xs)[k4] = w;
+        }
+      }
     }
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
-    named_barrier(1, NC);
-    float tot = 0.f;
-#pragma unroll
-    for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
-    const float r = 1.0f / sqrtf(tot / (float)p.K + p.eps);
-    const uint2* w4 = reinterpret_cast<const uint2*>(p.norm_w);
-    for (int k4 = tid; k4 < p.K / 4; k4 += NC) {
-      const float4 v = x4[k4];
-      const uint2 wb = w4[k4];
-      float4 o;
-      o.x = v.x * r * bf16lo(wb.x);
-      o.y = v.y * r * bf16hi(wb.x);
-      o.z = v.z * r * bf16lo(wb.y);
-      o.w = v.w * r * bf16hi(wb.y);
-      reinterpret_cast<float4*>(xs)[k4] = o;
-    }
   } else {
     const float4* x4 = reinterpret_cast<const float4*>(p.x);
-    for (int k4 = tid; k4 < p.K / 4; k4 += NC) reinterpret_cast<float4*>(xs)[k4] = x4[k4];
+    constexpr int PB = 4;
+    for (int base = tid; base < K4; base += NC * PB) {
+      float4 v[PB];
+#pragma unroll
+      for (int u = 0; u < PB; ++u)
+        if (base + u * NC < K4) v[u] = x4[base + u * NC];
+#pragma unroll
+      for (int u = 0; u < PB; ++u)
+        if (base + u * NC < K4) reinterpret_cast<float4*>(xs)[base + u * NC] = v[u];
+    }
   }
   if (p.x_copy && b == 0) {
     for (int k = tid; k < p.K; k += NC) p.x_copy[k] = p.x[k];
   }
   if (p.pos_advance && b == 0 && tid == 0) atomicAdd(p.pos_advance, 1);
-  for (int i = tid; i < p.max_rb_local * kConsumerWarps * kTileR; i += NC) part_s[i] = 0.f;
   named_barrier(1, NC);
 
-  const int rb_first = nloc > 0 ? (int)(t0 / p.ktiles) : 0;
+  float rnorm = 1.f;
+  if (PRO == PRO_NORM) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
+    rnorm = 1.0f / sqrtf(tot / (float)p.K + p.eps);
+  }
   int cur_rb = -1;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  float acc[kTileR];
+#pragma unroll
+  for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
   bool ok = true;
+  // cursors: the first tile of the current stage and this warp's two tiles in it
+  TileCursor st_cur{rb0, 0};
+  TileCursor my[kTilesPerWarp];
+#pragma unroll
+  for (int j = 0; j < kTilesPerWarp; ++j) {
+    my[j] = st_cur;
+    my[j].advance(warp + j * kConsumerWarps, p.ktiles);
+  }
+  const int c = lane * 8;
+  int slot = 0, phase = 0;
   for (int s = 0; s < nst; ++s) {
-    const int slot = s % p.nstages;
     // After a timed-out wait the warp stops waiting but keeps the same control
     // flow, so that every named barrier below is still reached by all warps.
-    if (ok && !mbar_wait(&full[slot], (s / p.nstages) & 1)) {
+    if (ok && !mbar_wait(&full[slot], phase)) {
       raise_error(p.err, ERR_FULL_WAIT);
       ok = false;
     }
-    const int li = s * kStageTiles + warp;
-    if (li < nloc) {
-      const int64_t t = t0 + li;
-      const int rb = (int)(t / p.ktiles), kt = (int)(t - (int64_t)rb * p.ktiles);
+    if (s == 0 && tid == 0) tl_mark_max(p.tl, 4);
+    // Copy this warp's tiles into registers and hand the slot back at once, so
+    // the next bulk copy is in flight while the FMAs run.
+    uint4 wv[kTilesPerWarp][kTileR];
+    const int64_t st_off = st_cur.offset(p.K);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int li = s * kStageTiles + warp + j * kConsumerWarps;
+      const int kw = (my[j].kt == p.ktiles - 1) ? p.kw_last : kTileK;
+      if (li < nloc && c < kw) {
+        const uint8_t* tp = stages + (size_t)slot * kStageBytes + (my[j].offset(p.K) - st_off);
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r)
+          wv[j][r] = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int li = s * kStageTiles + warp + j * kConsumerWarps;
+      if (li >= nloc) continue;
+      const int rb = my[j].rb, kt = my[j].kt;
       if (rb != cur_rb) {
         if (cur_rb >= 0) {
           const float v = warp_reduce4(acc, lane);
           if ((lane & 7) == 0)
-            part_s[((cur_rb - rb_first) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
+            part_s[((cur_rb - rb0) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
         }
         cur_rb = rb;
-        acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
       }
       const int kw = (kt == p.ktiles - 1) ? p.kw_last : kTileK;
-      const int64_t sa = t0 + (int64_t)s * kStageTiles;
-      const uint8_t* tp = stages + (size_t)slot * kStageBytes +
-                          (tile_byte_offset(t, p.ktiles, p.K) - tile_byte_offset(sa, p.ktiles, p.K));
-      const int c = lane * 8;
       if (c < kw) {
         const float4 xa = *reinterpret_cast<const float4*>(xs + kt * kTileK + c);
         const float4 xb = *reinterpret_cast<const float4*>(xs + kt * kTileK + c + 4);
 #pragma unroll
         for (int r = 0; r < kTileR; ++r) {
-          const uint4 wv = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
           float a = acc[r];
-          a = fmaf(bf16lo(wv.x), xa.x, a);
-          a = fmaf(bf16hi(wv.x), xa.y, a);
-          a = fmaf(bf16lo(wv.y), xa.z, a);
-          a = fmaf(bf16hi(wv.y), xa.w, a);
-          a = fmaf(bf16lo(wv.z), xb.x, a);
-          a = fmaf(bf16hi(wv.z), xb.y, a);
-          a = fmaf(bf16lo(wv.w), xb.z, a);
-          a = fmaf(bf16hi(wv.w), xb.w, a);
+          a = fmaf(bf16lo(wv[j][r].x), xa.x, a);
+          a = fmaf(bf16hi(wv[j][r].x), xa.y, a);
+          a = fmaf(bf16lo(wv[j][r].y), xa.z, a);
+          a = fmaf(bf16hi(wv[j][r].y), xa.w, a);
+          a = fmaf(bf16lo(wv[j][r].z), xb.x, a);
+          a = fmaf(bf16hi(wv[j][r].z), xb.y, a);
+          a = fmaf(bf16lo(wv[j][r].w), xb.z, a);
+          a = fmaf(bf16hi(wv[j][r].w), xb.w, a);
           acc[r] = a;
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
+    st_cur.advance(kStageTiles, p.ktiles);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, p.ktiles);
+    if (++slot == p.nstages) {
+      slot = 0;
+      phase ^= 1;
+    }
   }
   if (cur_rb >= 0) {
     const float v = warp_reduce4(acc, lane);
     if ((lane & 7) == 0)
-      part_s[((cur_rb - rb_first) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
+      part_s[((cur_rb - rb0) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
   }
   if (!ok && lane == 0) red[kConsumerWarps] = 1.f;  // abort mark
   named_barrier(1, NC);
+  if (tid == 0) {
+    tl_mark_min(p.tl, 5);
+    tl_mark_max(p.tl, 6);
+  }
   if (red[kConsumerWarps] != 0.f) {
     // Drain: wait (bounded) for the last copy into every slot, then leave.
     if (tid == 0)
@@ -271,48 +364,25 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fused(const GemvParams p) {
       }
     return;
   }
-  if (nloc == 0) return;
 
-  // ---- finish row blocks ------------------------------------------------------
-  const int rb_last = (int)((t1 - 1) / p.ktiles);
-  for (int j = tid; j <= rb_last - rb_first; j += NC) {
-    const int rb = rb_first + j;
-    float v[4];
+  // ---- finish this CTA's row blocks (sum over warps in warp order) ------------
+  for (int j = tid; j < nrb; j += NC) {
+    float v[kTileR];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float s = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) s += part_s[(j * kConsumerWarps + w) * kTileR + r];
-      v[r] = s;
-    }
-    const int64_t rb_t0 = (int64_t)rb * p.ktiles, rb_t1 = rb_t0 + p.ktiles;
-    if (rb_t0 >= t0 && rb_t1 <= t1) {
-      gemv_epilogue<EPI>(p, rb, v);
-      continue;
-    }
-    // split row block: publish, take a ticket, the last arrival finishes it
-    const int side = (j == 0) ? 0 : 1;
-    float* mine = p.part + ((size_t)b * 2 + side) * kTileR;
+    for (int r = 0; r < kTileR; ++r) {
+      float sum = 0.f;
 #pragma unroll
-    for (int r = 0; r < 4; ++r) mine[r] = v[r];
-    __threadfence();
-    const int c_lo = split_owner(p.ntiles, nb, rb_t0), c_hi = split_owner(p.ntiles, nb, rb_t1 - 1);
-    int expected = 0;
-    for (int c = c_lo; c <= c_hi; ++c)
-      expected += split_begin(p.ntiles, nb, c + 1) > split_begin(p.ntiles, nb, c);
-    const int prev = atomicAdd(&p.counters[rb], 1);
-    if (prev != expected - 1) continue;
-    __threadfence();
-    float tot[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = c_lo; c <= c_hi; ++c) {
-      const int64_t cs = split_begin(p.ntiles, nb, c), ce = split_begin(p.ntiles, nb, c + 1);
-      if (ce <= cs) continue;
-      const int sd = (cs / p.ktiles == rb) ? 0 : 1;
-      const float* q = p.part + ((size_t)c * 2 + sd) * kTileR;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) tot[r] += __ldcg(q + r);
+      for (int w = 0; w < kConsumerWarps; ++w) sum += part_s[(j * kConsumerWarps + w) * kTileR + r];
+      v[r] = sum * rnorm;
     }
-    gemv_epilogue<EPI>(p, rb, tot);
-    p.counters[rb] = 0;
+    gemv_epilogue<EPI>(p, rb0 + j, v);
+  }
+  if (p.tl) {
+    named_barrier(1, NC);
+    if (tid == 0) {
+      tl_mark_max(p.tl, 1);
+      tl_mark_min(p.tl, 7);
+    }
   }
 }
 
@@ -323,25 +393,48 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_fused(const GemvParams p) {
 // read once.  Within a CTA the 8 consumer warps take interleaved positions of
 // each chunk and keep a running (max, sum, acc) per query head; warps are
 // merged at the end of each head segment, and a head cut between CTAs is
-// merged by the last CTA to arrive, in CTA order.
+// merged by the o-projection kernel, in CTA order.
 
 struct AttnSmem {
   int hd, G, nstages;
-  __host__ __device__ size_t bars_off() const { return (size_t)nstages * 16384; }
+  __host__ __device__ size_t bars_off() const { return (size_t)nstages * kAttnStageBytes; }
   __host__ __device__ size_t ws_off() const { return bars_off() + 16 * (size_t)nstages; }
-  __host__ __device__ size_t seg_off() const {
+  __host__ __device__ size_t merge_off() const {
     return ws_off() + 4 * (size_t)kConsumerWarps * G * (hd + 2);
   }
-  __host__ __device__ size_t flag_off() const { return seg_off() + 4 * (size_t)G * (hd + 2); }
-  __host__ __device__ size_t total() const { return flag_off() + 16; }
+  // merge scratch: the record offset per split, then the heads to merge
+  __host__ __device__ size_t total() const { return merge_off() + 4 * (size_t)kMaxSplits + 16; }
 };
 
 size_t attn_smem_bytes(int hd, int G, int nstages) { return AttnSmem{hd, G, nstages}.total(); }
 
+// DL consecutive bf16 of one cached row, as raw bits (DL = 2 or 4).
+template <int DL>
+struct RowSlice {
+  uint32_t w[DL / 2];
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    if (DL == 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x;
+      w[DL / 2 - 1] = v.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+  }
+  __device__ __forceinline__ void unpack(float* f) const {
+#pragma unroll
+    for (int i = 0; i < DL / 2; ++i) {
+      f[2 * i] = bf16lo(w[i]);
+      f[2 * i + 1] = bf16hi(w[i]);
+    }
+  }
+};
+
 template <int HD, int G>
-__global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
-  constexpr int CH = 8192 / (HD * 2);  // positions per chunk (8 KB of K)
+__global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);  // positions per chunk (16 KB of K)
   constexpr int PW = CH / kConsumerWarps;  // positions per warp per chunk
+  constexpr int SUB = 4;                   // positions per online-softmax update
   constexpr int DL = HD / 32;          // dims per lane
   constexpr int NC = kConsumerWarps * 32;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -350,11 +443,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off());
   uint64_t* empty = full + p.nstages;
   float* ws = reinterpret_cast<float*>(smem + L.ws_off());    // [warp][G][HD+2]
-  float* seg = reinterpret_cast<float*>(smem + L.seg_off());  // [G][HD+2]
-  int* flag = reinterpret_cast<int*>(smem + L.flag_off());
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = gridDim.x, b = blockIdx.x;
+  if (tid == 0) tl_mark_min(p.tl, 0);
   // The step position is read before griddepcontrol.wait: it was last written by
   // the previous step's final kernel, and this kernel can only launch after the
   // preceding kernel's CTAs have all passed their own wait, i.e. after that
@@ -378,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
   if (warp == kConsumerWarps) {
     if (lane == 0) {
       bool waited = false;
+      int g = (int)(u0 / cph), c = (int)(u0 - (int64_t)g * cph);
+      const uint64_t pol_stream = policy_evict_first();
+      int slot = 0, phase = 0;
       for (int s = 0; s < nu; ++s) {
-        const int slot = s % p.nstages;
-        if (s >= p.nstages && !mbar_wait(&empty[slot], ((s / p.nstages) - 1) & 1)) {
+        if (s >= p.nstages && !mbar_wait(&empty[slot], phase ^ 1)) {
           raise_error(p.err, ERR_EMPTY_WAIT);
           break;
         }
-        const int64_t u = u0 + s;
-        const int g = (int)(u / cph), c = (int)(u - (int64_t)g * cph);
         const int rows = min(CH, n - c * CH);
         if (c == cph - 1 && !waited) {  // this chunk holds the row appended by K1
           pdl_wait();
@@ -394,9 +486,17 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
         const size_t off = ((size_t)g * p.max_ctx + (size_t)c * CH) * HD;
         const uint32_t bytes = (uint32_t)rows * HD * 2;
         mbar_arrive_expect_tx(&full[slot], 2 * bytes);
-        uint8_t* dst = stages + (size_t)slot * 16384;
-        bulk_g2s(dst, p.kc + off, bytes, &full[slot]);
-        bulk_g2s(dst + 8192, p.vc + off, bytes, &full[slot]);
+        uint8_t* dst = stages + (size_t)slot * kAttnStageBytes;
+        bulk_g2s_hint(dst, p.kc + off, bytes, &full[slot], pol_stream);
+        bulk_g2s_hint(dst + kAttnStageBytes / 2, p.vc + off, bytes, &full[slot], pol_stream);
+        if (++c == cph) {
+          c = 0;
+          ++g;
+        }
+        if (++slot == p.nstages) {
+          slot = 0;
+          phase ^= 1;
+        }
       }
     }
     return;
@@ -404,6 +504,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
 
   pdl_wait();  // q comes from K1
   pdl_trigger();
+  if (tid == 0) {
+    tl_mark_min(p.tl, 2);
+    tl_mark_max(p.tl, 3);
+  }
   float m[G], l[G], acc[G][DL];
   int cur_g = -1, seg_idx = 0;
   auto reset = [&]() {
@@ -416,7 +520,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
     }
   };
   float qr[G][DL];
-  // Ends the segment of KV head g: merge warps, then finish or publish.
+  // Ends the segment of KV head g: merge the warps' states; a head this CTA
+  // covered whole is normalised into o, a split head leaves a partial record
+  // (acc, m, l), merged after the loop by the last CTA of the head to finish.
+  int split_heads[2] = {-1, -1};
   auto end_segment = [&](int g) {
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
@@ -429,6 +536,10 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
       }
     }
     named_barrier(1, NC);
+    const int64_t h0 = (int64_t)g * cph, h1 = h0 + cph;
+    const bool whole = h0 >= u0 && h1 <= u1;
+    if (!whole) split_heads[seg_idx == 0 ? 0 : 1] = g;
+    float* rec = p.part + ((size_t)b * 2 + (seg_idx == 0 ? 0 : 1)) * G * (HD + 4);
     for (int i = tid; i < G * HD; i += NC) {
       const int gg = i / HD, j = i % HD;
       float M = -INFINITY;
@@ -440,71 +551,27 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
         A += wr[j] * e;
         Ls += wr[HD + 1] * e;
       }
-      seg[gg * (HD + 2) + j] = A;
-      if (j == 0) {
-        seg[gg * (HD + 2) + HD] = M;
-        seg[gg * (HD + 2) + HD + 1] = Ls;
-      }
-    }
-    named_barrier(1, NC);
-    const int64_t h0 = (int64_t)g * cph, h1 = h0 + cph;
-    if (h0 >= u0 && h1 <= u1) {  // whole head in this CTA
-      for (int i = tid; i < G * HD; i += NC) {
-        const int gg = i / HD, j = i % HD;
-        p.o[(size_t)(g * G + gg) * HD + j] = seg[gg * (HD + 2) + j] / seg[gg * (HD + 2) + HD + 1];
-      }
-    } else {
-      const int side = seg_idx == 0 ? 0 : 1;
-      float* mine = p.part + ((size_t)b * 2 + side) * G * (HD + 2);
-      for (int i = tid; i < G * (HD + 2); i += NC) mine[i] = seg[i];
-      __threadfence();
-      named_barrier(1, NC);
-      if (tid == 0) {
-        const int c_lo = split_owner(U, nb, h0), c_hi = split_owner(U, nb, h1 - 1);
-        int expected = 0;
-        for (int c = c_lo; c <= c_hi; ++c)
-          expected += split_begin(U, nb, c + 1) > split_begin(U, nb, c);
-        const int prev = atomicAdd(&p.counters[g], 1);
-        *flag = (prev == expected - 1);
-        if (*flag) __threadfence();
-      }
-      named_barrier(1, NC);
-      if (*flag) {
-        const int c_lo = split_owner(U, nb, h0), c_hi = split_owner(U, nb, h1 - 1);
-        for (int i = tid; i < G * HD; i += NC) {
-          const int gg = i / HD, j = i % HD;
-          float M = -INFINITY;
-          for (int c = c_lo; c <= c_hi; ++c) {
-            const int64_t cs = split_begin(U, nb, c), ce = split_begin(U, nb, c + 1);
-            if (ce <= cs) continue;
-            const int sd = (cs >= h0) ? 0 : 1;
-            M = fmaxf(M, __ldcg(p.part + (((size_t)c * 2 + sd) * G + gg) * (HD + 2) + HD));
-          }
-          float A = 0.f, Ls = 0.f;
-          for (int c = c_lo; c <= c_hi; ++c) {
-            const int64_t cs = split_begin(U, nb, c), ce = split_begin(U, nb, c + 1);
-            if (ce <= cs) continue;
-            const int sd = (cs >= h0) ? 0 : 1;
-            const float* pr = p.part + (((size_t)c * 2 + sd) * G + gg) * (HD + 2);
-            const float e = expf(__ldcg(pr + HD) - M);
-            A += __ldcg(pr + j) * e;
-            Ls += __ldcg(pr + HD + 1) * e;
-          }
-          p.o[(size_t)(g * G + gg) * HD + j] = A / Ls;
+      if (whole) {
+        p.o[(size_t)(g * G + gg) * HD + j] = A / Ls;
+      } else {
+        rec[gg * (HD + 4) + j] = A;
+        if (j == 0) {
+          rec[gg * (HD + 4) + HD] = M;
+          rec[gg * (HD + 4) + HD + 1] = Ls;
         }
-        if (tid == 0) p.counters[g] = 0;
       }
     }
+    // The records are released to the other CTAs by the ticket below: this
+    // barrier orders every thread's writes before thread 0's gpu-scope release.
     named_barrier(1, NC);
     ++seg_idx;
   };
 
   reset();
   bool ok = true;
+  int g = (int)(u0 / cph), c = (int)(u0 - (int64_t)g * cph);
+  int slot = 0, phase = 0;
   for (int s = 0; s < nu; ++s) {
-    const int slot = s % p.nstages;
-    const int64_t u = u0 + s;
-    const int g = (int)(u / cph), c = (int)(u - (int64_t)g * cph);
     if (g != cur_g) {
       if (cur_g >= 0) {
         end_segment(cur_g);
@@ -516,73 +583,155 @@ __global__ void __launch_bounds__(kThreads, 2) attn_decode(const AttnParams p) {
 #pragma unroll
         for (int j = 0; j < DL; ++j) qr[gg][j] = p.q[(size_t)(g * G + gg) * HD + lane * DL + j] * p.scale;
     }
-    if (ok && !mbar_wait(&full[slot], (s / p.nstages) & 1)) {
+    if (ok && !mbar_wait(&full[slot], phase)) {
       raise_error(p.err, ERR_FULL_WAIT);
       ok = false;  // keep the control flow (segment barriers) uniform
     }
+    if (s == 0 && tid == 0) tl_mark_max(p.tl, 4);
     const int rows = min(CH, n - c * CH);
-    const uint8_t* kb = stages + (size_t)slot * 16384;
-    const uint8_t* vb = kb + 8192;
-    float sc[PW][G];
+    const uint8_t* kb = stages + (size_t)slot * kAttnStageBytes;
+    const uint8_t* vb = kb + kAttnStageBytes / 2;
+    // This warp's K and V row slices into registers, then the slot goes back.
+    RowSlice<DL> kr[PW], vr[PW];
 #pragma unroll
     for (int i = 0; i < PW; ++i) {
       const int t = warp + i * kConsumerWarps;
-      float kv[DL];
       if (t < rows) {
-        if (DL == 4) {
-          const uint2 w2 = *reinterpret_cast<const uint2*>(kb + ((size_t)t * HD + lane * 4) * 2);
-          kv[0] = bf16lo(w2.x); kv[1] = bf16hi(w2.x); kv[2] = bf16lo(w2.y); kv[3] = bf16hi(w2.y);
-        } else {
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(kb + ((size_t)t * HD + lane * 2) * 2);
-          kv[0] = bf16lo(w1); kv[1] = bf16hi(w1);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < DL; ++j) kv[j] = 0.f;
+        kr[i].load(kb + ((size_t)t * HD + lane * DL) * 2);
+        vr[i].load(vb + ((size_t)t * HD + lane * DL) * 2);
       }
-#pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        float d = 0.f;
-#pragma unroll
-        for (int j = 0; j < DL; ++j) d = fmaf(qr[gg][j], kv[j], d);
-        d = warp_sum(d);
-        sc[i][gg] = (t < rows) ? d : -INFINITY;
-      }
-    }
-#pragma unroll
-    for (int gg = 0; gg < G; ++gg) {
-      float mx = m[gg];
-#pragma unroll
-      for (int i = 0; i < PW; ++i) mx = fmaxf(mx, sc[i][gg]);
-      if (mx == -INFINITY) continue;  // this warp has no position in the chunk
-      const float alpha = (m[gg] == -INFINITY) ? 0.f : expf(m[gg] - mx);
-      float ls = l[gg] * alpha;
-#pragma unroll
-      for (int j = 0; j < DL; ++j) acc[gg][j] *= alpha;
-#pragma unroll
-      for (int i = 0; i < PW; ++i) {
-        const int t = warp + i * kConsumerWarps;
-        if (t >= rows) continue;
-        const float pi = expf(sc[i][gg] - mx);
-        ls += pi;
-        float vv[DL];
-        if (DL == 4) {
-          const uint2 w2 = *reinterpret_cast<const uint2*>(vb + ((size_t)t * HD + lane * 4) * 2);
-          vv[0] = bf16lo(w2.x); vv[1] = bf16hi(w2.x); vv[2] = bf16lo(w2.y); vv[3] = bf16hi(w2.y);
-        } else {
-          const uint32_t w1 = *reinterpret_cast<const uint32_t*>(vb + ((size_t)t * HD + lane * 2) * 2);
-          vv[0] = bf16lo(w1); vv[1] = bf16hi(w1);
-        }
-#pragma unroll
-        for (int j = 0; j < DL; ++j) acc[gg][j] = fmaf(pi, vv[j], acc[gg][j]);
-      }
-      m[gg] = mx;
-      l[gg] = ls;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
+#pragma unroll
+    for (int i0 = 0; i0 < PW; i0 += SUB) {
+      if (warp + i0 * kConsumerWarps >= rows) break;  // warp-uniform
+      float sc[SUB][G];
+#pragma unroll
+      for (int i = 0; i < SUB; ++i) {
+        const int t = warp + (i0 + i) * kConsumerWarps;
+        float kv[DL];
+        kr[i0 + i].unpack(kv);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          float d = 0.f;
+#pragma unroll
+          for (int j = 0; j < DL; ++j) d = fmaf(qr[gg][j], kv[j], d);
+          d = warp_sum(d);
+          sc[i][gg] = (t < rows) ? d : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float mx = m[gg];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) mx = fmaxf(mx, sc[i][gg]);
+        const float alpha = (m[gg] == -INFINITY) ? 0.f : expf(m[gg] - mx);
+        float ls = l[gg] * alpha;
+#pragma unroll
+        for (int j = 0; j < DL; ++j) acc[gg][j] *= alpha;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+          const int t = warp + (i0 + i) * kConsumerWarps;
+          if (t >= rows) continue;
+          const float pi = expf(sc[i][gg] - mx);
+          ls += pi;
+          float vv[DL];
+          vr[i0 + i].unpack(vv);
+#pragma unroll
+          for (int j = 0; j < DL; ++j) acc[gg][j] = fmaf(pi, vv[j], acc[gg][j]);
+        }
+        m[gg] = mx;
+        l[gg] = ls;
+      }
+    }
+    if (++c == cph) {
+      c = 0;
+      ++g;
+    }
+    if (++slot == p.nstages) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+  if (tid == 0) {
+    tl_mark_min(p.tl, 5);
+    tl_mark_max(p.tl, 6);
   }
   if (cur_g >= 0) end_segment(cur_g);
+
+  // ---- heads split over CTAs: the last CTA to finish merges them --------------
+  // (tickets are taken after this CTA's whole loop, so merging never stalls it;
+  // the split arithmetic is 32-bit: units * grid stays far below 2^31)
+  int* mbase = reinterpret_cast<int*>(smem + L.merge_off());  // [kMaxSplits] record offset
+  int* todo = mbase + kMaxSplits;                              // [2]
+  const int U32 = (int)U;
+  auto part_begin = [&](int c) { return split_begin32(U32, nb, c); };
+  if (tid == 0) {
+    int prev[2] = {0, 0}, expected[2] = {0, 0};
+    for (int i = 0; i < 2; ++i) {
+      const int g = split_heads[i];
+      if (g < 0) continue;
+      const int c_lo = split_owner32(U32, nb, g * cph), c_hi = split_owner32(U32, nb, (g + 1) * cph - 1);
+      for (int c = c_lo; c <= c_hi; ++c) expected[i] += part_begin(c + 1) > part_begin(c);
+      // release this CTA's record, acquire the others'
+      prev[i] = atomic_add_acq_rel(&p.counters[g], 1);
+    }
+    for (int i = 0; i < 2; ++i)
+      todo[i] = (split_heads[i] >= 0 && prev[i] == expected[i] - 1) ? split_heads[i] : -1;
+  }
+  named_barrier(1, NC);
+  for (int i = 0; i < 2; ++i) {
+    const int g = todo[i];
+    if (g < 0) continue;
+    const int h0 = g * cph;
+    const int c_lo = split_owner32(U32, nb, h0), c_hi = split_owner32(U32, nb, h0 + cph - 1);
+    const int S = min(c_hi - c_lo + 1, kMaxSplits);
+    if (tid == 0 && c_hi - c_lo + 1 > kMaxSplits) raise_error(p.err, ERR_SPLITS);
+    // record offset of every split
+    for (int sp = tid; sp < S; sp += NC) {
+      const int c = c_lo + sp, cs = part_begin(c);
+      mbase[sp] = part_begin(c + 1) > cs ? ((c * 2 + (cs >= h0 ? 0 : 1)) * G) * (HD + 4) : -1;
+    }
+    named_barrier(1, NC);
+    // one round trip: each output loads every split's (m, l, acc) at once
+    for (int t = tid; t < G * HD; t += NC) {
+      const int gg = t / HD, j = t - gg * HD;
+      float mv[kMaxSplits], lv[kMaxSplits], av[kMaxSplits];
+      float M = -INFINITY;
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        mv[sp] = -INFINITY;
+        lv[sp] = 0.f;
+        av[sp] = 0.f;
+        if (sp < S && mbase[sp] >= 0) {
+          const float* rec = p.part + mbase[sp] + gg * (HD + 4);
+          mv[sp] = __ldcg(rec + HD);
+          lv[sp] = __ldcg(rec + HD + 1);
+          av[sp] = __ldcg(rec + j);
+        }
+      }
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) M = fmaxf(M, mv[sp]);
+      float Lsum = 0.f, o = 0.f;
+#pragma unroll
+      for (int sp = 0; sp < kMaxSplits; ++sp) {
+        const float e = (mv[sp] == -INFINITY) ? 0.f : expf(mv[sp] - M);
+        Lsum = fmaf(lv[sp], e, Lsum);
+        o = fmaf(av[sp], e, o);
+      }
+      p.o[(size_t)(g * G + gg) * HD + j] = o / Lsum;
+    }
+    if (tid == 0) p.counters[g] = 0;
+    named_barrier(1, NC);
+  }
+  if (p.tl) {
+    named_barrier(1, NC);
+    if (tid == 0) {
+      tl_mark_max(p.tl, 1);
+      tl_mark_min(p.tl, 7);
+    }
+  }
   if (!ok) {
     for (int s = 0; s < nu && s < p.nstages; ++s) {
       const int last = s + ((nu - 1 - s) / p.nstages) * p.nstages;
@@ -626,7 +775,8 @@ cudaError_t set_smem_limits() {
   return cudaSuccess;
 }
 
-static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s) {
+static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s,
+                              bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -636,26 +786,26 @@ static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 cudaError_t launch_gemv(int pro, int epi, const GemvParams& p, int grid, size_t smem,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool pdl) {
   const void* fn = gemv_kernel_ptr(pro, epi);
   if (!fn) return cudaErrorInvalidValue;
   GemvParams copy = p;
   void* args[] = {&copy};
-  return launch_pdl(fn, args, grid, smem, s);
+  return launch_pdl(fn, args, grid, smem, s, pdl);
 }
 
 cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
-                        cudaStream_t s) {
+                        cudaStream_t s, bool pdl) {
   const void* fn = attn_kernel_ptr(hd, G);
   if (!fn) return cudaErrorInvalidValue;
   AttnParams copy = p;
   void* args[] = {&copy};
-  return launch_pdl(fn, args, grid, smem, s);
+  return launch_pdl(fn, args, grid, smem, s, pdl);
 }
 
 // ---- load-time repack ------------------------------------------------------------

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtld_gb300.so")
 DEC_OK, DEC_ERR_ARG, DEC_ERR_SHAPE, DEC_ERR_STATE = 0, -1, -2, -3
 DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6, -7, -8
 DEC_W_BF16, DEC_W_Q4B32 = 0, 1
-DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH = 0, 1, 2
+DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL = 0, 1, 2, 4
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
@@ -27,7 +27,7 @@ KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
                 "norm_gateup_swiglu", "down_residual")
 
 EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_truncate_kv", "dec_step",
-            "dec_set_tap", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
+            "dec_set_tap", "dec_set_timeline", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
             "dec_destroy", "dec_last_error")
 
 
@@ -73,6 +73,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dec_truncate_kv": [vp, i32],
         "dec_step": [vp, vp, i32, vp, vp],
         "dec_set_tap": [vp, vp, vp, vp],
+        "dec_set_timeline": [vp, vp],
         "dec_sync_status": [vp, vp],
         "dec_get_info": [vp, ctypes.POINTER(Info)],
         "dec_launch_kernel": [vp, i32, i32, i32, vp],
@@ -135,10 +136,12 @@ class Shape:
 class Decoder:
     """One decode handle: weights, KV cache and the captured step graph."""
 
-    def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True):
+    def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True,
+                 pdl: bool = True):
         self.lib = load_library()
         self.shape = shape
-        flags = (DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
+        flags = ((DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
+                 | (0 if pdl else DEC_NO_PDL))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
                               shape.max_ctx, shape.weight_fmt, flags)
@@ -167,6 +170,9 @@ class Decoder:
 
     def set_tap(self, per_layer_out=None, qact=None, qscale=None):
         self._check(self.lib.dec_set_tap(self.h, _ptr(per_layer_out), _ptr(qact), _ptr(qscale)))
+
+    def set_timeline(self, buf=None):
+        self._check(self.lib.dec_set_timeline(self.h, _ptr(buf)))
 
     def sync_status(self, stream=None):
         self._check(self.lib.dec_sync_status(self.h, _stream_handle(stream)))
