@@ -169,6 +169,38 @@ int dec_get_info(const dec_handle* h, dec_info* info);
  * dec_step overwrites whatever these launches wrote. */
 int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream);
 
+/* Decode attention without any allocation, for callers that cannot call
+ * cudaMalloc: code whose device memory all belongs to another allocator (a
+ * framework's caching pool, a pre-sized arena) or that runs under a rule of no
+ * allocation after start-up, since cudaMalloc can block until the device is
+ * idle and fragments memory the caller manages.  The pages describe no such
+ * call; it is an addition of this library.
+ *
+ * Runs the same split-KV GQA attention kernel as dec_step for one token:
+ * q: device fp32 [n_q_heads][head_dim], already rotated by RoPE;
+ * k_cache, v_cache: device bf16 [n_kv_heads][ctx_stride][head_dim] (16-byte
+ * aligned); rows 0..n-1 of every KV head are attended (1 <= n <= ctx_stride);
+ * o: device fp32 [n_q_heads][head_dim], softmax(q.K^T / sqrt(head_dim)) V with
+ * query head h reading KV head floor(h * n_kv_heads / n_q_heads).
+ * Queued on `stream`; returns after enqueue.
+ *
+ * Scratch: one file-scope device array of about 1 MiB (partial records of
+ * heads split over CTAs, per-head counters, the position, an error flag),
+ * which every GPU that loads the library holds until the process exits.  The
+ * first call on each device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and sets the kernels' shared-memory
+ * limits; make that first call before any stream capture.  Every call shares
+ * the array and clears what must start at zero, so calls whose work overlaps
+ * on the GPU (other streams, other threads) race and must be serialised by
+ * the caller.  Limits: head_dim 64 or 128, n_kv_heads <= 64, n_q_heads /
+ * n_kv_heads in {1, 2, 4, 8}, the records of one call within the array (a
+ * call that would exceed it returns DEC_ERR_SHAPE), ctx_stride <= 65536.
+ * Returns DEC_ERR_ARG / DEC_ERR_SHAPE for bad arguments (nothing is queued)
+ * and DEC_ERR_CUDA if a launch fails. */
+int dec_attention_noalloc(const float* q, const void* k_cache, const void* v_cache, int n_q_heads,
+                          int n_kv_heads, int head_dim, int ctx_stride, int n, float* o,
+                          dec_stream_t stream);
+
 /* Frees every device buffer and the graph; accepts NULL and partially
  * created handles.  Waits for the device first. */
 int dec_destroy(dec_handle* h);

@@ -1,0 +1,111 @@
+// dec_attention_noalloc: the split-KV decode attention kernel for callers that
+// must not allocate device memory.  Its scratch (the per-CTA partial records,
+// the per-head arrival counters, the step position and the error flag) lives
+// in one file-scope __device__ array instead of a cudaMalloc'd workspace.
+#include <cmath>
+#include <cstdio>
+
+#include "../../include/dec.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace tld;
+
+namespace {
+
+// Limits of the fixed scratch.
+constexpr int kNoAllocRecordFloats = 1 << 18;  // 1 MiB of partial records
+constexpr int kNoAllocMaxKvHeads = 64;
+constexpr int kNoAllocMaxDevices = 64;
+
+struct NoAllocScratch {
+  float records[kNoAllocRecordFloats];
+  int counters[kNoAllocMaxKvHeads];
+  int pos;
+  int err;
+};
+
+// Every GPU that loads the library holds this array until the process exits.
+static __device__ __align__(256) NoAllocScratch g_noalloc_scratch;
+
+// Per-device set-up, done by the first call on each device.
+struct DeviceSetup {
+  bool done;
+  NoAllocScratch* scratch;  // device address of g_noalloc_scratch
+  int n_sm;
+};
+DeviceSetup g_setup[kNoAllocMaxDevices];
+
+// Clears the counters and the error flag and stores the position of this call.
+__global__ void noalloc_prepare(NoAllocScratch* s, int pos, int n_counters) {
+  for (int i = threadIdx.x; i < n_counters; i += blockDim.x) s->counters[i] = 0;
+  if (threadIdx.x == 0) {
+    s->pos = pos;
+    s->err = 0;
+  }
+}
+
+}  // namespace
+
+extern "C" int dec_attention_noalloc(const float* q, const void* k_cache, const void* v_cache,
+                                     int n_q_heads, int n_kv_heads, int head_dim, int ctx_stride,
+                                     int n, float* o, dec_stream_t stream) {
+  if (!q || !k_cache || !v_cache || !o) return DEC_ERR_ARG;
+  if (head_dim != 64 && head_dim != 128) return DEC_ERR_SHAPE;
+  if (n_kv_heads < 1 || n_kv_heads > kNoAllocMaxKvHeads || n_q_heads < 1 ||
+      n_q_heads % n_kv_heads)
+    return DEC_ERR_SHAPE;
+  const int G = n_q_heads / n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return DEC_ERR_SHAPE;
+  if (ctx_stride < 1 || ctx_stride > 65536 || n < 1 || n > ctx_stride) return DEC_ERR_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache)) & 15)
+    return DEC_ERR_ARG;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices)
+    return DEC_ERR_CUDA;
+  DeviceSetup& su = g_setup[dev];
+  if (!su.done) {
+    // With this device current: the device address of the scratch array (the
+    // host-side symbol is only a stand-in), the SM count, and the kernels'
+    // shared-memory limits.  Nothing here allocates.
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return DEC_ERR_CUDA;
+    int n_sm = 0;
+    if (cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DEC_ERR_CUDA;
+    if (set_smem_limits() != cudaSuccess) return DEC_ERR_CUDA;
+    su.scratch = static_cast<NoAllocScratch*>(ptr);
+    su.n_sm = n_sm;
+    su.done = true;
+  }
+
+  // Same grid and ring as the decoder's attention launch.
+  const int grid = su.n_sm < (kMaxSplits - 1) * n_kv_heads ? su.n_sm : (kMaxSplits - 1) * n_kv_heads;
+  if ((size_t)grid * 2 * G * (head_dim + 4) > (size_t)kNoAllocRecordFloats) return DEC_ERR_SHAPE;
+  const size_t fixed = attn_smem_bytes(head_dim, G, 0);
+  int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
+  ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  noalloc_prepare<<<1, 64, 0, s>>>(su.scratch, n - 1, n_kv_heads);
+  if (cudaGetLastError() != cudaSuccess) return DEC_ERR_CUDA;
+
+  AttnParams p{};
+  p.kc = static_cast<const uint16_t*>(k_cache);
+  p.vc = static_cast<const uint16_t*>(v_cache);
+  p.q = q;
+  p.o = o;
+  p.part = su.scratch->records;
+  p.counters = su.scratch->counters;
+  p.pos = &su.scratch->pos;
+  p.err = &su.scratch->err;
+  p.nkv = n_kv_heads;
+  p.max_ctx = ctx_stride;
+  p.nstages = ns;
+  p.scale = (float)(1.0 / std::sqrt((double)head_dim));
+  p.tl = nullptr;
+  if (launch_attn(head_dim, G, p, grid, attn_smem_bytes(head_dim, G, ns), s, false) != cudaSuccess)
+    return DEC_ERR_CUDA;
+  return DEC_OK;
+}

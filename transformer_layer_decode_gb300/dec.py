@@ -28,7 +28,7 @@ KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
 
 EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_truncate_kv", "dec_step",
             "dec_set_tap", "dec_set_timeline", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
-            "dec_destroy", "dec_last_error")
+            "dec_destroy", "dec_last_error", "dec_attention_noalloc")
 
 
 class DecError(RuntimeError):
@@ -78,6 +78,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dec_get_info": [vp, ctypes.POINTER(Info)],
         "dec_launch_kernel": [vp, i32, i32, i32, vp],
         "dec_destroy": [vp],
+        "dec_attention_noalloc": [vp, vp, vp, i32, i32, i32, i32, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -117,6 +118,16 @@ def _stream_handle(stream) -> int | None:
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+def attention_noalloc(q, k_cache, v_cache, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                      ctx_stride: int, n: int, o, stream=None):
+    """Decode attention through dec_attention_noalloc (no device allocation)."""
+    L = load_library()
+    rc = L.dec_attention_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), n_q_heads, n_kv_heads,
+                                 head_dim, ctx_stride, n, _ptr(o), _stream_handle(stream))
+    if rc != DEC_OK:
+        raise DecError(rc, "dec_attention_noalloc rejected its arguments or failed to launch")
 
 
 @dataclass
