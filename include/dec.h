@@ -142,6 +142,15 @@ int dec_step(dec_handle* h, const float* token_embedding, int pos, float* out_hi
  * discards the captured graph; it is recaptured at the next step. */
 int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qscale_tap);
 
+/* Integer block-dot tap (fused plan, DEC_W_Q4B32): at the next steps, the
+ * GEMV of `kernel` (0 = QKV, 2 = o-proj, 3 = gate/up, 4 = down) in `layer`
+ * writes every int32 block dot sum_{i<32} q_w * q_x into dots, device int32
+ * [rows][K/32], rows in the library's tiled order (QKV: q heads then k heads
+ * with dims (i, i + head_dim/2) adjacent, then v; gate/up: gate and up rows
+ * alternating).  NULL turns it off.  Discards the captured graph.  For the
+ * bit-exact check of the integer path against the int8 input tap. */
+int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots);
+
 /* GPU timeline probe of the fused plan (NULL turns it off): buf is device
  * uint64 [kernels_per_token][8]; at every step, launch i (layer * 5 + kernel)
  * records, in %globaltimer nanoseconds as atomic min / max: [0] earliest CTA

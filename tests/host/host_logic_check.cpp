@@ -38,7 +38,7 @@ static void check_split(int64_t total, int parts) {
 }
 
 static void check_tiled(int N, int K) {
-  const int ktiles = (K + kTileK - 1) / kTileK;
+  const TileGeom g = tile_geom(K, false);
   std::vector<int> seen((size_t)N * K, 0);
   for (int r = 0; r < N; ++r)
     for (int k = 0; k < K; ++k) {
@@ -48,19 +48,50 @@ static void check_tiled(int N, int K) {
     }
   for (size_t i = 0; i < seen.size(); ++i) CHECK(seen[i] == 1, "bijective at %zu (N=%d K=%d)", i, N, K);
   // tile t starts where tiled_elem_offset puts its first element; ranges are 16-byte multiples
-  const int64_t ntiles = (int64_t)(N / kTileR) * ktiles;
+  const int64_t ntiles = (int64_t)(N / kTileR) * g.ktiles;
   for (int64_t t = 0; t <= ntiles; ++t) {
-    const int64_t off = tile_byte_offset(t, ktiles, K);
+    const int64_t off = tile_byte_offset(t, g);
     CHECK(off % 16 == 0, "tile offset alignment");
     if (t < ntiles) {
-      const int64_t rb = t / ktiles, kt = t % ktiles;
+      const int64_t rb = t / g.ktiles, kt = t % g.ktiles;
       CHECK(off == 2 * tiled_elem_offset(rb * kTileR, kt * kTileK, K), "tile start");
     }
   }
-  CHECK(tile_byte_offset(ntiles, ktiles, K) == 2LL * N * K, "total bytes");
+  CHECK(tile_byte_offset(ntiles, g) == 2LL * N * K, "total bytes");
   for (int64_t a = 0; a + kStageTiles <= ntiles; a += 7) {
-    const int64_t bytes = tile_byte_offset(a + kStageTiles, ktiles, K) - tile_byte_offset(a, ktiles, K);
+    const int64_t bytes = tile_byte_offset(a + kStageTiles, g) - tile_byte_offset(a, g);
     CHECK(bytes <= kStageBytes && bytes % 16 == 0, "stage bytes %ld", (long)bytes);
+  }
+}
+
+// q4: every nibble byte and every scale lands on a distinct byte of the
+// matrix; each tile is 16-byte aligned and stages fit the q4 stage size.
+static void check_tiled_q4(int N, int K) {
+  const TileGeom g = tile_geom(K, true);
+  const int64_t total = (int64_t)(N / kTileR) * g.rb_bytes;
+  CHECK(total == (int64_t)N * (K / 2 + K / 16), "q4 bytes");
+  std::vector<int> seen((size_t)total, 0);
+  for (int r = 0; r < N; ++r) {
+    for (int c2 = 0; c2 < K / 2; ++c2) {
+      const int64_t o = q4_nibble_byte(r, c2, K);
+      CHECK(o >= 0 && o < total, "q4 nibble range");
+      if (o >= 0 && o < total) seen[o]++;
+    }
+    for (int b = 0; b < K / 32; ++b) {
+      const int64_t o = q4_scale_byte(r, b, K);
+      CHECK(o >= 0 && o + 1 < total && o % 2 == 0, "q4 scale range");
+      if (o >= 0 && o + 1 < total) {
+        seen[o]++;
+        seen[o + 1]++;
+      }
+    }
+  }
+  for (size_t i = 0; i < seen.size(); ++i) CHECK(seen[i] == 1, "q4 bijective at %zu (K=%d)", i, K);
+  const int64_t ntiles = (int64_t)(N / kTileR) * g.ktiles;
+  for (int64_t t = 0; t <= ntiles; ++t) CHECK(tile_byte_offset(t, g) % 16 == 0, "q4 tile alignment");
+  for (int64_t a = 0; a + kStageTiles <= ntiles; a += 3) {
+    const int64_t bytes = tile_byte_offset(a + kStageTiles, g) - tile_byte_offset(a, g);
+    CHECK(bytes <= kStageBytesQ4 && bytes % 16 == 0, "q4 stage bytes %ld", (long)bytes);
   }
 }
 
@@ -69,6 +100,7 @@ int main() {
     for (int parts : {1, 5, 148, 152, 160}) check_split(total, parts);
   for (int K : {8, 264, 512, 1000, 1408, 2048, 4096}) check_tiled(16, K);
   check_tiled(64, 11008);
+  for (int K : {64, 512, 1408, 2048, 4096, 11008}) check_tiled_q4(8, K);
   std::printf(fails ? "FAILED %d\n" : "OK\n", fails);
   return fails ? 1 : 0;
 }

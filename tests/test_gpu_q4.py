@@ -1,0 +1,127 @@
+"""GPU parity of the int4-weight / int8-activation path.
+
+- every layer's output against the fp64 oracle (same float tolerance);
+- the integer block dots bit-exact: the GPU's own int8 GEMV inputs (activation
+  tap) and the int4 weights give, in int64 on the CPU, exactly the int32 dots
+  the GPU kernels computed (block-dot tap), for all four projections;
+- the GPU's int8 activations against the oracle's quantisation of the same
+  layer input: equal up to +-1 where fp32 and fp64 straddle a rounding boundary.
+"""
+import numpy as np
+import pytest
+
+from harness import assert_close, oracle_stack, run_gpu, run_oracle
+from oracle import oracle as orc
+from transformer_layer_decode_gb300 import dec, synth, workload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+SMALL = {
+    "q4_gqa4_d64": synth.Workload("q4_gqa4_d64", 2, 512, 8, 2, 64, 1408, prefill=100, steps=3,
+                                  weight_fmt="q4"),
+    "q4_mha_d128": synth.Workload("q4_mha_d128", 2, 1024, 8, 8, 128, 2816, prefill=70, steps=2,
+                                  weight_fmt="q4"),
+    "q4_ragged_empty": synth.Workload("q4_ragged_empty", 1, 1088, 16, 4, 64, 1216, prefill=0,
+                                      steps=2, weight_fmt="q4"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused"])
+def test_q4_layers_match_oracle(name, mode):
+    w = SMALL[name]
+    max_ctx = w.prefill + w.steps + 2
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=(mode == "unfused"),
+                                    graph=(mode != "fused_eager"), keep_host=True)
+    xs = workload.step_inputs(w, w.steps)
+    got = run_gpu(d, w, xs)
+    d.close()
+    ref = run_oracle(oracle_stack(w, host, max_ctx), w, xs)
+    for s in range(w.steps):
+        for l in range(w.n_layers):
+            assert_close(got[s, l], ref[s, l], f"{name} {mode} step {s} layer {l}")
+
+
+def _tiled_to_abi(w, kernel):
+    """(tensor id, ABI row) of every tiled row of a fused GEMV."""
+    hd, nq, nkv = w.head_dim, w.n_q_heads, w.n_kv_heads
+    out = []
+    if kernel == 0:
+        for sec, t, heads in ((0, synth.T_WQ, nq), (1, synth.T_WK, nkv)):
+            for R in range(heads * hd):
+                head, j = divmod(R, hd)
+                out.append((t, head * hd + (j // 2 if j % 2 == 0 else j // 2 + hd // 2)))
+        out += [(synth.T_WV, r) for r in range(nkv * hd)]
+    elif kernel == 3:
+        for R in range(2 * w.ffn):
+            out.append((synth.T_WGATE if R % 2 == 0 else synth.T_WUP, R // 2))
+    else:
+        t = synth.T_WO if kernel == 2 else synth.T_WDOWN
+        out += [(t, r) for r in range(w.shape(t)[0])]
+    return out
+
+
+@pytest.mark.parametrize("kernel", [0, 2, 3, 4])
+def test_q4_integer_block_dots_bit_exact(kernel):
+    w = SMALL["q4_gqa4_d64"]
+    layer = 1
+    max_ctx = w.prefill + 3
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True)
+    km = max(w.hidden, w.ffn, w.n_q_heads * w.head_dim)
+    qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
+    qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")
+    K = {0: w.hidden, 2: w.n_q_heads * w.head_dim, 3: w.hidden, 4: w.ffn}[kernel]
+    rows = _tiled_to_abi(w, kernel)
+    dots = torch.full((len(rows), K // 32), -2**31, dtype=torch.int32, device="cuda")
+    d.set_tap(None, qact, qsc)
+    d.set_dot_tap(layer, kernel, dots)
+    emb = torch.from_numpy(synth.step_input(w, 0)).cuda()
+    out = torch.empty_like(emb)
+    d.step(emb, w.prefill, out)
+    d.sync_status()
+    d.close()
+    slot = {0: 0, 2: 1, 3: 2, 4: 3}[kernel]
+    qx = qact[layer, slot, :K].cpu().numpy()
+    gpu = dots.cpu().numpy().astype(np.int64)
+    lw = host["layers"][layer]
+    by_tensor = {}
+    for t in {t for t, _ in rows}:
+        packed, _ = lw.q4[t]
+        by_tensor[t] = orc.q4_blockdots(packed, qx)       # int64, every ABI row
+    ref = np.stack([by_tensor[t][r] for t, r in rows])
+    assert np.array_equal(gpu, ref), f"{np.count_nonzero(gpu != ref)} block dots differ"
+
+
+def test_q4_int8_activations_match_oracle_quantisation():
+    """Teacher-forced: the oracle quantises the same layer input; codes agree up to +-1."""
+    w = SMALL["q4_mha_d128"]
+    max_ctx = w.prefill + 3
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True)
+    km = max(w.hidden, w.ffn, w.n_q_heads * w.head_dim)
+    qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
+    qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")
+    tap = torch.zeros(w.n_layers, w.hidden, device="cuda")
+    d.set_tap(tap, qact, qsc)
+    x = synth.step_input(w, 0)
+    emb = torch.from_numpy(x).cuda()
+    out = torch.empty_like(emb)
+    d.step(emb, w.prefill, out)
+    d.sync_status()
+    d.close()
+    st = oracle_stack(w, host, max_ctx)
+    inputs = [x.astype(np.float64)] + [tap[l].cpu().numpy().astype(np.float64)
+                                       for l in range(w.n_layers - 1)]
+    qa = qact.cpu().numpy()
+    for l in range(w.n_layers):
+        _, taps = st.layer_step(l, inputs[l], w.prefill, qtap=True)
+        for slot, K in enumerate((w.hidden, w.n_q_heads * w.head_dim, w.hidden, w.ffn)):
+            diff = qa[l, slot, :K].astype(np.int32) - taps[slot][0].astype(np.int32)
+            assert np.abs(diff).max() <= 1, (l, slot, np.abs(diff).max())
+            frac = np.count_nonzero(diff) / K
+            # slot 0 quantises the oracle's own normalisation of the same input;
+            # later slots follow values that already differ slightly
+            assert frac <= (1e-3 if slot == 0 else 2e-2), (l, slot, frac)

@@ -2,6 +2,7 @@
 // mbarriers, programmatic dependent launch, bounded waits and bf16 unpacking.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -12,6 +13,7 @@ namespace tld {
 // Bounded waits: a wait that legitimately takes more than a few milliseconds
 // means something is broken; the kernel then raises the error flag and leaves.
 constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 enum ErrBits : int { ERR_FULL_WAIT = 1, ERR_EMPTY_WAIT = 2, ERR_DRAIN = 4, ERR_SPLITS = 8 };
 
@@ -52,10 +54,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for phase `parity` of `bar` to complete; false after kWaitLimit tries.
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Waits for phase `parity` of `bar` to complete; false once kWaitLimitNs of
+// wall time have passed (measured on %globaltimer, whatever each try_wait's
+// own suspension time is) or after kWaitLimit tries.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
   return false;
 }
 
@@ -113,11 +127,6 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // Timeline probe of one launch (ns, %globaltimer): [0] first CTA start,
 // [1] last CTA end, [2] / [3] first / last return from griddepcontrol.wait,

@@ -23,9 +23,9 @@ constexpr int kNumMats = 7;  // q k v o gate up down
 
 struct Tiled {  // one fused-plan matrix in the tiled layout
   uint8_t* w = nullptr;
-  int N = 0, K = 0, ktiles = 0, kw_last = 0, n_rb = 0, nstages = 0, max_rb_local = 0;
-  int64_t ntiles = 0;
-  size_t smem = 0;
+  TileGeom geo{};
+  int N = 0, K = 0, n_rb = 0, nstages = 0, max_rb_local = 0;
+  size_t bytes = 0, smem = 0;
 };
 
 struct LayerDev {
@@ -33,6 +33,8 @@ struct LayerDev {
   uint16_t* ffn_norm = nullptr;
   Tiled qkv, o, gu, down;                       // fused plan
   uint16_t* mats[kNumMats] = {};                // unfused plan: row-major bf16
+  uint8_t* q4n[kNumMats] = {};                  // unfused plan: q4 nibbles [N][K/2]
+  uint16_t* q4s[kNumMats] = {};                 // unfused plan: q4 scales [N][K/32]
   uint16_t* kc = nullptr;
   uint16_t* vc = nullptr;
   uint32_t loaded = 0;                          // bit per tensor id
@@ -52,6 +54,8 @@ struct dec_handle {
   // activations / workspace
   float *X = nullptr, *h1 = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
   float *n1 = nullptr, *k = nullptr, *v = nullptr, *g = nullptr, *u = nullptr, *y = nullptr;
+  int8_t* qbuf = nullptr;  // unfused q4: int8 GEMV input
+  float* dbuf = nullptr;   // and its block scales
   float* apart = nullptr;  // attention partial records
   int* acount = nullptr;   // attention arrivals per split head
   int att_grid = 0;
@@ -66,6 +70,8 @@ struct dec_handle {
   int64_t weight_bytes = 0, kv_bytes = 0, ws_bytes = 0;
   // taps
   uint64_t* timeline = nullptr;
+  int32_t* dot_tap = nullptr;
+  int dot_layer = -1, dot_kernel = -1;
   float* tap = nullptr;
   int8_t* qtap = nullptr;
   float* qstap = nullptr;
@@ -117,21 +123,20 @@ int dev_alloc(dec_handle* h, T** p, size_t bytes, int64_t* account) {
 }
 
 // Plans one tiled matrix: each CTA owns whole row blocks; the ring gets as
-// many 32 KB stages as the shared-memory budget leaves.
-void plan_tiled(Tiled& t, int N, int K, int n_sm) {
+// many stages as the shared-memory budget leaves.
+void plan_tiled(Tiled& t, int N, int K, int n_sm, bool q4) {
   t.N = N;
   t.K = K;
-  t.ktiles = (K + kTileK - 1) / kTileK;
-  t.kw_last = K - kTileK * (t.ktiles - 1);
+  t.geo = tile_geom(K, q4);
   t.n_rb = N / kTileR;
-  t.ntiles = (int64_t)t.n_rb * t.ktiles;
+  t.bytes = (size_t)t.n_rb * t.geo.rb_bytes;
   t.max_rb_local = (t.n_rb + n_sm - 1) / n_sm;
-  const size_t fixed = gemv_smem_bytes(K, 0, t.max_rb_local);
-  int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kStageBytes);
-  if (ns < 2) ns = 2;  // may then exceed the co-residency budget (large K)
+  const size_t fixed = gemv_smem_bytes(K, q4, 0, t.max_rb_local);
+  int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / t.geo.stage_bytes);
+  if (ns < 2) ns = 2;
   if (ns > 8) ns = 8;
   t.nstages = ns;
-  t.smem = gemv_smem_bytes(K, ns, t.max_rb_local);
+  t.smem = gemv_smem_bytes(K, q4, ns, t.max_rb_local);
 }
 
 int max_k(const dec_model_desc& d) {
@@ -165,6 +170,9 @@ uint32_t required_mask(const dec_model_desc& d) {
   return m;
 }
 
+// Index 0..6 of a matrix tensor id (q k v o gate up down).
+int mat_index(int tensor) { return tensor <= DEC_T_WO ? tensor - DEC_T_WQ : tensor - DEC_T_WQ - 1; }
+
 void drop_graph(dec_handle* h) {
   if (h->exec) cudaGraphExecDestroy(h->exec);
   if (h->graph_g) cudaGraphDestroy(h->graph_g);
@@ -178,11 +186,8 @@ void drop_graph(dec_handle* h) {
 GemvParams gemv_base(const dec_handle* h, const Tiled& t) {
   GemvParams p{};
   p.w = t.w;
-  p.K = t.K;
-  p.ktiles = t.ktiles;
-  p.kw_last = t.kw_last;
+  p.geo = t.geo;
   p.n_rb = t.n_rb;
-  p.ntiles = t.ntiles;
   p.nstages = t.nstages;
   p.max_rb_local = t.max_rb_local;
   p.eps = h->d.rms_eps;
@@ -270,12 +275,23 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
   const bool first = in_step && l == 0;
   const bool last = l == h->d.n_layers - 1;
   uint64_t* tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + kernel) : nullptr;
+  const bool q4 = h->d.weight_fmt == DEC_W_Q4B32;
+  // int8 input taps: q, o, gate and down projections of layer l
+  const int km = max_k(h->d);
+  auto qtaps = [&](GemvParams& p, int slot) {
+    if (in_step && h->qtap) {
+      p.qtap = h->qtap + ((size_t)l * 4 + slot) * km;
+      p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
+    }
+    if (in_step && h->dot_tap && h->dot_layer == l && h->dot_kernel == kernel) p.dots = h->dot_tap;
+  };
   cudaError_t e = cudaSuccess;
   switch (kernel) {
     case 0: {
       GemvParams p = k1_params(h, l, first ? emb : h->X, first);
       p.tl = tl;
-      e = launch_gemv(PRO_NORM, EPI_QKV, p, nb, L.qkv.smem, s, h->pdl);
+      qtaps(p, 0);
+      e = launch_gemv(PRO_NORM, EPI_QKV, q4, p, nb, L.qkv.smem, s, h->pdl);
       break;
     }
     case 1: {
@@ -287,19 +303,22 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
     case 2: {
       GemvParams p = k3_params(h, l);
       p.tl = tl;
-      e = launch_gemv(PRO_PLAIN, EPI_RESID, p, nb, L.o.smem, s, h->pdl);
+      qtaps(p, 1);
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.o.smem, s, h->pdl);
       break;
     }
     case 3: {
       GemvParams p = k4_params(h, l);
       p.tl = tl;
-      e = launch_gemv(PRO_NORM, EPI_SWIGLU, p, nb, L.gu.smem, s, h->pdl);
+      qtaps(p, 2);
+      e = launch_gemv(PRO_NORM, EPI_SWIGLU, q4, p, nb, L.gu.smem, s, h->pdl);
       break;
     }
     case 4: {
       GemvParams p = k5_params(h, l, (in_step && last) ? out : h->X, in_step && last);
       p.tl = tl;
-      e = launch_gemv(PRO_PLAIN, EPI_RESID, p, nb, L.down.smem, s, h->pdl);
+      qtaps(p, 3);
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.down.smem, s, h->pdl);
       break;
     }
     default:
@@ -314,33 +333,51 @@ int enqueue_unfused_layer(dec_handle* h, int l, const float* x_in, float* out, b
   const dec_model_desc& d = h->d;
   const LayerDev& L = h->layers[l];
   const int H = d.hidden, hd = d.head_dim, F = d.ffn, nq = d.n_q_heads, nkv = d.n_kv_heads;
+  const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+  const int km = max_k(d);
   float* tap = h->tap ? h->tap + (size_t)l * H : nullptr;
 #define TLD_U(call)                                        \
   do {                                                     \
     cudaError_t e_ = (call);                               \
     if (e_ != cudaSuccess) return cuda_fail(h, e_, #call); \
   } while (0)
+  // q4: one quantisation per GEMV input vector (slot = q, o, gate/up, down)
+  auto quant = [&](const float* z, int K, int slot) {
+    int8_t* qt = h->qtap ? h->qtap + ((size_t)l * 4 + slot) * km : nullptr;
+    float* st = h->qtap ? h->qstap + ((size_t)l * 4 + slot) * (km / 32) : nullptr;
+    return unf::quantize(z, K, h->qbuf, h->dbuf, qt, st, s);
+  };
+  auto proj = [&](int m, int N, int K, const float* z, float* y) {
+    return q4 ? unf::gemv_q4(L.q4n[m], L.q4s[m], N, K, h->qbuf, h->dbuf, y, s)
+              : unf::gemv(L.mats[m], N, K, z, y, s);
+  };
   TLD_U(unf::rms_scale(x_in, H, d.rms_eps, h->n1, s));
   TLD_U(unf::mul(h->n1, L.attn_norm, H, s));
-  TLD_U(unf::gemv(L.mats[0], nq * hd, H, h->n1, h->q, s));
-  TLD_U(unf::gemv(L.mats[1], nkv * hd, H, h->n1, h->k, s));
-  TLD_U(unf::gemv(L.mats[2], nkv * hd, H, h->n1, h->v, s));
+  if (q4) TLD_U(quant(h->n1, H, 0));
+  TLD_U(proj(0, nq * hd, H, h->n1, h->q));
+  TLD_U(proj(1, nkv * hd, H, h->n1, h->k));
+  TLD_U(proj(2, nkv * hd, H, h->n1, h->v));
   TLD_U(unf::rope(h->q, h->k, nq, nkv, hd, h->d_pos, h->rope, s));
   TLD_U(unf::kv_append(h->k, h->v, nkv, hd, d.max_ctx, h->d_pos, L.kc, L.vc, s));
   TLD_U(unf::attention(h->q, L.kc, L.vc, nq, nkv, hd, d.max_ctx, h->d_pos, h->o, s));
-  TLD_U(unf::gemv(L.mats[3], H, nq * hd, h->o, h->y, s));
+  if (q4) TLD_U(quant(h->o, nq * hd, 1));
+  TLD_U(proj(3, H, nq * hd, h->o, h->y));
   TLD_U(unf::add(x_in, h->y, h->h1, nullptr, H, nullptr, s));
   TLD_U(unf::rms_scale(h->h1, H, d.rms_eps, h->n1, s));
   TLD_U(unf::mul(h->n1, L.ffn_norm, H, s));
-  TLD_U(unf::gemv(L.mats[4], F, H, h->n1, h->g, s));
-  TLD_U(unf::gemv(L.mats[5], F, H, h->n1, h->u, s));
+  if (q4) TLD_U(quant(h->n1, H, 2));
+  TLD_U(proj(4, F, H, h->n1, h->g));
+  TLD_U(proj(5, F, H, h->n1, h->u));
   TLD_U(unf::swiglu(h->g, h->u, h->a, F, s));
-  TLD_U(unf::gemv(L.mats[6], H, F, h->a, h->y, s));
+  if (q4) TLD_U(quant(h->a, F, 3));
+  TLD_U(proj(6, H, F, h->a, h->y));
   TLD_U(unf::add(h->h1, h->y, out, tap, H, last ? h->d_pos : nullptr, s));
 #undef TLD_U
   return DEC_OK;
 }
+// one kernel per op; the q4 form adds one quantisation per GEMV input vector
 constexpr int kUnfusedKernelsPerLayer = 17;
+constexpr int kUnfusedKernelsPerLayerQ4 = 21;
 
 // Queues one whole token.  Records the first and last kernel nodes when capturing.
 int enqueue_step(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing) {
@@ -387,15 +424,26 @@ int capture(dec_handle* h, const float* emb, float* out) {
   return DEC_OK;
 }
 
+// The taps a captured launch of kernel k (0 QKV, 4 down) of layer l carries.
+void set_captured_taps(const dec_handle* h, GemvParams& p, int l, int k) {
+  const int km = max_k(h->d), slot = k == 0 ? 0 : 3;
+  if (h->qtap) {
+    p.qtap = h->qtap + ((size_t)l * 4 + slot) * km;
+    p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
+  }
+  if (h->dot_tap && h->dot_layer == l && h->dot_kernel == k) p.dots = h->dot_tap;
+}
+
 // Points the captured graph at new input / output buffers.
 int patch_io(dec_handle* h, const float* emb, float* out) {
   if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
   if (emb != h->cap_emb) {
     GemvParams p = k1_params(h, 0, emb, true);
     p.tl = h->timeline;
+    set_captured_taps(h, p, 0, 0);
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
-    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_NORM, EPI_QKV));
+    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_NORM, EPI_QKV, h->d.weight_fmt == DEC_W_Q4B32));
     kp.gridDim = dim3(h->n_sm);
     kp.blockDim = dim3(kThreads);
     kp.sharedMemBytes = (unsigned)h->layers[0].qkv.smem;
@@ -407,9 +455,10 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
     const int l = h->d.n_layers - 1;
     GemvParams p = k5_params(h, l, out, true);
     p.tl = h->timeline ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 4) : nullptr;
+    set_captured_taps(h, p, l, 4);
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
-    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_PLAIN, EPI_RESID));
+    kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_PLAIN, EPI_RESID, h->d.weight_fmt == DEC_W_Q4B32));
     kp.gridDim = dim3(h->n_sm);
     kp.blockDim = dim3(kThreads);
     kp.sharedMemBytes = (unsigned)h->layers[l].down.smem;
@@ -451,8 +500,9 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   if (d.max_ctx > 65536) return fail(nullptr, DEC_ERR_SHAPE, "max_ctx > 65536");
   if (d.weight_fmt != DEC_W_BF16 && d.weight_fmt != DEC_W_Q4B32)
     return fail(nullptr, DEC_ERR_ARG, "unknown weight_fmt %d", d.weight_fmt);
-  if (d.weight_fmt == DEC_W_Q4B32)
-    return fail(nullptr, DEC_ERR_SHAPE, "int4 weights are not built in this library yet");
+  if (d.weight_fmt == DEC_W_Q4B32 &&
+      (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64))
+    return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
@@ -486,17 +536,22 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     A(&L.attn_norm, 2 * (size_t)H, &h->weight_bytes);
     A(&L.ffn_norm, 2 * (size_t)H, &h->weight_bytes);
     if (h->fused) {
-      plan_tiled(L.qkv, (nq + 2 * nkv) * hd, H, h->n_sm);
-      plan_tiled(L.o, H, nq * hd, h->n_sm);
-      plan_tiled(L.gu, 2 * F, H, h->n_sm);
-      plan_tiled(L.down, H, F, h->n_sm);
-      for (Tiled* t : {&L.qkv, &L.o, &L.gu, &L.down})
-        A(&t->w, 2 * (size_t)t->N * t->K, &h->weight_bytes);
+      const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+      plan_tiled(L.qkv, (nq + 2 * nkv) * hd, H, h->n_sm, q4);
+      plan_tiled(L.o, H, nq * hd, h->n_sm, q4);
+      plan_tiled(L.gu, 2 * F, H, h->n_sm, q4);
+      plan_tiled(L.down, H, F, h->n_sm, q4);
+      for (Tiled* t : {&L.qkv, &L.o, &L.gu, &L.down}) A(&t->w, t->bytes, &h->weight_bytes);
     } else {
       for (int m = 0; m < kNumMats; ++m) {
         int N, K;
         mat_shape(d, DEC_T_WQ + (m < 4 ? m : m + 1), &N, &K);
-        A(&L.mats[m], 2 * (size_t)N * K, &h->weight_bytes);
+        if (d.weight_fmt == DEC_W_Q4B32) {
+          A(&L.q4n[m], (size_t)N * K / 2, &h->weight_bytes);
+          A(&L.q4s[m], (size_t)N * (K / 32) * 2, &h->weight_bytes);
+        } else {
+          A(&L.mats[m], 2 * (size_t)N * K, &h->weight_bytes);
+        }
       }
     }
     A(&L.kc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
@@ -514,6 +569,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   A(&h->g, 4 * (size_t)F, &h->ws_bytes);
   A(&h->u, 4 * (size_t)F, &h->ws_bytes);
   A(&h->y, 4 * (size_t)km, &h->ws_bytes);
+  A(&h->qbuf, (size_t)km, &h->ws_bytes);
+  A(&h->dbuf, 4 * (size_t)(km / 32 + 1), &h->ws_bytes);
   A(&h->apart, 4 * (size_t)h->att_grid * 2 * G * (hd + 4), &h->ws_bytes);
   A(&h->acount, 4 * (size_t)nkv, &h->ws_bytes);
   A(&h->d_pos, 16, &h->ws_bytes);
@@ -567,14 +624,18 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
     L.loaded |= 1u << tensor;
     return DEC_OK;
   }
+  const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+  const bool scales = q4 && tensor >= DEC_T_SCALES;
+  const int mt = scales ? tensor - DEC_T_SCALES : tensor;
   int N, K;
-  mat_shape(d, tensor, &N, &K);
+  mat_shape(d, mt, &N, &K);
   if (N == 0) return fail(h, DEC_ERR_ARG, "tensor id %d invalid for this weight format", tensor);
-  const size_t want = 2 * (size_t)N * K;
+  const size_t want = !q4 ? 2 * (size_t)N * K : scales ? (size_t)N * (K / 32) * 2 : (size_t)N * K / 2;
   if (bytes != want) return fail(h, DEC_ERR_ARG, "tensor %d: %zu bytes, expected %zu", tensor, bytes, want);
   if (!h->fused) {
-    const int m = tensor <= DEC_T_WO ? tensor - DEC_T_WQ : tensor - DEC_T_WQ - 1;
-    TLD_CUDA(h, cudaMemcpy(L.mats[m], src, bytes, cudaMemcpyDefault));
+    const int m = mat_index(mt);
+    void* dst = !q4 ? (void*)L.mats[m] : scales ? (void*)L.q4s[m] : (void*)L.q4n[m];
+    TLD_CUDA(h, cudaMemcpy(dst, src, bytes, cudaMemcpyDefault));
     L.loaded |= 1u << tensor;
     return DEC_OK;
   }
@@ -592,20 +653,26 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
   }
   TLD_CUDA(h, cudaMemcpy(h->staging, src, bytes, cudaMemcpyDefault));
   const int hd = d.head_dim;
-  cudaError_t e;
-  switch (tensor) {
-    case DEC_T_WQ: e = launch_repack_bf16(h->staging, N, K, L.qkv.w, 0, 1, hd, 0); break;
-    case DEC_T_WK:
-      e = launch_repack_bf16(h->staging, N, K, L.qkv.w, d.n_q_heads * hd, 1, hd, 0);
-      break;
-    case DEC_T_WV:
-      e = launch_repack_bf16(h->staging, N, K, L.qkv.w, (d.n_q_heads + d.n_kv_heads) * hd, 0, hd, 0);
-      break;
-    case DEC_T_WO: e = launch_repack_bf16(h->staging, N, K, L.o.w, 0, 0, hd, 0); break;
-    case DEC_T_WGATE: e = launch_repack_bf16(h->staging, N, K, L.gu.w, 0, 2, hd, 0); break;
-    case DEC_T_WUP: e = launch_repack_bf16(h->staging, N, K, L.gu.w, 1, 2, hd, 0); break;
-    default: e = launch_repack_bf16(h->staging, N, K, L.down.w, 0, 0, hd, 0); break;
+  // destination matrix, first tiled row and row map of each tensor
+  uint8_t* dst = nullptr;
+  int row0 = 0, kind = 0;
+  switch (mt) {
+    case DEC_T_WQ: dst = L.qkv.w; row0 = 0; kind = 1; break;
+    case DEC_T_WK: dst = L.qkv.w; row0 = d.n_q_heads * hd; kind = 1; break;
+    case DEC_T_WV: dst = L.qkv.w; row0 = (d.n_q_heads + d.n_kv_heads) * hd; kind = 0; break;
+    case DEC_T_WO: dst = L.o.w; row0 = 0; kind = 0; break;
+    case DEC_T_WGATE: dst = L.gu.w; row0 = 0; kind = 2; break;
+    case DEC_T_WUP: dst = L.gu.w; row0 = 1; kind = 2; break;
+    default: dst = L.down.w; row0 = 0; kind = 0; break;
   }
+  cudaError_t e;
+  if (!q4)
+    e = launch_repack_bf16(h->staging, N, K, dst, row0, kind, hd, 0);
+  else if (scales)
+    e = launch_repack_q4(nullptr, h->staging, N, K, dst, row0, kind, hd, 0);
+  else
+    e = launch_repack_q4(reinterpret_cast<const uint8_t*>(h->staging), nullptr, N, K, dst, row0,
+                         kind, hd, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(h, e, "weight repack");
   L.loaded |= 1u << tensor;
@@ -683,6 +750,20 @@ int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qs
   return DEC_OK;
 }
 
+int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (dots && (!h->fused || h->d.weight_fmt != DEC_W_Q4B32))
+    return fail(h, DEC_ERR_STATE, "block-dot taps need the fused plan with int4 weights");
+  if (dots && (layer < 0 || layer >= h->d.n_layers || (kernel != 0 && kernel != 2 && kernel != 3 &&
+                                                        kernel != 4)))
+    return fail(h, DEC_ERR_ARG, "bad layer %d / kernel %d for a block-dot tap", layer, kernel);
+  h->dot_tap = dots;
+  h->dot_layer = dots ? layer : -1;
+  h->dot_kernel = dots ? kernel : -1;
+  drop_graph(h);
+  return DEC_OK;
+}
+
 int dec_set_timeline(dec_handle* h, uint64_t* buf) {
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
   if (buf && !h->fused) return fail(h, DEC_ERR_STATE, "the timeline probe needs the fused plan");
@@ -705,7 +786,9 @@ int dec_sync_status(dec_handle* h, dec_stream_t stream) {
 
 int dec_get_info(const dec_handle* h, dec_info* info) {
   if (!h || !info) return DEC_ERR_ARG;
-  info->kernels_per_layer = h->fused ? 5 : kUnfusedKernelsPerLayer;
+  info->kernels_per_layer = h->fused ? 5
+                            : h->d.weight_fmt == DEC_W_Q4B32 ? kUnfusedKernelsPerLayerQ4
+                                                             : kUnfusedKernelsPerLayer;
   info->kernels_per_token = info->kernels_per_layer * h->d.n_layers;
   info->n_sm = h->n_sm;
   info->kv_len = h->kv_len;

@@ -20,14 +20,18 @@ __host__ __device__ inline int split_owner(int64_t total, int parts, int64_t u) 
   return (int)(((u + 1) * parts - 1) / total);
 }
 
-// ---- tiled weight layout ----------------------------------------------------
+// ---- tiled weight layouts ---------------------------------------------------
 // A [N][K] matrix is stored as row blocks of kTileR rows; each row block is a
-// run of k-tiles of kTileK columns (the last one kw = K - kTileK*(ktiles-1)
-// wide), each k-tile row-major inside.  Tiles are consecutive in memory in
-// (row block, k-tile) order, so any range of tiles is one contiguous run of
-// bytes: a CTA that owns tiles [t0, t1) streams exactly one slab.
+// run of k-tiles (the last one narrower when K is not a multiple of the tile
+// width), consecutive in memory in (row block, k-tile) order, so any range of
+// tiles is one contiguous run of bytes: a CTA that owns a range of row blocks
+// streams exactly one slab.
+//   bf16: k-tiles of kTileK columns, row-major inside ([kTileR][kw] bf16).
+//   q4:   k-tiles of kTileKQ4 columns (32 blocks of 32); inside, the packed
+//         nibbles [kTileR][kw/2 bytes], then the fp16 scales [kw/32][kTileR].
 constexpr int kTileR = 4;
 constexpr int kTileK = 256;
+constexpr int kTileKQ4 = 1024;
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
 // Shared memory budget per CTA.  Above half of the SM's 228 KB, so two CTAs of
@@ -38,27 +42,65 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 pro
 #endif
 constexpr int kSmemBudget = TLD_SMEM_BUDGET_KB * 1024;
 constexpr int kAttnStageBytes = 32768;  // K chunk + V chunk, 16 KB each
-// Bytes of its slab each GEMV CTA pulls into L2 at launch (beyond its ring).
-constexpr int kL2PrefetchBytes = 256 * 1024;
-constexpr int kTimelineSlots = 8;  // u64 per launch of the timeline probe
+constexpr int kTimelineSlots = 8;       // u64 per launch of the timeline probe
 // Most attention CTAs one KV head may be split over (bounds the merge).
 constexpr int kMaxSplits = 32;
-constexpr int kStageTiles = 2 * kConsumerWarps;      // two tiles per consumer warp per stage
+constexpr int kStageTiles = 2 * kConsumerWarps;  // two tiles per consumer warp per stage
 constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
-constexpr int kStageBytes = kStageTiles * kTileR * kTileK * 2;  // 32 KB
+constexpr int kTileBytes = kTileR * kTileK * 2;                          // 2 KB
+constexpr int kTileBytesQ4 = kTileR * (kTileKQ4 / 2 + kTileKQ4 / 16);    // 2304 B
+constexpr int kStageBytes = kStageTiles * kTileBytes;                    // 32 KB
+constexpr int kStageBytesQ4 = kStageTiles * kTileBytesQ4;                // 36 KB
 
-__host__ __device__ inline int64_t tile_byte_offset(int64_t t, int ktiles, int K) {
-  int64_t rb = t / ktiles, kt = t - rb * ktiles;
-  return rb * (int64_t)kTileR * K * 2 + kt * (int64_t)kTileR * kTileK * 2;
+// Byte geometry of one tiled matrix.
+struct TileGeom {
+  int K, tile_k, ktiles, kw_last;
+  int64_t rb_bytes, tile_bytes;
+  int stage_bytes;
+};
+
+__host__ __device__ inline TileGeom tile_geom(int K, bool q4) {
+  TileGeom g;
+  g.K = K;
+  g.tile_k = q4 ? kTileKQ4 : kTileK;
+  g.ktiles = (K + g.tile_k - 1) / g.tile_k;
+  g.kw_last = K - g.tile_k * (g.ktiles - 1);
+  g.rb_bytes = q4 ? (int64_t)kTileR * (K / 2 + K / 16) : (int64_t)kTileR * K * 2;
+  g.tile_bytes = q4 ? kTileBytesQ4 : kTileBytes;
+  g.stage_bytes = q4 ? kStageBytesQ4 : kStageBytes;
+  return g;
 }
 
-// Element (row r, col k) of a [N][K] matrix inside the tiled layout.
+__host__ __device__ inline int64_t tile_byte_offset(int64_t t, const TileGeom& g) {
+  const int64_t rb = t / g.ktiles, kt = t - rb * g.ktiles;
+  return rb * g.rb_bytes + kt * g.tile_bytes;
+}
+
+// bf16: element (row r, col k) inside the tiled layout (in elements).
 __host__ __device__ inline int64_t tiled_elem_offset(int64_t r, int64_t k, int K) {
-  int ktiles = (K + kTileK - 1) / kTileK;
-  int64_t kt = k / kTileK;
-  int kw = (kt == ktiles - 1) ? K - kTileK * (ktiles - 1) : kTileK;
+  const int ktiles = (K + kTileK - 1) / kTileK;
+  const int64_t kt = k / kTileK;
+  const int kw = (kt == ktiles - 1) ? K - kTileK * (ktiles - 1) : kTileK;
   return (r / kTileR) * (int64_t)kTileR * K + kt * (int64_t)kTileR * kTileK +
          (r % kTileR) * kw + (k - kt * kTileK);
+}
+
+// q4: byte of the packed pair (row r, columns 2c2 and 2c2+1).
+__host__ __device__ inline int64_t q4_nibble_byte(int64_t r, int64_t c2, int K) {
+  const TileGeom g = tile_geom(K, true);
+  const int64_t kt = (2 * c2) / kTileKQ4;
+  const int kw = (kt == g.ktiles - 1) ? g.kw_last : kTileKQ4;
+  return (r / kTileR) * g.rb_bytes + kt * g.tile_bytes + (r % kTileR) * (kw / 2) +
+         (c2 - kt * (kTileKQ4 / 2));
+}
+
+// q4: byte of the fp16 scale of (row r, block b).
+__host__ __device__ inline int64_t q4_scale_byte(int64_t r, int64_t b, int K) {
+  const TileGeom g = tile_geom(K, true);
+  const int64_t kt = (32 * b) / kTileKQ4;
+  const int kw = (kt == g.ktiles - 1) ? g.kw_last : kTileKQ4;
+  return (r / kTileR) * g.rb_bytes + kt * g.tile_bytes + kTileR * (kw / 2) +
+         ((b - kt * (kTileKQ4 / 32)) * kTileR + (r % kTileR)) * 2;
 }
 
 enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
@@ -66,9 +108,8 @@ enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
 
 struct GemvParams {
   const uint8_t* w;  // tiled weights
-  int K, ktiles, kw_last, n_rb;
-  int64_t ntiles;
-  int nstages, max_rb_local;
+  TileGeom geo;
+  int n_rb, nstages, max_rb_local;
   // prologue
   const float* x;          // input vector [K]
   const uint16_t* norm_w;  // bf16 [K] (PRO_NORM)
@@ -90,6 +131,10 @@ struct GemvParams {
   // EPI_SWIGLU: rows interleave gate and up
   float* a_out;
   uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
+  // q4 weights: the int8 input of this GEMV is also written here by CTA 0
+  int8_t* qtap;    // [K] natural order, or null
+  float* qstap;    // [K/32] block scales, or null
+  int32_t* dots;   // [n_rb * kTileR][K/32] integer block dots (tiled row order), or null
 };
 
 struct AttnParams {
@@ -107,16 +152,16 @@ struct AttnParams {
 };
 
 // Shared memory the fused kernels need.
-size_t gemv_smem_bytes(int K, int nstages, int max_rb_local);
+size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local);
 size_t attn_smem_bytes(int hd, int G, int nstages);
 
 // Launch with programmatic stream serialization (the kernel may start while
 // the previous one on the stream finishes; it waits before reading its inputs).
-cudaError_t launch_gemv(int pro, int epi, const GemvParams& p, int grid, size_t smem,
+cudaError_t launch_gemv(int pro, int epi, bool q4, const GemvParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
 cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
-const void* gemv_kernel_ptr(int pro, int epi);
+const void* gemv_kernel_ptr(int pro, int epi, bool q4);
 const void* attn_kernel_ptr(int hd, int G);
 cudaError_t set_smem_limits();
 
@@ -127,6 +172,10 @@ cudaError_t set_smem_limits();
 //   gate/up:   dst_row0 + 2*s (+1 for up via dst_row0)  (kind 2)
 cudaError_t launch_repack_bf16(const uint16_t* src, int rows, int K, uint8_t* dst_tiled,
                                int dst_row0, int kind, int hd, cudaStream_t s);
+// The same row maps for q4 weights: packed nibbles [rows][K/2] and fp16 scales
+// [rows][K/32] into the q4 tiled layout.
+cudaError_t launch_repack_q4(const uint8_t* nibbles, const uint16_t* scales, int rows, int K,
+                             uint8_t* dst_tiled, int dst_row0, int kind, int hd, cudaStream_t s);
 
 // ---- the unfused plan: one kernel per op -------------------------------------
 namespace unf {
@@ -142,6 +191,11 @@ cudaError_t attention(const float* q, const uint16_t* kc, const uint16_t* vc, in
 cudaError_t add(const float* a, const float* b, float* out, float* tap, int n, int* pos_advance,
                 cudaStream_t s);
 cudaError_t swiglu(const float* g, const float* u, float* a, int F, cudaStream_t s);
+// q4 path: per-32 absmax int8 quantization of z; GEMV on ABI-layout q4 weights.
+cudaError_t quantize(const float* z, int K, int8_t* qx, float* dx, int8_t* qtap, float* qstap,
+                     cudaStream_t s);
+cudaError_t gemv_q4(const uint8_t* packed, const uint16_t* scales, int N, int K, const int8_t* qx,
+                    const float* dx, float* y, cudaStream_t s);
 }  // namespace unf
 
 }  // namespace tld

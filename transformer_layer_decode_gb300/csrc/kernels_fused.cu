@@ -30,19 +30,27 @@ namespace tld {
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
 
 // ---- shared memory layout of the GEMV kernel -------------------------------
+// ring of stages | mbarriers | x (fp32, K) | [q4: int8 x (K), block scales,
+// block sums] | per-warp row-block partials | warp sums
 struct GemvSmem {
-  int K, nstages, max_rb_local;
-  __host__ __device__ size_t bars_off() const { return (size_t)nstages * kStageBytes; }
+  int K, nstages, max_rb_local, stage_bytes;
+  bool q4;
+  __host__ __device__ size_t bars_off() const { return (size_t)nstages * stage_bytes; }
   __host__ __device__ size_t xs_off() const { return bars_off() + 16 * (size_t)nstages; }
-  __host__ __device__ size_t part_off() const { return xs_off() + 4 * (size_t)((K + 3) & ~3); }
+  __host__ __device__ size_t qx_off() const { return xs_off() + 4 * (size_t)((K + 3) & ~3); }
+  __host__ __device__ size_t dx_off() const { return qx_off() + (q4 ? (size_t)K : 0); }
+  __host__ __device__ size_t sx_off() const { return dx_off() + (q4 ? 4 * (size_t)(K / 32) : 0); }
+  __host__ __device__ size_t part_off() const {
+    return sx_off() + (q4 ? 4 * (size_t)(K / 32) : 0);
+  }
   __host__ __device__ size_t red_off() const {
     return part_off() + 4 * (size_t)max_rb_local * kConsumerWarps * kTileR;
   }
-  __host__ __device__ size_t total() const { return red_off() + 4 * 32; }  // red: warp sums + abort mark
+  __host__ __device__ size_t total() const { return red_off() + 4 * 32; }  // warp sums + abort mark
 };
 
-size_t gemv_smem_bytes(int K, int nstages, int max_rb_local) {
-  return GemvSmem{K, nstages, max_rb_local}.total();
+size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
+  return GemvSmem{K, nstages, max_rb_local, q4 ? kStageBytesQ4 : kStageBytes, q4}.total();
 }
 
 // Epilogue of one finished row block (kTileR tiled rows, values v).
@@ -107,8 +115,8 @@ struct TileCursor {
     }
   }
   // byte offset of the tile from the matrix start
-  __device__ __forceinline__ int64_t offset(int K) const {
-    return (int64_t)rb * kTileR * K * 2 + (int64_t)kt * kTileR * kTileK * 2;
+  __device__ __forceinline__ int64_t offset(const TileGeom& g) const {
+    return (int64_t)rb * g.rb_bytes + (int64_t)kt * g.tile_bytes;
   }
 };
 
@@ -127,25 +135,98 @@ __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
   return k;
 }
 
-template <int PRO, int EPI>
+// Per-32-block absmax int8 quantization of the fp32 vector xs[K] (K % 32 == 0):
+// dx = amax / 127 (fp32 divide), q = round-half-even(z / dx) clamped to +-127,
+// q = 0 when dx == 0.  Eight lanes serve a block, four elements each.  The int8
+// values are stored for dp4a against packed nibbles: in each group of eight,
+// the even elements first, then the odd ones.  sx holds each block's sum of q.
+__device__ void quantize_blocks(const float* xs, int K, uint8_t* qx, float* dx, int* sx,
+                                int8_t* qtap, float* qstap, int tid, int NC) {
+  const int lane = tid & 31, sub = lane & 7, warp = tid >> 5;
+  const int nblk = K / 32;
+  // Four blocks per warp per round; the round count is the same for all lanes
+  // of a warp (the shuffles below name the whole warp).
+  for (int base = warp * 4; base < nblk; base += (NC >> 5) * 4) {
+    const int blk = base + (lane >> 3);
+    const bool live = blk < nblk;
+    const int e = blk * 32 + sub * 4;
+    const float4 z = live ? *reinterpret_cast<const float4*>(xs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float amax = fmaxf(fmaxf(fabsf(z.x), fabsf(z.y)), fmaxf(fabsf(z.z), fabsf(z.w)));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q[4];
+    const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int v = 0;
+      if (d != 0.0f) {
+        v = __float2int_rn(__fdiv_rn(zz[i], d));
+        v = v > 127 ? 127 : (v < -127 ? -127 : v);
+      }
+      q[i] = v;
+    }
+    int sum = q[0] + q[1] + q[2] + q[3];
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (!live) continue;
+    // elements e..e+3 = 8g + 4h + {0,1,2,3}: evens go to bytes 8g+2h, 8g+2h+1,
+    // odds to bytes 8g+4+2h, 8g+4+2h+1
+    const int g8 = e & ~7, h = (e >> 2) & 1;
+    *reinterpret_cast<uint16_t*>(qx + g8 + 2 * h) = (uint16_t)((q[0] & 0xff) | ((q[2] & 0xff) << 8));
+    *reinterpret_cast<uint16_t*>(qx + g8 + 4 + 2 * h) =
+        (uint16_t)((q[1] & 0xff) | ((q[3] & 0xff) << 8));
+    if (sub == 0) {
+      dx[blk] = d;
+      sx[blk] = sum;
+    }
+    if (qtap) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qtap[e + i] = (int8_t)q[i];
+      if (sub == 0) qstap[blk] = d;
+    }
+  }
+}
+
+// Integer dot of one 32-block: packed nibbles (q + 8) against the arranged
+// int8 activations, minus 8 * (sum of the activations).
+__device__ __forceinline__ int q4_block_dot(const uint4 w, const uint4 x0, const uint4 x1, int sx) {
+  constexpr uint32_t M = 0x0F0F0F0Fu;
+  int d = 0;
+  d = __dp4a((int)(w.x & M), (int)x0.x, d);
+  d = __dp4a((int)((w.x >> 4) & M), (int)x0.y, d);
+  d = __dp4a((int)(w.y & M), (int)x0.z, d);
+  d = __dp4a((int)((w.y >> 4) & M), (int)x0.w, d);
+  d = __dp4a((int)(w.z & M), (int)x1.x, d);
+  d = __dp4a((int)((w.z >> 4) & M), (int)x1.y, d);
+  d = __dp4a((int)(w.w & M), (int)x1.z, d);
+  d = __dp4a((int)((w.w >> 4) & M), (int)x1.w, d);
+  return d - 8 * sx;
+}
+
+template <int PRO, int EPI, bool Q4>
 __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const GemvSmem L{p.K, p.nstages, p.max_rb_local};
+  const TileGeom& geo = p.geo;
+  const int K = geo.K;
+  const GemvSmem L{K, p.nstages, p.max_rb_local, geo.stage_bytes, Q4};
   uint8_t* stages = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bars_off());
   uint64_t* empty = full + p.nstages;
   float* xs = reinterpret_cast<float*>(smem + L.xs_off());
+  uint8_t* qx = smem + L.qx_off();
+  float* dxs = reinterpret_cast<float*>(smem + L.dx_off());
+  int* sxs = reinterpret_cast<int*>(smem + L.sx_off());
   float* part_s = reinterpret_cast<float*>(smem + L.part_off());
   float* red = reinterpret_cast<float*>(smem + L.red_off());
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nb = gridDim.x, b = blockIdx.x;
   if (tid == 0) tl_mark_min(p.tl, 0);
-  // whole row blocks [rb0, rb1) of this CTA = tiles [t0, t1)
+  // whole row blocks [rb0, rb1) of this CTA = tiles [rb0 * ktiles, rb1 * ktiles)
   const int rb0 = (int)split_begin(p.n_rb, nb, b), rb1 = (int)split_begin(p.n_rb, nb, b + 1);
   const int nrb = rb1 - rb0;
-  const int64_t t0 = (int64_t)rb0 * p.ktiles;
-  const int nloc = nrb * p.ktiles;
+  const int nloc = nrb * geo.ktiles;
   const int nst = (nloc + kStageTiles - 1) / kStageTiles;
 
   if (tid == 0) {
@@ -161,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
     // ---- producer: stream this CTA's slab (weights only: no wait needed) ----
     if (lane == 0) {
       TileCursor cur{rb0, 0};
-      const int64_t end_off = (int64_t)rb1 * kTileR * p.K * 2;
+      const int64_t end_off = (int64_t)rb1 * geo.rb_bytes;
       const uint64_t pol_stream = policy_evict_first();
       int slot = 0, phase = 0;
       for (int s = 0; s < nst; ++s) {
@@ -169,12 +250,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
           raise_error(p.err, ERR_EMPTY_WAIT);
           break;
         }
-        const int64_t oa = cur.offset(p.K);
-        cur.advance(kStageTiles, p.ktiles);
-        const int64_t ob = (s == nst - 1) ? end_off : cur.offset(p.K);
+        const int64_t oa = cur.offset(geo);
+        cur.advance(kStageTiles, geo.ktiles);
+        const int64_t ob = (s == nst - 1) ? end_off : cur.offset(geo);
         const uint32_t bytes = (uint32_t)(ob - oa);
         mbar_arrive_expect_tx(&full[slot], bytes);
-        bulk_g2s_hint(stages + (size_t)slot * kStageBytes, p.w + oa, bytes, &full[slot], pol_stream);
+        bulk_g2s_hint(stages + (size_t)slot * geo.stage_bytes, p.w + oa, bytes, &full[slot],
+                      pol_stream);
         if (++slot == p.nstages) {
           slot = 0;
           phase ^= 1;
@@ -186,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
 
   // ---- consumers -------------------------------------------------------------
   constexpr int NC = kConsumerWarps * 32;
-  const int K4 = p.K / 4;
+  const int K4 = K / 4;
   // Before the wait: the RMSNorm weights (static) go to xs as fp32.
   if (PRO == PRO_NORM) {
     const uint2* w4 = reinterpret_cast<const uint2*>(p.norm_w);
@@ -209,9 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
   // everything before the previous kernel is complete when the next one starts.
   pdl_trigger();
 
-  if (PRO == PRO_NORM) {
-    // RMSNorm is a per-vector scale: the projection runs on x*w and the scale
-    // 1/sqrt(mean(x^2)+eps) is applied to the finished rows.
+  {
     const float4* x4 = reinterpret_cast<const float4*>(p.x);
     float ss = 0.f;
     constexpr int PB = 4;  // loads in flight per thread
@@ -223,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
 #pragma unroll
       for (int u = 0; u < PB; ++u) {
         const int k4 = base + u * NC;
-        if (k4 < K4) {
+        if (k4 >= K4) continue;
+        if (PRO == PRO_NORM) {
           ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
           float4 w = reinterpret_cast<float4*>(xs)[k4];
           w.x *= v[u].x;
@@ -231,37 +312,49 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
           w.z *= v[u].z;
           w.w *= v[u].w;
           reinterpret_cast<float4*>(xs)[k4] = w;
+        } else {
+          reinterpret_cast<float4*>(xs)[k4] = v[u];
         }
       }
     }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-  } else {
-    const float4* x4 = reinterpret_cast<const float4*>(p.x);
-    constexpr int PB = 4;
-    for (int base = tid; base < K4; base += NC * PB) {
-      float4 v[PB];
-#pragma unroll
-      for (int u = 0; u < PB; ++u)
-        if (base + u * NC < K4) v[u] = x4[base + u * NC];
-#pragma unroll
-      for (int u = 0; u < PB; ++u)
-        if (base + u * NC < K4) reinterpret_cast<float4*>(xs)[base + u * NC] = v[u];
+    if (PRO == PRO_NORM) {
+      ss = warp_sum(ss);
+      if (lane == 0) red[warp] = ss;
     }
   }
   if (p.x_copy && b == 0) {
-    for (int k = tid; k < p.K; k += NC) p.x_copy[k] = p.x[k];
+    for (int k = tid; k < K; k += NC) p.x_copy[k] = p.x[k];
   }
   if (p.pos_advance && b == 0 && tid == 0) atomicAdd(p.pos_advance, 1);
   named_barrier(1, NC);
 
+  // RMSNorm is a per-vector scale 1/sqrt(mean(x^2)+eps).  bf16 weights: the
+  // projection runs on x*w and the scale multiplies the finished rows.  q4
+  // weights: the normalised vector itself is quantised, so it is scaled first.
   float rnorm = 1.f;
   if (PRO == PRO_NORM) {
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
-    rnorm = 1.0f / sqrtf(tot / (float)p.K + p.eps);
+    rnorm = 1.0f / sqrtf(tot / (float)K + p.eps);
   }
+  if (Q4) {
+    if (PRO == PRO_NORM) {
+      for (int k4 = tid; k4 < K4; k4 += NC) {
+        float4 v = reinterpret_cast<float4*>(xs)[k4];
+        v.x *= rnorm;
+        v.y *= rnorm;
+        v.z *= rnorm;
+        v.w *= rnorm;
+        reinterpret_cast<float4*>(xs)[k4] = v;
+      }
+      named_barrier(1, NC);
+      rnorm = 1.f;
+    }
+    quantize_blocks(xs, K, qx, dxs, sxs, b == 0 ? p.qtap : nullptr, p.qstap, tid, NC);
+    named_barrier(1, NC);
+  }
+
   int cur_rb = -1;
   float acc[kTileR];
 #pragma unroll
@@ -273,9 +366,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
 #pragma unroll
   for (int j = 0; j < kTilesPerWarp; ++j) {
     my[j] = st_cur;
-    my[j].advance(warp + j * kConsumerWarps, p.ktiles);
+    my[j].advance(warp + j * kConsumerWarps, geo.ktiles);
   }
-  const int c = lane * 8;
+  // bf16: lane owns columns [8 lane, 8 lane + 8) of a tile; q4: lane owns block `lane`
+  const int c = Q4 ? lane * 32 : lane * 8;
   int slot = 0, phase = 0;
   for (int s = 0; s < nst; ++s) {
     // After a timed-out wait the warp stops waiting but keeps the same control
@@ -286,18 +380,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
     }
     if (s == 0 && tid == 0) tl_mark_max(p.tl, 4);
     // Copy this warp's tiles into registers and hand the slot back at once, so
-    // the next bulk copy is in flight while the FMAs run.
+    // the next bulk copy is in flight while the arithmetic runs.
     uint4 wv[kTilesPerWarp][kTileR];
-    const int64_t st_off = st_cur.offset(p.K);
+    uint2 scl[kTilesPerWarp];
+    const int64_t st_off = st_cur.offset(geo);
 #pragma unroll
     for (int j = 0; j < kTilesPerWarp; ++j) {
       const int li = s * kStageTiles + warp + j * kConsumerWarps;
-      const int kw = (my[j].kt == p.ktiles - 1) ? p.kw_last : kTileK;
+      const int kw = (my[j].kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
       if (li < nloc && c < kw) {
-        const uint8_t* tp = stages + (size_t)slot * kStageBytes + (my[j].offset(p.K) - st_off);
+        const uint8_t* tp = stages + (size_t)slot * geo.stage_bytes + (my[j].offset(geo) - st_off);
+        if (Q4) {
 #pragma unroll
-        for (int r = 0; r < kTileR; ++r)
-          wv[j][r] = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
+          for (int r = 0; r < kTileR; ++r)
+            wv[j][r] = *reinterpret_cast<const uint4*>(tp + (size_t)r * (kw / 2) + lane * 16);
+          scl[j] = *reinterpret_cast<const uint2*>(tp + (size_t)kTileR * (kw / 2) + lane * 8);
+        } else {
+#pragma unroll
+          for (int r = 0; r < kTileR; ++r)
+            wv[j][r] = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
+        }
       }
     }
     __syncwarp();
@@ -317,8 +419,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
 #pragma unroll
         for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
       }
-      const int kw = (kt == p.ktiles - 1) ? p.kw_last : kTileK;
-      if (c < kw) {
+      const int kw = (kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
+      if (c >= kw) continue;
+      if (Q4) {
+        const int blk = kt * (kTileKQ4 / 32) + lane;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(qx + blk * 32);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(qx + blk * 32 + 16);
+        const float dxb = dxs[blk];
+        const int sxb = sxs[blk];
+        const uint32_t sc2[2] = {scl[j].x, scl[j].y};
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) {
+          const int idot = q4_block_dot(wv[j][r], x0, x1, sxb);
+          const uint16_t hb = (uint16_t)(r & 1 ? sc2[r >> 1] >> 16 : sc2[r >> 1] & 0xffff);
+          const float sw = __half2float(__ushort_as_half(hb));
+          acc[r] = fmaf(sw * dxb, (float)idot, acc[r]);
+          if (p.dots) p.dots[(size_t)(rb * kTileR + r) * (K / 32) + blk] = idot;
+        }
+      } else {
         const float4 xa = *reinterpret_cast<const float4*>(xs + kt * kTileK + c);
         const float4 xb = *reinterpret_cast<const float4*>(xs + kt * kTileK + c + 4);
 #pragma unroll
@@ -336,9 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
         }
       }
     }
-    st_cur.advance(kStageTiles, p.ktiles);
+    st_cur.advance(kStageTiles, geo.ktiles);
 #pragma unroll
-    for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, p.ktiles);
+    for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, geo.ktiles);
     if (++slot == p.nstages) {
       slot = 0;
       phase ^= 1;
@@ -742,10 +860,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
 
 // ---- launch plumbing -----------------------------------------------------------
 
-const void* gemv_kernel_ptr(int pro, int epi) {
-  if (pro == PRO_NORM && epi == EPI_QKV) return (const void*)gemv_fused<PRO_NORM, EPI_QKV>;
-  if (pro == PRO_PLAIN && epi == EPI_RESID) return (const void*)gemv_fused<PRO_PLAIN, EPI_RESID>;
-  if (pro == PRO_NORM && epi == EPI_SWIGLU) return (const void*)gemv_fused<PRO_NORM, EPI_SWIGLU>;
+const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
+#define TLD_GEMV(P_, E_)                                                        \
+  if (pro == P_ && epi == E_)                                                  \
+    return q4 ? (const void*)gemv_fused<P_, E_, true> : (const void*)gemv_fused<P_, E_, false>;
+  TLD_GEMV(PRO_NORM, EPI_QKV) TLD_GEMV(PRO_PLAIN, EPI_RESID) TLD_GEMV(PRO_NORM, EPI_SWIGLU)
+#undef TLD_GEMV
   return nullptr;
 }
 
@@ -760,8 +880,12 @@ const void* attn_kernel_ptr(int hd, int G) {
 
 cudaError_t set_smem_limits() {
   const int max_smem = 227 * 1024;
-  const void* ks[] = {gemv_kernel_ptr(PRO_NORM, EPI_QKV), gemv_kernel_ptr(PRO_PLAIN, EPI_RESID),
-                      gemv_kernel_ptr(PRO_NORM, EPI_SWIGLU)};
+  const void* ks[] = {gemv_kernel_ptr(PRO_NORM, EPI_QKV, false),
+                      gemv_kernel_ptr(PRO_PLAIN, EPI_RESID, false),
+                      gemv_kernel_ptr(PRO_NORM, EPI_SWIGLU, false),
+                      gemv_kernel_ptr(PRO_NORM, EPI_QKV, true),
+                      gemv_kernel_ptr(PRO_PLAIN, EPI_RESID, true),
+                      gemv_kernel_ptr(PRO_NORM, EPI_SWIGLU, true)};
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
@@ -790,9 +914,9 @@ static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_gemv(int pro, int epi, const GemvParams& p, int grid, size_t smem,
+cudaError_t launch_gemv(int pro, int epi, bool q4, const GemvParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl) {
-  const void* fn = gemv_kernel_ptr(pro, epi);
+  const void* fn = gemv_kernel_ptr(pro, epi, q4);
   if (!fn) return cudaErrorInvalidValue;
   GemvParams copy = p;
   void* args[] = {&copy};
@@ -832,6 +956,39 @@ cudaError_t launch_repack_bf16(const uint16_t* src, int rows, int K, uint8_t* ds
   const int grid = rows < 4096 ? rows : 4096;
   repack_bf16_kernel<<<grid, 256, 0, s>>>(src, rows, K, reinterpret_cast<uint16_t*>(dst_tiled),
                                           dst_row0, kind, hd);
+  return cudaGetLastError();
+}
+
+__device__ __forceinline__ int64_t repack_row(int s, int dst_row0, int kind, int hd) {
+  if (kind == 1) {
+    const int head = s / hd, j = s % hd, half = hd / 2;
+    return dst_row0 + head * hd + (j < half ? 2 * j : 2 * (j - half) + 1);
+  }
+  if (kind == 2) return dst_row0 + 2 * (int64_t)s;
+  return dst_row0 + s;
+}
+
+__global__ void repack_q4_kernel(const uint8_t* __restrict__ nib, const uint16_t* __restrict__ sc,
+                                 int rows, int K, uint8_t* __restrict__ dst, int dst_row0, int kind,
+                                 int hd) {
+  for (int s = blockIdx.x; s < rows; s += gridDim.x) {
+    const int64_t r = repack_row(s, dst_row0, kind, hd);
+    if (nib) {
+      const uint8_t* in = nib + (size_t)s * (K / 2);
+      for (int c2 = threadIdx.x; c2 < K / 2; c2 += blockDim.x) dst[q4_nibble_byte(r, c2, K)] = in[c2];
+    }
+    if (sc) {
+      const uint16_t* in = sc + (size_t)s * (K / 32);
+      for (int bb = threadIdx.x; bb < K / 32; bb += blockDim.x)
+        *reinterpret_cast<uint16_t*>(dst + q4_scale_byte(r, bb, K)) = in[bb];
+    }
+  }
+}
+
+cudaError_t launch_repack_q4(const uint8_t* nibbles, const uint16_t* scales, int rows, int K,
+                             uint8_t* dst_tiled, int dst_row0, int kind, int hd, cudaStream_t s) {
+  const int grid = rows < 4096 ? rows : 4096;
+  repack_q4_kernel<<<grid, 256, 0, s>>>(nibbles, scales, rows, K, dst_tiled, dst_row0, kind, hd);
   return cudaGetLastError();
 }
 

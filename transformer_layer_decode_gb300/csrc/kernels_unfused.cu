@@ -6,6 +6,8 @@
 // keeps": per-op kernels stay the reference).  The ops and their order are the
 // layer chain of "RDNA4 Decode Kernel Fusion: Pipeline Barriers, Not Launches,
 // Are the Win", section "Decode is where the bubble has nowhere to go".
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -155,7 +157,72 @@ __global__ void swiglu_kernel(const float* __restrict__ g, const float* __restri
   if (i < F) a[i] = g[i] / (1.0f + expf(-g[i])) * u[i];
 }
 
+// Per-32 absmax int8 quantisation (one warp per block): dx = amax / 127,
+// q = round-half-even(z / dx) clamped to +-127, natural element order.
+__global__ void quantize_kernel(const float* __restrict__ z, int K, int8_t* __restrict__ qx,
+                                float* __restrict__ dx, int8_t* qtap, float* qstap) {
+  const int blk = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (blk * 32 >= K) return;
+  const float v = z[blk * 32 + lane];
+  const float amax = warp_max(fabsf(v));
+  const float d = __fdiv_rn(amax, 127.0f);
+  int q = 0;
+  if (d != 0.0f) {
+    q = __float2int_rn(__fdiv_rn(v, d));
+    q = q > 127 ? 127 : (q < -127 ? -127 : q);
+  }
+  qx[blk * 32 + lane] = (int8_t)q;
+  if (lane == 0) dx[blk] = d;
+  if (qtap) {
+    qtap[blk * 32 + lane] = (int8_t)q;
+    if (lane == 0) qstap[blk] = d;
+  }
+}
+
+// y = W x for q4 weights in the ABI layout (nibbles [N][K/2], fp16 scales
+// [N][K/32]) and int8 x with block scales: one warp per row, one lane per block.
+__global__ void gemv_q4_kernel(const uint8_t* __restrict__ nib, const uint16_t* __restrict__ sc,
+                               int N, int K, const int8_t* __restrict__ qx,
+                               const float* __restrict__ dx, float* __restrict__ y) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= N) return;
+  const int nb = K / 32;
+  float acc = 0.f;
+  for (int b = lane; b < nb; b += 32) {
+    const uint4 w = *reinterpret_cast<const uint4*>(nib + (size_t)row * (K / 2) + b * 16);
+    const uint4 xa = *reinterpret_cast<const uint4*>(qx + b * 32);
+    const uint4 xb = *reinterpret_cast<const uint4*>(qx + b * 32 + 16);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+    int dot = 0, xsum = 0;
+    for (int i = 0; i < 4; ++i) {
+      // weight word i holds elements 8i..8i+7: low nibbles the even ones
+      const int even = (int)__byte_perm(xw[2 * i], xw[2 * i + 1], 0x6420);
+      const int odd = (int)__byte_perm(xw[2 * i], xw[2 * i + 1], 0x7531);
+      dot = __dp4a((int)(ww[i] & 0x0F0F0F0Fu), even, dot);
+      dot = __dp4a((int)((ww[i] >> 4) & 0x0F0F0F0Fu), odd, dot);
+      xsum = __dp4a(0x01010101, (int)xw[2 * i], xsum);
+      xsum = __dp4a(0x01010101, (int)xw[2 * i + 1], xsum);
+    }
+    const float s = __half2float(__ushort_as_half(sc[(size_t)row * nb + b]));
+    acc = fmaf(s * dx[b], (float)(dot - 8 * xsum), acc);
+  }
+  acc = warp_sum(acc);
+  if (lane == 0) y[row] = acc;
+}
+
 static inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+cudaError_t quantize(const float* z, int K, int8_t* qx, float* dx, int8_t* qtap, float* qstap,
+                     cudaStream_t s) {
+  quantize_kernel<<<cdiv(K / 32, 8), 256, 0, s>>>(z, K, qx, dx, qtap, qstap);
+  return cudaGetLastError();
+}
+cudaError_t gemv_q4(const uint8_t* packed, const uint16_t* scales, int N, int K, const int8_t* qx,
+                    const float* dx, float* y, cudaStream_t s) {
+  gemv_q4_kernel<<<cdiv(N, 8), 256, 0, s>>>(packed, scales, N, K, qx, dx, y);
+  return cudaGetLastError();
+}
 
 cudaError_t rms_scale(const float* x, int H, float eps, float* n, cudaStream_t s) {
   rms_scale_kernel<<<1, 1024, 0, s>>>(x, H, eps, n);

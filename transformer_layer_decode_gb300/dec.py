@@ -27,7 +27,7 @@ KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
                 "norm_gateup_swiglu", "down_residual")
 
 EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_truncate_kv", "dec_step",
-            "dec_set_tap", "dec_set_timeline", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
+            "dec_set_tap", "dec_set_dot_tap", "dec_set_timeline", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
             "dec_destroy", "dec_last_error", "dec_attention_noalloc")
 
 
@@ -74,6 +74,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dec_step": [vp, vp, i32, vp, vp],
         "dec_set_tap": [vp, vp, vp, vp],
         "dec_set_timeline": [vp, vp],
+        "dec_set_dot_tap": [vp, i32, i32, vp],
         "dec_sync_status": [vp, vp],
         "dec_get_info": [vp, ctypes.POINTER(Info)],
         "dec_launch_kernel": [vp, i32, i32, i32, vp],
@@ -181,6 +182,9 @@ class Decoder:
 
     def set_tap(self, per_layer_out=None, qact=None, qscale=None):
         self._check(self.lib.dec_set_tap(self.h, _ptr(per_layer_out), _ptr(qact), _ptr(qscale)))
+
+    def set_dot_tap(self, layer: int = 0, kernel: int = 0, dots=None):
+        self._check(self.lib.dec_set_dot_tap(self.h, layer, kernel, _ptr(dots)))
 
     def set_timeline(self, buf=None):
         self._check(self.lib.dec_set_timeline(self.h, _ptr(buf)))
