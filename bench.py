@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only)")
+    ap.add_argument("--plan", default="fused", choices=["fused", "persistent", "unfused"],
+                    help="fused five-kernel layer, the persistent per-token kernel, or the "
+                         "one-kernel-per-op ablation")
+    ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
     return ap.parse_args()
 
 
@@ -65,15 +69,22 @@ def kernel_bytes(w, kernel: int, n_ctx: int) -> int:
     """Algorithmic bytes of one launch of a fused kernel (weights, norm vector,
     input and output vectors; for attention the K/V rows read and q, o)."""
     H, F, hd, nq, nkv = w.hidden, w.ffn, w.head_dim, w.n_q_heads, w.n_kv_heads
+    bpp = 2.0 if w.weight_fmt == "bf16" else 0.5 + 2.0 / 32  # bytes per weight
     if kernel == 0:
-        return 2 * (nq + 2 * nkv) * hd * H + 2 * H + 4 * H + 4 * nq * hd + 2 * 2 * nkv * hd
+        return int(bpp * (nq + 2 * nkv) * hd * H) + 2 * H + 4 * H + 4 * nq * hd + 2 * 2 * nkv * hd
     if kernel == 1:
         return 2 * 2 * nkv * hd * n_ctx + 4 * nq * hd * 2
     if kernel == 2:
-        return 2 * H * nq * hd + 4 * nq * hd + 4 * H * 2
+        return int(bpp * H * nq * hd) + 4 * nq * hd + 4 * H * 2
     if kernel == 3:
-        return 2 * 2 * F * H + 2 * H + 4 * H + 4 * F
-    return 2 * H * F + 4 * F + 4 * H * 2
+        return int(bpp * 2 * F * H) + 2 * H + 4 * H + 4 * F
+    return int(bpp * H * F) + 4 * F + 4 * H * 2
+
+
+def metric_name(w) -> str:
+    if w.name == "stack32_h4096_mha":
+        return "batch-1 decode tok/s (7B-shape bf16)"
+    return f"batch-1 decode tok/s ({w.name}, {w.weight_fmt})"
 
 
 def measured_peaks():
@@ -270,7 +281,7 @@ def run_reference(args, w, rank, world):
               f"scaled to whole tokens" if n_layers < w.n_layers else
               f"whole tokens at pos {w.prefill}")
     return {
-        "impl": "reference", "metric": "batch-1 decode tok/s (7B-shape bf16)",
+        "impl": "reference", "metric": metric_name(w),
         "value": value, "unit": "tok/s", "n_gpus": args.gpus, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_step * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -295,7 +306,10 @@ def run_ours(args, w, rank, world, local_rank):
     K, W = args.steps, args.warmup
     max_ctx = w.prefill + max(K, W) + 2
     want_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=want_cpu)
+    unfused = args.plan == "unfused"
+    persistent = args.plan == "persistent"
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=want_cpu, unfused=unfused,
+                                    persistent=persistent, graph=not args.eager)
     info = d.info()
     H = w.hidden
     xs = torch.from_numpy(workload.step_inputs(w, max(K, W))).to(dev)
@@ -366,32 +380,40 @@ def run_ours(args, w, rank, world, local_rank):
     assert np.all(np.isfinite(host_out.numpy())), "non-finite decode output"
 
     # ---- dominant kernel alone: back to back over all layers' weights ----------
-    d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)  # warm
-    reps = 3
-    torch.cuda.synchronize()
-    tw0 = time.time()
-    ev0.record(stream)
-    for _ in range(reps):
-        d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)
-    ev1.record(stream)
-    torch.cuda.synchronize()
-    tw1 = time.time()
-    d.sync_status()
-    clocks.mark(tw0, tw1)
-    clocks.stop()
-    k_ms = ev0.elapsed_time(ev1) / (reps * w.n_layers)
     n_ctx = w.prefill + K  # KV length after the timed steps
     kb = kernel_bytes(w, DOMINANT_KERNEL, n_ctx)
     peak, peak_kind = measured_peaks()
-    achieved = kb / (k_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(w.name)
+    if persistent:
+        # one kernel per step: its launches are exactly the timed region's steps
+        kb = bytes_per_token(w, w.prefill + (K + 1) / 2.0)["total"]
+        k_ms = ms / K
+        achieved = kb / (k_ms * 1e-3) / 1e9
+    elif not unfused:
+        d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)  # warm
+        reps = 3
+        torch.cuda.synchronize()
+        tw0 = time.time()
+        ev0.record(stream)
+        for _ in range(reps):
+            d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        tw1 = time.time()
+        d.sync_status()
+        clocks.mark(tw0, tw1)
+        k_ms = ev0.elapsed_time(ev1) / (reps * w.n_layers)
+        achieved = kb / (k_ms * 1e-3) / 1e9
+    else:
+        k_ms, achieved = None, None
+    clocks.stop()
+    traffic = profiled_traffic(w.name) if args.plan == "fused" else None
 
     tok_s = world * K / (ms * 1e-3)
     tok_s_e2e = world * K / (ms_e2e * 1e-3)
     bpt = bytes_per_token(w, w.prefill + (K + 1) / 2.0)
 
     result = {
-        "metric": "batch-1 decode tok/s (7B-shape bf16)",
+        "metric": metric_name(w),
         "value": tok_s, "unit": "tok/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.weight_fmt == "bf16" else "int4/int8",
@@ -400,15 +422,18 @@ def run_ours(args, w, rank, world, local_rank):
                    "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
                    "ffn": w.ffn, "prefill": w.prefill, "batch": 1,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "plan": "fused, CUDA graph", "kernels_per_token": info.kernels_per_token,
+                   "plan": f"{args.plan}, {'eager' if args.eager else 'CUDA graph'}",
+                   "kernels_per_layer": info.kernels_per_layer,
+                   "kernels_per_token": info.kernels_per_token,
                    "l2": "no flush: each step streams %.1f GB of weights + KV (> 129 MB L2)"
                          % (bpt["total"] / 1e9)},
         "hbm": {"bytes_per_token": bpt["total"], "achieved_gbs": bpt["total"] * tok_s / world / 1e9,
                 "peak_gbs": peak, "peak_kind": peak_kind,
                 "frac": bpt["total"] * tok_s / world / 1e9 / peak},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "norm_gateup_swiglu", "bytes_per_launch": kb,
+                     "frac": achieved / peak if achieved else None, "traffic": traffic,
+                     "kernel": "token_persistent" if persistent else "norm_gateup_swiglu",
+                     "bytes_per_launch": kb,
                      "avg_launch_ms": k_ms, "peak_kind": peak_kind},
         "e2e": {"value": tok_s_e2e, "unit": "tok/s", "h2d_bytes_per_step": 4 * H,
                 "d2h_bytes_per_step": 4 * H},

@@ -59,8 +59,13 @@ enum dec_flags {
   DEC_PLAN_FUSED = 0,    /* five kernels per layer (default) */
   DEC_PLAN_UNFUSED = 1,  /* one kernel per op: the ablation / reference chain */
   DEC_NO_GRAPH = 2,      /* launch eagerly instead of replaying a CUDA graph */
-  DEC_NO_PDL = 4         /* fused plan: launch without programmatic dependent launch,
+  DEC_NO_PDL = 4,        /* fused plan: launch without programmatic dependent launch,
                             so each kernel starts only after the previous one ends */
+  DEC_PLAN_PERSISTENT = 8, /* the fused layer's five phases for every layer in one
+                              persistent kernel per step (one CTA per SM, grid barriers
+                              between phases, one weight stream through the step) */
+  DEC_NO_L2_AHEAD = 16     /* fused plan: do not prefetch the next kernel's bytes into L2
+                              at the end of each kernel's stream */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
@@ -92,7 +97,8 @@ typedef struct dec_model_desc {
 } dec_model_desc;
 
 typedef struct dec_info {
-  int32_t kernels_per_layer;  /* launches per layer of the chosen plan */
+  int32_t kernels_per_layer;  /* launches per layer of the chosen plan (1 for the
+                                 persistent plan, whose one launch covers every layer) */
   int32_t kernels_per_token;  /* launches per dec_step */
   int32_t n_sm;               /* SMs the grids are sized for */
   int32_t kv_len;             /* current KV length (next pos) */
@@ -158,7 +164,10 @@ int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots);
  * griddepcontrol.wait, [4] latest arrival of a CTA's first stage, [5] / [6]
  * earliest / latest end of a CTA's streaming loop, [7] earliest CTA end.
  * The caller initialises the min slots (0, 2, 5, 7) to UINT64_MAX and the max
- * slots (1, 3, 4, 6) to 0.
+ * slots (1, 3, 4, 6) to 0.  With DEC_PLAN_PERSISTENT, row i is phase i of the
+ * step (layer * 5 + phase) and records [0] / [1] the earliest / latest return
+ * from the grid barrier before it, [2] / [3] the earliest / latest end of its
+ * work, and row 0 slot [5] the earliest CTA start.
  * Setting it discards the captured graph.  For measurement only ("RDNA4
  * Decode Kernel Fusion", section "What I am building next": GPU timestamps). */
 int dec_set_timeline(dec_handle* h, uint64_t* buf);

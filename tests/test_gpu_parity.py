@@ -14,10 +14,10 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 
-def _check(w, steps, *, unfused=False, graph=True, max_ctx=None):
+def _check(w, steps, *, unfused=False, graph=True, persistent=False, max_ctx=None):
     max_ctx = max_ctx or w.prefill + steps + 2
     d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=unfused, graph=graph,
-                                    keep_host=True)
+                                    persistent=persistent, keep_host=True)
     xs = workload.step_inputs(w, steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -48,16 +48,17 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused"])
+@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused", "persistent"])
 def test_small_shapes(name, mode):
     _check(SMALL[name], SMALL[name].steps, unfused=(mode == "unfused"),
-           graph=(mode != "fused_eager"))
+           graph=(mode != "fused_eager"), persistent=(mode == "persistent"))
 
 
-def test_stack16_h2048_all_steps():
+@pytest.mark.parametrize("persistent", [False, True])
+def test_stack16_h2048_all_steps(persistent):
     """16-layer 1B-shape stack, 64 steps from pos 1023, every layer at every step."""
     w = synth.WORKLOADS["stack16_h2048"]
-    _, worst = _check(w, w.steps)
+    _, worst = _check(w, w.steps, persistent=persistent)
     print("stack16 worst max|err| %.3e rel-L2 %.3e" % worst)
 
 
@@ -66,12 +67,16 @@ def test_plans_agree_and_are_deterministic():
     xs = workload.step_inputs(w, 3)
     outs = {}
     for key, kw in {"graph": {}, "graph2": {}, "eager": {"graph": False},
+                    "persistent": {"persistent": True},
+                    "persistent_eager": {"persistent": True, "graph": False},
                     "unfused": {"unfused": True}}.items():
         d, _ = workload.make_decoder(w, max_ctx=64, **kw)
         outs[key] = run_gpu(d, w, xs)
         d.close()
     assert np.array_equal(outs["graph"], outs["graph2"]), "fused plan not run-to-run identical"
     assert np.array_equal(outs["graph"], outs["eager"]), "graph replay differs from eager launch"
+    assert np.array_equal(outs["graph"], outs["persistent"]), "persistent plan differs from fused"
+    assert np.array_equal(outs["persistent"], outs["persistent_eager"])
     for s in range(3):
         for l in range(w.n_layers):
             assert_close(outs["graph"][s, l], outs["unfused"][s, l], f"fused vs unfused {s},{l}")
@@ -96,14 +101,15 @@ def test_residual_wiring_zero_projections():
             assert np.array_equal(got[s, l], xs[s])
 
 
-def test_io_pointers_can_change_between_steps():
+@pytest.mark.parametrize("persistent", [False, True])
+def test_io_pointers_can_change_between_steps(persistent):
     """The captured graph is re-pointed when the caller passes new buffers."""
     w = SMALL["ragged_g2_empty"]
     xs = workload.step_inputs(w, 3)
     d_ref, _ = workload.make_decoder(w, max_ctx=16, graph=False)
     ref = run_gpu(d_ref, w, xs, taps=False)
     d_ref.close()
-    d, _ = workload.make_decoder(w, max_ctx=16)
+    d, _ = workload.make_decoder(w, max_ctx=16, persistent=persistent)
     outs = []
     for s in range(3):
         emb = torch.from_numpy(xs[s]).cuda()          # a fresh buffer every step

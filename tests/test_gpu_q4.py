@@ -31,12 +31,13 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused"])
+@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused", "persistent"])
 def test_q4_layers_match_oracle(name, mode):
     w = SMALL[name]
     max_ctx = w.prefill + w.steps + 2
     d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=(mode == "unfused"),
-                                    graph=(mode != "fused_eager"), keep_host=True)
+                                    graph=(mode != "fused_eager"),
+                                    persistent=(mode == "persistent"), keep_host=True)
     xs = workload.step_inputs(w, w.steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -65,12 +66,13 @@ def _tiled_to_abi(w, kernel):
     return out
 
 
+@pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("kernel", [0, 2, 3, 4])
-def test_q4_integer_block_dots_bit_exact(kernel):
+def test_q4_integer_block_dots_bit_exact(kernel, persistent):
     w = SMALL["q4_gqa4_d64"]
     layer = 1
     max_ctx = w.prefill + 3
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True)
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, persistent=persistent)
     km = max(w.hidden, w.ffn, w.n_q_heads * w.head_dim)
     qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
     qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")

@@ -15,7 +15,13 @@ namespace tld {
 constexpr uint32_t kWaitLimit = 1u << 22;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-enum ErrBits : int { ERR_FULL_WAIT = 1, ERR_EMPTY_WAIT = 2, ERR_DRAIN = 4, ERR_SPLITS = 8 };
+enum ErrBits : int {
+  ERR_FULL_WAIT = 1,
+  ERR_EMPTY_WAIT = 2,
+  ERR_DRAIN = 4,
+  ERR_SPLITS = 8,
+  ERR_GRID_WAIT = 16
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -60,15 +66,20 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
-// Waits for phase `parity` of `bar` to complete; false once kWaitLimitNs of
-// wall time have passed (measured on %globaltimer, whatever each try_wait's
-// own suspension time is) or after kWaitLimit tries.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Waits for phase `parity` of `bar` to complete.  Gives up (returns false)
+// once kWaitLimitNs of wall time have passed (measured on %globaltimer,
+// whatever each try_wait's own suspension time is), after kWaitLimit tries, or
+// as soon as *abort (an error flag some other wait already raised) is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          const int* abort = nullptr) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1; i < kWaitLimit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if ((i & 63) == 0) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (abort && *reinterpret_cast<const volatile int*>(abort)) return false;
+    }
   }
   return false;
 }

@@ -48,7 +48,7 @@ thread_local std::string g_create_error;
 struct dec_handle {
   dec_model_desc d{};
   int n_sm = 0, G = 0;
-  bool fused = true, graph = true, pdl = true;
+  bool fused = true, graph = true, pdl = true, persistent = false, l2_ahead = true;
   std::vector<LayerDev> layers;
   std::vector<void*> allocs;
   // activations / workspace
@@ -56,6 +56,11 @@ struct dec_handle {
   float *n1 = nullptr, *k = nullptr, *v = nullptr, *g = nullptr, *u = nullptr, *y = nullptr;
   int8_t* qbuf = nullptr;  // unfused q4: int8 GEMV input
   float* dbuf = nullptr;   // and its block scales
+  // persistent plan
+  PLayer* d_players = nullptr;
+  int* d_bar = nullptr;
+  int p_nstages = 0, p_slot = 0;
+  size_t p_smem = 0;
   float* apart = nullptr;  // attention partial records
   int* acount = nullptr;   // attention arrivals per split head
   int att_grid = 0;
@@ -268,6 +273,38 @@ cudaGraphNode_t last_captured_node(cudaStream_t s) {
   return deps[n - 1];
 }
 
+// What kernel `kernel` of layer l prefetches into L2 for the kernel after it.
+L2Ahead l2_ahead_of(const dec_handle* h, int kernel, int l) {
+  L2Ahead a{};
+  if (!h->l2_ahead) return a;
+  const LayerDev& L = h->layers[l];
+  auto rows = [&](const Tiled& t) {
+    a.base = t.w;
+    a.unit_bytes = t.geo.rb_bytes;
+    a.n_units = t.n_rb;
+    a.grid = h->n_sm;
+    a.cap = kL2AheadBytes;
+  };
+  switch (kernel) {
+    case 0:  // attention reads this layer's K/V
+      a.kv = 1;
+      a.base = reinterpret_cast<const uint8_t*>(L.kc);
+      a.vbase = reinterpret_cast<const uint8_t*>(L.vc);
+      a.nkv = h->d.n_kv_heads;
+      a.hd = h->d.head_dim;
+      a.max_ctx = h->d.max_ctx;
+      a.pos = h->d_pos;
+      a.grid = h->att_grid;
+      a.cap = kL2AheadBytes;
+      break;
+    case 1: rows(L.o); break;
+    case 2: rows(L.gu); break;
+    case 3: rows(L.down); break;
+    default: rows(h->layers[(l + 1) % h->d.n_layers].qkv); break;  // the next layer (or token)
+  }
+  return a;
+}
+
 int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, float* out,
                          bool in_step, cudaStream_t s) {
   const int nb = h->n_sm;
@@ -290,6 +327,7 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
     case 0: {
       GemvParams p = k1_params(h, l, first ? emb : h->X, first);
       p.tl = tl;
+      p.ahead = l2_ahead_of(h, 0, l);
       qtaps(p, 0);
       e = launch_gemv(PRO_NORM, EPI_QKV, q4, p, nb, L.qkv.smem, s, h->pdl);
       break;
@@ -297,12 +335,14 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
     case 1: {
       AttnParams p = k2_params(h, l);
       p.tl = tl;
+      p.ahead = l2_ahead_of(h, 1, l);
       e = launch_attn(h->d.head_dim, h->G, p, h->att_grid, h->attn_smem, s, h->pdl);
       break;
     }
     case 2: {
       GemvParams p = k3_params(h, l);
       p.tl = tl;
+      p.ahead = l2_ahead_of(h, 2, l);
       qtaps(p, 1);
       e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.o.smem, s, h->pdl);
       break;
@@ -310,6 +350,7 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
     case 3: {
       GemvParams p = k4_params(h, l);
       p.tl = tl;
+      p.ahead = l2_ahead_of(h, 3, l);
       qtaps(p, 2);
       e = launch_gemv(PRO_NORM, EPI_SWIGLU, q4, p, nb, L.gu.smem, s, h->pdl);
       break;
@@ -317,6 +358,7 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
     case 4: {
       GemvParams p = k5_params(h, l, (in_step && last) ? out : h->X, in_step && last);
       p.tl = tl;
+      p.ahead = l2_ahead_of(h, 4, l);
       qtaps(p, 3);
       e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.down.smem, s, h->pdl);
       break;
@@ -379,9 +421,50 @@ int enqueue_unfused_layer(dec_handle* h, int l, const float* x_in, float* out, b
 constexpr int kUnfusedKernelsPerLayer = 17;
 constexpr int kUnfusedKernelsPerLayerQ4 = 21;
 
+// Parameters of the persistent per-token kernel for one step.
+TokenParams token_params(const dec_handle* h, const float* emb, float* out) {
+  TokenParams P{};
+  const LayerDev& L0 = h->layers[0];
+  P.layers = h->d_players;
+  P.n_layers = h->d.n_layers;
+  P.hidden = h->d.hidden;
+  P.qkv = k1_params(h, 0, emb, false);
+  P.o = k3_params(h, 0);
+  P.gu = k4_params(h, 0);
+  P.down = k5_params(h, 0, out, false);
+  P.down.tap = nullptr;
+  (void)L0;
+  P.attn = k2_params(h, 0);
+  P.att_grid = h->att_grid;
+  P.emb = emb;
+  P.out = out;
+  P.X = h->X;
+  P.tap = h->tap;
+  P.pos = h->d_pos;
+  P.bar = h->d_bar;
+  P.err = h->d_err;
+  P.nstages = h->p_nstages;
+  P.slot_bytes = h->p_slot;
+  P.qtap = h->qtap;
+  P.qstap = h->qstap;
+  P.km = max_k(h->d);
+  P.dots = h->dot_tap;
+  P.dot_layer = h->dot_layer;
+  P.dot_kernel = h->dot_kernel;
+  P.tl = h->timeline;
+  return P;
+}
+
 // Queues one whole token.  Records the first and last kernel nodes when capturing.
 int enqueue_step(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing) {
   const int Lc = h->d.n_layers;
+  if (h->persistent) {
+    cudaError_t e = launch_persistent(h->d.head_dim, h->G, h->d.weight_fmt == DEC_W_Q4B32,
+                                      token_params(h, emb, out), h->n_sm, h->p_smem, s);
+    if (e != cudaSuccess) return cuda_fail(h, e, "persistent kernel launch");
+    if (capturing) h->first_node = h->last_node = last_captured_node(s);
+    return DEC_OK;
+  }
   if (!h->fused) {
     for (int l = 0; l < Lc; ++l) {
       // the unfused chain ping-pongs the residual stream through X
@@ -437,6 +520,22 @@ void set_captured_taps(const dec_handle* h, GemvParams& p, int l, int k) {
 // Points the captured graph at new input / output buffers.
 int patch_io(dec_handle* h, const float* emb, float* out) {
   if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
+  if (h->persistent) {
+    if (emb == h->cap_emb && out == h->cap_out) return DEC_OK;
+    TokenParams P = token_params(h, emb, out);
+    void* args[] = {&P};
+    cudaKernelNodeParams kp{};
+    kp.func = const_cast<void*>(
+        persistent_kernel_ptr(h->d.head_dim, h->G, h->d.weight_fmt == DEC_W_Q4B32));
+    kp.gridDim = dim3(h->n_sm);
+    kp.blockDim = dim3(kThreads);
+    kp.sharedMemBytes = (unsigned)h->p_smem;
+    kp.kernelParams = args;
+    TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->first_node, &kp));
+    h->cap_emb = emb;
+    h->cap_out = out;
+    return DEC_OK;
+  }
   if (emb != h->cap_emb) {
     GemvParams p = k1_params(h, 0, emb, true);
     p.tl = h->timeline;
@@ -471,6 +570,9 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
 
 int set_device_pos(dec_handle* h, int pos) {
   TLD_CUDA(h, cudaMemcpy(h->d_pos, &pos, sizeof(int), cudaMemcpyHostToDevice));
+  // the persistent kernel's barrier counters alternate by position parity:
+  // after a jump of the position both start from zero
+  if (h->d_bar) TLD_CUDA(h, cudaMemset(h->d_bar, 0, 2 * sizeof(int)));
   return DEC_OK;
 }
 
@@ -503,7 +605,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   if (d.weight_fmt == DEC_W_Q4B32 &&
       (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64))
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
-  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL))
+  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -513,6 +615,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->fused = !(d.flags & DEC_PLAN_UNFUSED);
   h->graph = !(d.flags & DEC_NO_GRAPH);
   h->pdl = !(d.flags & DEC_NO_PDL);
+  h->l2_ahead = !(d.flags & DEC_NO_L2_AHEAD);
+  h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
@@ -573,6 +677,10 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   A(&h->dbuf, 4 * (size_t)(km / 32 + 1), &h->ws_bytes);
   A(&h->apart, 4 * (size_t)h->att_grid * 2 * G * (hd + 4), &h->ws_bytes);
   A(&h->acount, 4 * (size_t)nkv, &h->ws_bytes);
+  if (h->persistent) {
+    A(&h->d_players, sizeof(PLayer) * (size_t)d.n_layers, &h->ws_bytes);
+    A(&h->d_bar, 16, &h->ws_bytes);
+  }
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
   A(&h->rope, sizeof(float2) * (size_t)d.max_ctx * (hd / 2), &h->ws_bytes);
@@ -595,6 +703,15 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       }
     e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess && h->persistent) {
+    std::vector<PLayer> pl(d.n_layers);
+    for (int l = 0; l < d.n_layers; ++l) {
+      const LayerDev& L = h->layers[l];
+      pl[l] = PLayer{L.qkv.w, L.o.w, L.gu.w, L.down.w, L.attn_norm, L.ffn_norm, L.kc, L.vc};
+    }
+    e = cudaMemcpy(h->d_players, pl.data(), sizeof(PLayer) * pl.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(h->d_bar, 0, 16);
+  }
   if (e != cudaSuccess) {
     g_create_error = std::string("initialising device buffers: ") + cudaGetErrorString(e);
     dec_destroy(h);
@@ -605,6 +722,30 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
     h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+  }
+  if (h->persistent) {
+    // one ring for every phase: slots as large as the largest stage; the work
+    // area is the largest phase's; all of it within one CTA per SM
+    const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+    h->p_slot = q4 ? kStageBytesQ4 : kStageBytes;
+    if (kAttnStageBytes > h->p_slot) h->p_slot = kAttnStageBytes;
+    h->p_nstages = 1;  // placeholder for the work-size query
+    const size_t work = persistent_work_bytes(token_params(h, nullptr, nullptr), hd, G, q4);
+    int ns = (int)(((size_t)kSmemBudget > work ? kSmemBudget - work : 0) / (h->p_slot + 16));
+    ns = ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    h->p_nstages = ns;
+    h->p_smem = (size_t)ns * h->p_slot + 16 * (size_t)ns + work;
+    int per_sm = 0;
+    const void* fn = persistent_kernel_ptr(hd, G, q4);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)h->p_smem);
+    if (e == cudaSuccess)
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, h->p_smem);
+    if (e != cudaSuccess || per_sm < 1) {
+      g_create_error = std::string("persistent kernel cannot be resident: ") +
+                       (e != cudaSuccess ? cudaGetErrorString(e) : "no room on an SM");
+      dec_destroy(h);
+      return e != cudaSuccess ? DEC_ERR_CUDA : DEC_ERR_SHAPE;
+    }
   }
   *out = h;
   return DEC_OK;
@@ -766,7 +907,7 @@ int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots) {
 
 int dec_set_timeline(dec_handle* h, uint64_t* buf) {
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
-  if (buf && !h->fused) return fail(h, DEC_ERR_STATE, "the timeline probe needs the fused plan");
+  if (buf && !h->fused) return fail(h, DEC_ERR_STATE, "the timeline probe needs a fused plan");
   h->timeline = buf;
   drop_graph(h);
   return DEC_OK;
@@ -786,10 +927,10 @@ int dec_sync_status(dec_handle* h, dec_stream_t stream) {
 
 int dec_get_info(const dec_handle* h, dec_info* info) {
   if (!h || !info) return DEC_ERR_ARG;
-  info->kernels_per_layer = h->fused ? 5
+  info->kernels_per_layer = h->persistent ? 1 : h->fused ? 5
                             : h->d.weight_fmt == DEC_W_Q4B32 ? kUnfusedKernelsPerLayerQ4
                                                              : kUnfusedKernelsPerLayer;
-  info->kernels_per_token = info->kernels_per_layer * h->d.n_layers;
+  info->kernels_per_token = h->persistent ? 1 : info->kernels_per_layer * h->d.n_layers;
   info->n_sm = h->n_sm;
   info->kv_len = h->kv_len;
   info->weight_bytes = h->weight_bytes;
@@ -800,7 +941,8 @@ int dec_get_info(const dec_handle* h, dec_info* info) {
 
 int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream) {
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
-  if (!h->fused) return fail(h, DEC_ERR_STATE, "kernel launches need the fused plan");
+  if (!h->fused || h->persistent)
+    return fail(h, DEC_ERR_STATE, "single-kernel launches need the five-kernel fused plan");
   if (kernel < 0 || kernel > 4 || count < 0 || first_layer < 0 || first_layer >= h->d.n_layers)
     return fail(h, DEC_ERR_ARG, "bad kernel / layer / count");
   const uint32_t need = required_mask(h->d);

@@ -45,6 +45,7 @@ constexpr int kAttnStageBytes = 32768;  // K chunk + V chunk, 16 KB each
 constexpr int kTimelineSlots = 8;       // u64 per launch of the timeline probe
 // Most attention CTAs one KV head may be split over (bounds the merge).
 constexpr int kMaxSplits = 32;
+constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
 constexpr int kStageTiles = 2 * kConsumerWarps;  // two tiles per consumer warp per stage
 constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
 constexpr int kTileBytes = kTileR * kTileK * 2;                          // 2 KB
@@ -103,6 +104,21 @@ __host__ __device__ inline int64_t q4_scale_byte(int64_t r, int64_t b, int K) {
          ((b - kt * (kTileKQ4 / 32)) * kTileR + (r % kTileR)) * 2;
 }
 
+// The next kernel's share of the bytes of one CTA index, fetched into L2 by
+// that CTA's producer once its own stream is issued: HBM keeps streaming
+// through the tail of a kernel (its last stages, epilogue, merge), when the
+// next kernel's CTAs cannot start yet.  GEMV next: units are row blocks of
+// unit_bytes at base.  Attention next: units are K/V chunks of the layer
+// cache at kc / vc (kv != 0).
+struct L2Ahead {
+  const uint8_t* base;  // null: nothing to fetch
+  const uint8_t* vbase;
+  int64_t unit_bytes;
+  int n_units, grid, cap;  // unit count, the next kernel's grid, bytes per CTA at most
+  int kv, nkv, hd, max_ctx;
+  const int* pos;
+};
+
 enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
 enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
 
@@ -135,6 +151,7 @@ struct GemvParams {
   int8_t* qtap;    // [K] natural order, or null
   float* qstap;    // [K/32] block scales, or null
   int32_t* dots;   // [n_rb * kTileR][K/32] integer block dots (tiled row order), or null
+  L2Ahead ahead;
 };
 
 struct AttnParams {
@@ -149,7 +166,50 @@ struct AttnParams {
   int nkv, max_ctx, nstages;
   float scale;
   uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
+  L2Ahead ahead;
 };
+
+// ---- the persistent per-token kernel ---------------------------------------
+struct PLayer {  // per-layer pointers
+  const uint8_t* wqkv;
+  const uint8_t* wo;
+  const uint8_t* wgu;
+  const uint8_t* wd;
+  const uint16_t* attn_norm;
+  const uint16_t* ffn_norm;
+  uint16_t* kc;
+  uint16_t* vc;
+};
+
+struct TokenParams {
+  const PLayer* layers;  // device [n_layers]
+  int n_layers, hidden;
+  // parameter templates of the phases (shapes, geometry, workspace pointers);
+  // the per-layer and per-step pointers are filled in by the kernel
+  GemvParams qkv, o, gu, down;
+  AttnParams attn;
+  int att_grid;          // CTAs taking part in the attention phase
+  const float* emb;      // step input
+  float* out;            // step output
+  float* X;              // residual stream between layers
+  float* tap;            // per-layer outputs [n_layers][hidden] or null
+  int* pos;              // device step position (read at start, +1 at the end)
+  int* bar;              // two grid-barrier counters, alternating by position parity
+  int* err;
+  int nstages, slot_bytes;
+  int8_t* qtap;          // int8 GEMV-input taps [n_layers][4][km] or null
+  float* qstap;
+  int km;
+  int32_t* dots;         // block-dot tap of one GEMV or null
+  int dot_layer, dot_kernel;
+  uint64_t* tl;          // timeline probe [5 * n_layers][kTimelineSlots] or null
+};
+
+size_t persistent_work_bytes(const TokenParams& P, int hd, int G, bool q4);
+const void* persistent_kernel_ptr(int hd, int G, bool q4);
+// Cooperative launch (all CTAs resident) of the persistent kernel.
+cudaError_t launch_persistent(int hd, int G, bool q4, const TokenParams& P, int grid, size_t smem,
+                              cudaStream_t s);
 
 // Shared memory the fused kernels need.
 size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local);

@@ -1,0 +1,893 @@
+// Device-side phases of the decode layer, shared by the five-kernel plan
+// (one phase per kernel launch) and the persistent per-token kernel (all
+// phases of all layers in one launch, separated by grid barriers).
+//
+// Every phase streams its bytes (weights, or K/V rows) through one ring of
+// shared-memory stages: a producer thread fills stages with 1-D bulk copies
+// (TMA) that complete on the stage's "full" mbarrier; the eight consumer warps
+// copy their part of a stage to registers, arrive on its "empty" mbarrier and
+// compute.  A ring position counts stages since the ring was initialised, so
+// one ring can carry the stages of many phases back to back.
+#pragma once
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace tld {
+
+constexpr int kNC = kConsumerWarps * 32;  // consumer threads
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+// ---- the stage ring ----------------------------------------------------------
+struct Ring {
+  uint8_t* stages;
+  uint64_t* full;
+  uint64_t* empty;
+  int n, slot_bytes;
+  __device__ __forceinline__ uint8_t* slot(int s) const { return stages + (size_t)s * slot_bytes; }
+};
+
+struct RingPos {
+  int slot, phase, count;  // count = stages passed since the ring was initialised
+  __device__ __forceinline__ void next(int n) {
+    ++count;
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1;
+    }
+  }
+};
+
+__device__ __forceinline__ void ring_init(const Ring& R) {
+  for (int s = 0; s < R.n; ++s) {
+    mbar_init(&R.full[s], 1);
+    mbar_init(&R.empty[s], kConsumerWarps);
+  }
+  fence_mbar_init();
+}
+
+// Producer: the next slot may be refilled once its previous stage was consumed.
+__device__ __forceinline__ bool ring_reserve(const Ring& R, const RingPos& P, int* err) {
+  if (P.count < R.n) return true;
+  if (mbar_wait(&R.empty[P.slot], P.phase ^ 1, err)) return true;
+  raise_error(err, ERR_EMPTY_WAIT);
+  return false;
+}
+
+// After an error: wait (bounded in time, not cut short by the error flag) for
+// the last copies into every slot, so none lands after the CTA has left.
+__device__ __forceinline__ void ring_drain(const Ring& R, const RingPos& P, int* err) {
+  for (int k = P.count - R.n > 0 ? P.count - R.n : 0; k < P.count; ++k)
+    if (!mbar_wait(&R.full[k % R.n], (k / R.n) & 1)) raise_error(err, ERR_DRAIN);
+}
+
+// ---- GEMV --------------------------------------------------------------------
+// The pointers of a GEMV phase that change from layer to layer (and, for the
+// first and last layer, from step to step); everything else comes from a
+// GemvParams that is the same for every layer.
+struct GemvIO {
+  const uint8_t* w;
+  const uint16_t* norm_w;
+  const float* x;
+  float* x_copy;
+  float* out;
+  float* tap;
+  uint16_t* kc;
+  uint16_t* vc;
+  int8_t* qtap;
+  float* qstap;
+  int32_t* dots;
+};
+
+__device__ __forceinline__ GemvIO gemv_io(const GemvParams& p) {
+  return GemvIO{p.w, p.norm_w, p.x, p.x_copy, p.out, p.tap, p.kc, p.vc, p.qtap, p.qstap, p.dots};
+}
+// Work area of a GEMV phase: x (fp32, K) | [q4: int8 x (K), block scales,
+// block sums] | per-warp row-block partials | warp sums + abort mark.
+struct GemvLayout {
+  int K, max_rb_local;
+  bool q4;
+  __host__ __device__ size_t qx_off() const { return 4 * (size_t)((K + 3) & ~3); }
+  __host__ __device__ size_t dx_off() const { return qx_off() + (q4 ? (size_t)K : 0); }
+  __host__ __device__ size_t sx_off() const { return dx_off() + (q4 ? 4 * (size_t)(K / 32) : 0); }
+  __host__ __device__ size_t part_off() const { return sx_off() + (q4 ? 4 * (size_t)(K / 32) : 0); }
+  __host__ __device__ size_t red_off() const {
+    return part_off() + 4 * (size_t)max_rb_local * kConsumerWarps * kTileR;
+  }
+  __host__ __device__ size_t total() const { return red_off() + 4 * 32; }
+};
+
+struct GemvWork {
+  float* xs;
+  uint8_t* qx;
+  float* dx;
+  int* sx;
+  float* part;
+  float* red;
+  __device__ GemvWork(uint8_t* base, const GemvLayout& L)
+      : xs(reinterpret_cast<float*>(base)),
+        qx(base + L.qx_off()),
+        dx(reinterpret_cast<float*>(base + L.dx_off())),
+        sx(reinterpret_cast<int*>(base + L.sx_off())),
+        part(reinterpret_cast<float*>(base + L.part_off())),
+        red(reinterpret_cast<float*>(base + L.red_off())) {}
+};
+
+// Epilogue of one finished row block (kTileR tiled rows, values v).
+template <int EPI>
+__device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO& io, int rb,
+                                              const float v[kTileR]) {
+  const int R0 = rb * kTileR;
+  if (EPI == EPI_QKV) {
+    const int hd = p.hd, half = hd / 2;
+    const int qrows = p.nq * hd, krows = p.nkv * hd;
+    const int pos = *p.pos;
+    if (R0 < qrows + krows) {
+      // rows (2i, 2i+1) of a head hold dims i and i + hd/2: rotate the pair
+      const bool is_q = R0 < qrows;
+      const int local = is_q ? R0 : R0 - qrows;
+      const int head = local / hd, i0 = (local % hd) / 2;
+      const float2* cs = p.rope + (size_t)pos * half;
+#pragma unroll
+      for (int pr = 0; pr < kTileR / 2; ++pr) {
+        const int i = i0 + pr;
+        const float a = v[2 * pr], b = v[2 * pr + 1];
+        const float2 c = cs[i];
+        const float ra = a * c.x - b * c.y;
+        const float rb2 = a * c.y + b * c.x;
+        if (is_q) {
+          p.q_out[head * hd + i] = ra;
+          p.q_out[head * hd + i + half] = rb2;
+        } else {
+          uint16_t* row = io.kc + ((size_t)head * p.max_ctx + pos) * hd;
+          row[i] = f32_to_bf16_bits(ra);
+          row[i + half] = f32_to_bf16_bits(rb2);
+        }
+      }
+    } else {
+      const int local = R0 - qrows - krows;
+      const int head = local / hd, j = local % hd;
+      uint16_t* row = io.vc + ((size_t)head * p.max_ctx + pos) * hd;
+#pragma unroll
+      for (int r = 0; r < kTileR; ++r) row[j + r] = f32_to_bf16_bits(v[r]);
+    }
+  } else if (EPI == EPI_RESID) {
+#pragma unroll
+    for (int r = 0; r < kTileR; ++r) {
+      const float y = __ldcg(p.resid + R0 + r) + v[r];
+      io.out[R0 + r] = y;
+      if (io.tap) io.tap[R0 + r] = y;
+    }
+  } else {  // EPI_SWIGLU: tiled rows alternate gate and up of the same output
+    const int j = R0 / 2;
+#pragma unroll
+    for (int pr = 0; pr < kTileR / 2; ++pr) p.a_out[j + pr] = silu_f(v[2 * pr]) * v[2 * pr + 1];
+  }
+}
+
+// A position in the tiled matrix, advanced without divisions.
+struct TileCursor {
+  int rb, kt;
+  __device__ __forceinline__ void advance(int n, int ktiles) {
+    kt += n;
+    while (kt >= ktiles) {
+      kt -= ktiles;
+      ++rb;
+    }
+  }
+  // byte offset of the tile from the matrix start
+  __device__ __forceinline__ int64_t offset(const TileGeom& g) const {
+    return (int64_t)rb * g.rb_bytes + (int64_t)kt * g.tile_bytes;
+  }
+};
+
+// Reduce 4 per-lane row accumulators over the warp: each butterfly step keeps
+// half of the rows and hands the other half to the partner lane; lane 8r ends
+// with the total of row r.
+__device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
+  const bool h16 = lane & 16;
+  const float k0 = (h16 ? a[2] : a[0]) + __shfl_xor_sync(0xffffffffu, h16 ? a[0] : a[2], 16);
+  const float k1 = (h16 ? a[3] : a[1]) + __shfl_xor_sync(0xffffffffu, h16 ? a[1] : a[3], 16);
+  const bool h8 = lane & 8;
+  float k = (h8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, h8 ? k0 : k1, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
+// Per-32-block absmax int8 quantization of the fp32 vector xs[K] (K % 32 == 0):
+// dx = amax / 127 (fp32 divide), q = round-half-even(z / dx) clamped to +-127,
+// q = 0 when dx == 0.  Eight lanes serve a block, four elements each.  The int8
+// values are stored for dp4a against packed nibbles: in each group of eight,
+// the even elements first, then the odd ones.  sx holds each block's sum of q.
+__device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, float* dx, int* sx,
+                                int8_t* qtap, float* qstap, int tid, int NC) {
+  const int lane = tid & 31, sub = lane & 7, warp = tid >> 5;
+  const int nblk = K / 32;
+  // Four blocks per warp per round; the round count is the same for all lanes
+  // of a warp (the shuffles below name the whole warp).
+  for (int base = warp * 4; base < nblk; base += (NC >> 5) * 4) {
+    const int blk = base + (lane >> 3);
+    const bool live = blk < nblk;
+    const int e = blk * 32 + sub * 4;
+    const float4 z = live ? *reinterpret_cast<const float4*>(xs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float amax = fmaxf(fmaxf(fabsf(z.x), fabsf(z.y)), fmaxf(fabsf(z.z), fabsf(z.w)));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float d = __fdiv_rn(amax, 127.0f);
+    int q[4];
+    const float zz[4] = {z.x, z.y, z.z, z.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int v = 0;
+      if (d != 0.0f) {
+        v = __float2int_rn(__fdiv_rn(zz[i], d));
+        v = v > 127 ? 127 : (v < -127 ? -127 : v);
+      }
+      q[i] = v;
+    }
+    int sum = q[0] + q[1] + q[2] + q[3];
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    if (!live) continue;
+    // elements e..e+3 = 8g + 4h + {0,1,2,3}: evens go to bytes 8g+2h, 8g+2h+1,
+    // odds to bytes 8g+4+2h, 8g+4+2h+1
+    const int g8 = e & ~7, h = (e >> 2) & 1;
+    *reinterpret_cast<uint16_t*>(qx + g8 + 2 * h) = (uint16_t)((q[0] & 0xff) | ((q[2] & 0xff) << 8));
+    *reinterpret_cast<uint16_t*>(qx + g8 + 4 + 2 * h) =
+        (uint16_t)((q[1] & 0xff) | ((q[3] & 0xff) << 8));
+    if (sub == 0) {
+      dx[blk] = d;
+      sx[blk] = sum;
+    }
+    if (qtap) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) qtap[e + i] = (int8_t)q[i];
+      if (sub == 0) qstap[blk] = d;
+    }
+  }
+}
+
+// Integer dot of one 32-block: packed nibbles (q + 8) against the arranged
+// int8 activations, minus 8 * (sum of the activations).
+__device__ __forceinline__ int q4_block_dot(const uint4 w, const uint4 x0, const uint4 x1, int sx) {
+  constexpr uint32_t M = 0x0F0F0F0Fu;
+  int d = 0;
+  d = __dp4a((int)(w.x & M), (int)x0.x, d);
+  d = __dp4a((int)((w.x >> 4) & M), (int)x0.y, d);
+  d = __dp4a((int)(w.y & M), (int)x0.z, d);
+  d = __dp4a((int)((w.y >> 4) & M), (int)x0.w, d);
+  d = __dp4a((int)(w.z & M), (int)x1.x, d);
+  d = __dp4a((int)((w.z >> 4) & M), (int)x1.y, d);
+  d = __dp4a((int)(w.w & M), (int)x1.z, d);
+  d = __dp4a((int)((w.w >> 4) & M), (int)x1.w, d);
+  return d - 8 * sx;
+}
+
+// Producer of a GEMV phase: this CTA's slab, whole row blocks [rb0, rb1).
+__device__ __forceinline__ void gemv_produce(const GemvParams& p, const uint8_t* w, const Ring& R,
+                                             RingPos& P, int rb0, int rb1, uint64_t pol) {
+  const TileGeom& geo = p.geo;
+  const int nloc = (rb1 - rb0) * geo.ktiles;
+  const int nst = (nloc + kStageTiles - 1) / kStageTiles;
+  TileCursor cur{rb0, 0};
+  const int64_t end_off = (int64_t)rb1 * geo.rb_bytes;
+  for (int s = 0; s < nst; ++s) {
+    if (!ring_reserve(R, P, p.err)) return;
+    const int64_t oa = cur.offset(geo);
+    cur.advance(kStageTiles, geo.ktiles);
+    const int64_t ob = (s == nst - 1) ? end_off : cur.offset(geo);
+    const uint32_t bytes = (uint32_t)(ob - oa);
+    mbar_arrive_expect_tx(&R.full[P.slot], bytes);
+    bulk_g2s_hint(R.slot(P.slot), w + oa, bytes, &R.full[P.slot], pol);
+    P.next(R.n);
+  }
+}
+
+// L2 prefetch of this CTA index's share of the next kernel (see L2Ahead).
+template <int HD>
+__device__ void l2_ahead_kv(const L2Ahead& a, int b);
+
+__device__ __forceinline__ void l2_ahead(const L2Ahead& a, int b) {
+  if (!a.base || b >= a.grid) return;
+  if (a.kv) {
+    if (a.hd == 64) l2_ahead_kv<64>(a, b);
+    else l2_ahead_kv<128>(a, b);
+    return;
+  }
+  const int64_t r0 = split_begin(a.n_units, a.grid, b), r1 = split_begin(a.n_units, a.grid, b + 1);
+  int64_t left = (r1 - r0) * a.unit_bytes;
+  if (left > a.cap) left = a.cap;
+  // 16-byte aligned start (the buffers themselves are)
+  const int64_t start = r0 * a.unit_bytes, lead = start & 15;
+  const uint8_t* src = a.base + (start - lead);
+  left = (left + lead) & ~(int64_t)15;
+  for (int64_t o = 0; o < left; o += kStageBytes) {
+    const int64_t n = left - o < kStageBytes ? left - o : kStageBytes;
+    bulk_prefetch_l2(src + o, (uint32_t)n);
+  }
+}
+
+// Consumer work of a GEMV phase that does not depend on its input vector:
+// the RMSNorm weights (static) go to xs as fp32; the partials are cleared.
+template <int PRO>
+__device__ __forceinline__ void gemv_pre(const GemvParams& p, const uint16_t* norm_w,
+                                         const GemvWork& W, int tid) {
+  const int K4 = p.geo.K / 4;
+  if (PRO == PRO_NORM) {
+    const uint2* w4 = reinterpret_cast<const uint2*>(norm_w);
+    for (int k4 = tid; k4 < K4; k4 += kNC) {
+      const uint2 wb = w4[k4];
+      reinterpret_cast<float4*>(W.xs)[k4] =
+          make_float4(bf16lo(wb.x), bf16hi(wb.x), bf16lo(wb.y), bf16hi(wb.y));
+    }
+  }
+  for (int i = tid; i < p.max_rb_local * kConsumerWarps * kTileR; i += kNC) W.part[i] = 0.f;
+  if (tid == 0) W.red[kConsumerWarps] = 0.f;
+}
+
+// Consumer part of a GEMV phase once its input vector is ready: the prologue
+// (input, RMSNorm, quantisation), the streaming loop over this CTA's tiles and
+// the row-block epilogue.  Returns false if a wait ran out.
+template <int PRO, int EPI, bool Q4>
+__device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io, const GemvWork& W,
+                                          const Ring& R, RingPos& P, int rb0, int rb1, int tid,
+                                          bool first_cta) {
+  const TileGeom& geo = p.geo;
+  const int K = geo.K, K4 = K / 4;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nrb = rb1 - rb0;
+  const int nloc = nrb * geo.ktiles;
+  const int nst = (nloc + kStageTiles - 1) / kStageTiles;
+  float* xs = W.xs;
+  {
+    // the input vector was written by another phase: read it from L2
+    const float4* x4 = reinterpret_cast<const float4*>(io.x);
+    float ss = 0.f;
+    constexpr int PB = 4;  // loads in flight per thread
+    for (int base = tid; base < K4; base += kNC * PB) {
+      float4 v[PB];
+#pragma unroll
+      for (int u = 0; u < PB; ++u)
+        if (base + u * kNC < K4) v[u] = __ldcg(x4 + base + u * kNC);
+#pragma unroll
+      for (int u = 0; u < PB; ++u) {
+        const int k4 = base + u * kNC;
+        if (k4 >= K4) continue;
+        if (PRO == PRO_NORM) {
+          ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+          float4 w = reinterpret_cast<float4*>(xs)[k4];
+          w.x *= v[u].x;
+          w.y *= v[u].y;
+          w.z *= v[u].z;
+          w.w *= v[u].w;
+          reinterpret_cast<float4*>(xs)[k4] = w;
+        } else {
+          reinterpret_cast<float4*>(xs)[k4] = v[u];
+        }
+      }
+    }
+    if (PRO == PRO_NORM) {
+      ss = warp_sum(ss);
+      if (lane == 0) W.red[warp] = ss;
+    }
+  }
+  if (io.x_copy && first_cta) {
+    for (int k = tid; k < K; k += kNC) io.x_copy[k] = __ldcg(io.x + k);
+  }
+  if (p.pos_advance && first_cta && tid == 0) atomicAdd(p.pos_advance, 1);
+  named_barrier(1, kNC);
+
+  // RMSNorm is a per-vector scale 1/sqrt(mean(x^2)+eps).  bf16 weights: the
+  // projection runs on x*w and the scale multiplies the finished rows.  q4
+  // weights: the normalised vector itself is quantised, so it is scaled first.
+  float rnorm = 1.f;
+  if (PRO == PRO_NORM) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kConsumerWarps; ++w) tot += W.red[w];
+    rnorm = 1.0f / sqrtf(tot / (float)K + p.eps);
+  }
+  if (Q4) {
+    if (PRO == PRO_NORM) {
+      for (int k4 = tid; k4 < K4; k4 += kNC) {
+        float4 v = reinterpret_cast<float4*>(xs)[k4];
+        v.x *= rnorm;
+        v.y *= rnorm;
+        v.z *= rnorm;
+        v.w *= rnorm;
+        reinterpret_cast<float4*>(xs)[k4] = v;
+      }
+      named_barrier(1, kNC);
+      rnorm = 1.f;
+    }
+    quantize_blocks(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid, kNC);
+    named_barrier(1, kNC);
+  }
+
+  int cur_rb = -1;
+  float acc[kTileR];
+#pragma unroll
+  for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
+  bool ok = true;
+  // cursors: the first tile of the current stage and this warp's two tiles in it
+  TileCursor st_cur{rb0, 0};
+  TileCursor my[kTilesPerWarp];
+#pragma unroll
+  for (int j = 0; j < kTilesPerWarp; ++j) {
+    my[j] = st_cur;
+    my[j].advance(warp + j * kConsumerWarps, geo.ktiles);
+  }
+  // bf16: lane owns columns [8 lane, 8 lane + 8) of a tile; q4: lane owns block `lane`
+  const int c = Q4 ? lane * 32 : lane * 8;
+  for (int s = 0; s < nst; ++s) {
+    // After a timed-out wait the warp stops waiting but keeps the same control
+    // flow, so that every named barrier below is still reached by all warps.
+    if (ok && !mbar_wait(&R.full[P.slot], P.phase, p.err)) {
+      raise_error(p.err, ERR_FULL_WAIT);
+      ok = false;
+    }
+    if (s == 0 && tid == 0) tl_mark_max(p.tl, 4);
+    // Copy this warp's tiles into registers and hand the slot back at once, so
+    // the next bulk copy is in flight while the arithmetic runs.
+    uint4 wv[kTilesPerWarp][kTileR];
+    uint2 scl[kTilesPerWarp];
+    const int64_t st_off = st_cur.offset(geo);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int li = s * kStageTiles + warp + j * kConsumerWarps;
+      const int kw = (my[j].kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
+      if (li < nloc && c < kw) {
+        const uint8_t* tp = R.slot(P.slot) + (my[j].offset(geo) - st_off);
+        if (Q4) {
+#pragma unroll
+          for (int r = 0; r < kTileR; ++r)
+            wv[j][r] = *reinterpret_cast<const uint4*>(tp + (size_t)r * (kw / 2) + lane * 16);
+          scl[j] = *reinterpret_cast<const uint2*>(tp + (size_t)kTileR * (kw / 2) + lane * 8);
+        } else {
+#pragma unroll
+          for (int r = 0; r < kTileR; ++r)
+            wv[j][r] = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[P.slot]);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) {
+      const int li = s * kStageTiles + warp + j * kConsumerWarps;
+      if (li >= nloc) continue;
+      const int rb = my[j].rb, kt = my[j].kt;
+      if (rb != cur_rb) {
+        if (cur_rb >= 0) {
+          const float v = warp_reduce4(acc, lane);
+          if ((lane & 7) == 0)
+            W.part[((cur_rb - rb0) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
+        }
+        cur_rb = rb;
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
+      }
+      const int kw = (kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
+      if (c >= kw) continue;
+      if (Q4) {
+        const int blk = kt * (kTileKQ4 / 32) + lane;
+        const uint4 x0 = *reinterpret_cast<const uint4*>(W.qx + blk * 32);
+        const uint4 x1 = *reinterpret_cast<const uint4*>(W.qx + blk * 32 + 16);
+        const float dxb = W.dx[blk];
+        const int sxb = W.sx[blk];
+        const uint32_t sc2[2] = {scl[j].x, scl[j].y};
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) {
+          const int idot = q4_block_dot(wv[j][r], x0, x1, sxb);
+          const uint16_t hb = (uint16_t)(r & 1 ? sc2[r >> 1] >> 16 : sc2[r >> 1] & 0xffff);
+          const float sw = __half2float(__ushort_as_half(hb));
+          acc[r] = fmaf(sw * dxb, (float)idot, acc[r]);
+          if (io.dots) io.dots[(size_t)(rb * kTileR + r) * (K / 32) + blk] = idot;
+        }
+      } else {
+        const float4 xa = *reinterpret_cast<const float4*>(xs + kt * kTileK + c);
+        const float4 xb = *reinterpret_cast<const float4*>(xs + kt * kTileK + c + 4);
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) {
+          float a = acc[r];
+          a = fmaf(bf16lo(wv[j][r].x), xa.x, a);
+          a = fmaf(bf16hi(wv[j][r].x), xa.y, a);
+          a = fmaf(bf16lo(wv[j][r].y), xa.z, a);
+          a = fmaf(bf16hi(wv[j][r].y), xa.w, a);
+          a = fmaf(bf16lo(wv[j][r].z), xb.x, a);
+          a = fmaf(bf16hi(wv[j][r].z), xb.y, a);
+          a = fmaf(bf16lo(wv[j][r].w), xb.z, a);
+          a = fmaf(bf16hi(wv[j][r].w), xb.w, a);
+          acc[r] = a;
+        }
+      }
+    }
+    st_cur.advance(kStageTiles, geo.ktiles);
+#pragma unroll
+    for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, geo.ktiles);
+    P.next(R.n);
+  }
+  if (cur_rb >= 0) {
+    const float v = warp_reduce4(acc, lane);
+    if ((lane & 7) == 0)
+      W.part[((cur_rb - rb0) * kConsumerWarps + warp) * kTileR + (lane >> 3)] = v;
+  }
+  if (!ok && lane == 0) W.red[kConsumerWarps] = 1.f;  // abort mark
+  named_barrier(1, kNC);
+  if (tid == 0) {
+    tl_mark_min(p.tl, 5);
+    tl_mark_max(p.tl, 6);
+  }
+  if (W.red[kConsumerWarps] != 0.f) return false;
+
+  // ---- finish this CTA's row blocks (sum over warps in warp order) ------------
+  for (int j = tid; j < nrb; j += kNC) {
+    float v[kTileR];
+#pragma unroll
+    for (int r = 0; r < kTileR; ++r) {
+      float sum = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) sum += W.part[(j * kConsumerWarps + w) * kTileR + r];
+      v[r] = sum * rnorm;
+    }
+    gemv_epilogue<EPI>(p, io, rb0 + j, v);
+  }
+  return true;
+}
+
+// ---- attention ---------------------------------------------------------------
+// One unit = one chunk of CH cached positions of one KV head (its K rows, then
+// its V rows, 16 KB each).  The grid splits the units of all KV heads evenly;
+// every CTA serves all G query heads of the KV heads it touches, so each K/V
+// byte is read once.  Within a CTA the 8 consumer warps take interleaved
+// positions of each chunk and keep a running (max, sum, acc) per query head;
+// warps are merged at the end of each head segment, and a head cut between
+// CTAs is merged, after its loop, by the last of its CTAs to finish.
+
+// Work area of an attention phase: per-warp states | merge scratch.
+struct AttnLayout {
+  int hd, G;
+  __host__ __device__ size_t merge_off() const {
+    return 4 * (size_t)kConsumerWarps * G * (hd + 2);
+  }
+  // the record offsets of the splits of two heads, then the heads to merge
+  __host__ __device__ size_t total() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
+};
+
+// This CTA's share of the attention units at KV length n.
+struct AttnSplit {
+  int n, cph, U, u0, u1, nu;
+};
+
+template <int HD>
+__device__ __forceinline__ AttnSplit attn_split(int pos, int nkv, int b, int nb) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
+  AttnSplit S;
+  S.n = pos + 1;
+  S.cph = (S.n + CH - 1) / CH;
+  S.U = nkv * S.cph;
+  S.u0 = split_begin32(S.U, nb, b);
+  S.u1 = split_begin32(S.U, nb, b + 1);
+  S.nu = S.u1 - S.u0;
+  return S;
+}
+
+template <int HD>
+__device__ void l2_ahead_kv(const L2Ahead& a, int b) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
+  const AttnSplit S = attn_split<HD>(*a.pos, a.nkv, b, a.grid);
+  int left = a.cap;
+  int u = S.u0;
+  while (u < S.u1 && left > 0) {
+    // one head segment: its chunks are contiguous in K and in V
+    const int g = u / S.cph, c0 = u - g * S.cph;
+    const int c1 = min(S.cph, c0 + (S.u1 - u));
+    const int rows = min(c1 * CH, S.n) - c0 * CH;
+    int bytes = rows * HD * 2;
+    if (bytes > left / 2) bytes = left / 2;
+    const size_t off = ((size_t)g * a.max_ctx + (size_t)c0 * CH) * HD * 2;
+    for (int o = 0; o < bytes; o += kStageBytes) {
+      const uint32_t n = (uint32_t)min(bytes - o, kStageBytes) & ~15u;
+      bulk_prefetch_l2(a.base + off + o, n);
+      bulk_prefetch_l2(a.vbase + off + o, n);
+    }
+    left -= 2 * bytes;
+    u += c1 - c0;
+  }
+}
+
+// DL consecutive bf16 of one cached row, as raw bits (DL = 2 or 4).
+template <int DL>
+struct RowSlice {
+  uint32_t w[DL / 2];
+  __device__ __forceinline__ void load(const uint8_t* p) {
+    if (DL == 4) {
+      const uint2 v = *reinterpret_cast<const uint2*>(p);
+      w[0] = v.x;
+      w[DL / 2 - 1] = v.y;
+    } else {
+      w[0] = *reinterpret_cast<const uint32_t*>(p);
+    }
+  }
+  __device__ __forceinline__ void unpack(float* f) const {
+#pragma unroll
+    for (int i = 0; i < DL / 2; ++i) {
+      f[2 * i] = bf16lo(w[i]);
+      f[2 * i + 1] = bf16hi(w[i]);
+    }
+  }
+};
+
+// Producer of an attention phase: this CTA's chunks.  wait_pos() is called
+// once before the first chunk that holds the row appended by this step's QKV
+// phase (the other rows were written by earlier steps).
+template <int HD, class WaitPos>
+__device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t* kc,
+                                             const uint16_t* vc, const Ring& R, RingPos& P,
+                                             const AttnSplit& S, uint64_t pol, WaitPos&& wait_pos) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
+  bool waited = false;
+  int g = S.u0 / S.cph, c = S.u0 - g * S.cph;
+  for (int s = 0; s < S.nu; ++s) {
+    if (!ring_reserve(R, P, p.err)) return;
+    const int rows = min(CH, S.n - c * CH);
+    if (c == S.cph - 1 && !waited) {
+      wait_pos();
+      waited = true;
+    }
+    const size_t off = ((size_t)g * p.max_ctx + (size_t)c * CH) * HD;
+    const uint32_t bytes = (uint32_t)rows * HD * 2;
+    mbar_arrive_expect_tx(&R.full[P.slot], 2 * bytes);
+    uint8_t* dst = R.slot(P.slot);
+    bulk_g2s_hint(dst, kc + off, bytes, &R.full[P.slot], pol);
+    bulk_g2s_hint(dst + kAttnStageBytes / 2, vc + off, bytes, &R.full[P.slot], pol);
+    if (++c == S.cph) {
+      c = 0;
+      ++g;
+    }
+    P.next(R.n);
+  }
+}
+
+// Consumer part of an attention phase (q must be ready).  Returns false if a
+// wait ran out.
+template <int HD, int G>
+__device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, const Ring& R, RingPos& P,
+                          const AttnSplit& S, int b, int nb, int tid) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);  // positions per chunk (16 KB of K)
+  constexpr int PW = CH / kConsumerWarps;              // positions per warp per chunk
+  constexpr int SUB = 4;                               // positions per online-softmax update
+  constexpr int DL = HD / 32;                          // dims per lane
+  const int warp = tid >> 5, lane = tid & 31;
+  float* ws = reinterpret_cast<float*>(work);  // [warp][G][HD+2]
+  const int n = S.n, cph = S.cph, U = S.U, u0 = S.u0, u1 = S.u1, nu = S.nu;
+  float m[G], l[G], acc[G][DL];
+  int cur_g = -1, seg_idx = 0;
+  auto reset = [&]() {
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      m[gg] = -INFINITY;
+      l[gg] = 0.f;
+#pragma unroll
+      for (int j = 0; j < DL; ++j) acc[gg][j] = 0.f;
+    }
+  };
+  float qr[G][DL];
+  // Ends the segment of KV head g: merge the warps' states; a head this CTA
+  // covered whole is normalised into o, a split head leaves a partial record
+  // (acc, m, l), merged after the loop by the last CTA of the head to finish.
+  int split_heads[2] = {-1, -1};
+  auto end_segment = [&](int g) {
+#pragma unroll
+    for (int gg = 0; gg < G; ++gg) {
+      float* w = ws + ((size_t)warp * G + gg) * (HD + 2);
+#pragma unroll
+      for (int j = 0; j < DL; ++j) w[lane * DL + j] = acc[gg][j];
+      if (lane == 0) {
+        w[HD] = m[gg];
+        w[HD + 1] = l[gg];
+      }
+    }
+    named_barrier(1, kNC);
+    const int64_t h0 = (int64_t)g * cph, h1 = h0 + cph;
+    const bool whole = h0 >= u0 && h1 <= u1;
+    if (!whole) split_heads[seg_idx == 0 ? 0 : 1] = g;
+    float* rec = p.part + ((size_t)b * 2 + (seg_idx == 0 ? 0 : 1)) * G * (HD + 4);
+    for (int i = tid; i < G * HD; i += kNC) {
+      const int gg = i / HD, j = i % HD;
+      float M = -INFINITY;
+      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws[(w * G + gg) * (HD + 2) + HD]);
+      float A = 0.f, Ls = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float* wr = ws + (w * G + gg) * (HD + 2);
+        const float e = (wr[HD] == -INFINITY) ? 0.f : expf(wr[HD] - M);
+        A += wr[j] * e;
+        Ls += wr[HD + 1] * e;
+      }
+      if (whole) {
+        p.o[(size_t)(g * G + gg) * HD + j] = A / Ls;
+      } else {
+        rec[gg * (HD + 4) + j] = A;
+        if (j == 0) {
+          rec[gg * (HD + 4) + HD] = M;
+          rec[gg * (HD + 4) + HD + 1] = Ls;
+        }
+      }
+    }
+    // The records are released to the other CTAs by the ticket below: this
+    // barrier orders every thread's writes before thread 0's gpu-scope release.
+    named_barrier(1, kNC);
+    ++seg_idx;
+  };
+
+  reset();
+  bool ok = true;
+  int g = u0 / cph, c = u0 - g * cph;
+  for (int s = 0; s < nu; ++s) {
+    if (g != cur_g) {
+      if (cur_g >= 0) {
+        end_segment(cur_g);
+        reset();
+      }
+      cur_g = g;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg)
+#pragma unroll
+        for (int j = 0; j < DL; ++j) qr[gg][j] = __ldcg(p.q + (size_t)(g * G + gg) * HD + lane * DL + j) * p.scale;
+    }
+    if (ok && !mbar_wait(&R.full[P.slot], P.phase, p.err)) {
+      raise_error(p.err, ERR_FULL_WAIT);
+      ok = false;  // keep the control flow (segment barriers) uniform
+    }
+    if (s == 0 && tid == 0) tl_mark_max(p.tl, 4);
+    const int rows = min(CH, n - c * CH);
+    const uint8_t* kb = R.slot(P.slot);
+    const uint8_t* vb = kb + kAttnStageBytes / 2;
+    // This warp's K and V row slices into registers, then the slot goes back.
+    RowSlice<DL> kr[PW], vr[PW];
+#pragma unroll
+    for (int i = 0; i < PW; ++i) {
+      const int t = warp + i * kConsumerWarps;
+      if (t < rows) {
+        kr[i].load(kb + ((size_t)t * HD + lane * DL) * 2);
+        vr[i].load(vb + ((size_t)t * HD + lane * DL) * 2);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[P.slot]);
+#pragma unroll
+    for (int i0 = 0; i0 < PW; i0 += SUB) {
+      if (warp + i0 * kConsumerWarps >= rows) break;  // warp-uniform
+      float sc[SUB][G];
+#pragma unroll
+      for (int i = 0; i < SUB; ++i) {
+        const int t = warp + (i0 + i) * kConsumerWarps;
+        float kv[DL];
+        kr[i0 + i].unpack(kv);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          float d = 0.f;
+#pragma unroll
+          for (int j = 0; j < DL; ++j) d = fmaf(qr[gg][j], kv[j], d);
+          d = warp_sum(d);
+          sc[i][gg] = (t < rows) ? d : -INFINITY;
+        }
+      }
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        float mx = m[gg];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) mx = fmaxf(mx, sc[i][gg]);
+        const float alpha = (m[gg] == -INFINITY) ? 0.f : expf(m[gg] - mx);
+        float ls = l[gg] * alpha;
+#pragma unroll
+        for (int j = 0; j < DL; ++j) acc[gg][j] *= alpha;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+          const int t = warp + (i0 + i) * kConsumerWarps;
+          if (t >= rows) continue;
+          const float pi = expf(sc[i][gg] - mx);
+          ls += pi;
+          float vv[DL];
+          vr[i0 + i].unpack(vv);
+#pragma unroll
+          for (int j = 0; j < DL; ++j) acc[gg][j] = fmaf(pi, vv[j], acc[gg][j]);
+        }
+        m[gg] = mx;
+        l[gg] = ls;
+      }
+    }
+    if (++c == cph) {
+      c = 0;
+      ++g;
+    }
+    P.next(R.n);
+  }
+  if (tid == 0) {
+    tl_mark_min(p.tl, 5);
+    tl_mark_max(p.tl, 6);
+  }
+  if (cur_g >= 0) end_segment(cur_g);
+
+  // ---- heads split over CTAs: the last CTA to finish merges them --------------
+  // (tickets are taken after this CTA's whole loop, so merging never stalls it;
+  // the split arithmetic is 32-bit: units * grid stays far below 2^31)
+  int* mbase = reinterpret_cast<int*>(work + AttnLayout{HD, G}.merge_off());  // [2][kMaxSplits]
+  int* todo = mbase + 2 * kMaxSplits;                                         // [2]: head, splits
+  const int U32 = U;
+  auto part_begin = [&](int c) { return split_begin32(U32, nb, c); };
+  if (tid < 2) {
+    // thread i takes the ticket of this CTA's i-th split head (both in flight at once)
+    const int g = split_heads[tid];
+    int head = -1;
+    if (g >= 0) {
+      const int c_lo = split_owner32(U32, nb, g * cph), c_hi = split_owner32(U32, nb, (g + 1) * cph - 1);
+      int expected = 0;
+      for (int c = c_lo; c <= c_hi; ++c) expected += part_begin(c + 1) > part_begin(c);
+      // release this CTA's record, acquire the others'
+      if (atomic_add_acq_rel(&p.counters[g], 1) == expected - 1) head = g;
+    }
+    todo[tid] = head;
+  }
+  named_barrier(1, kNC);
+  // record offset of every split of the heads to merge
+  for (int t = tid; t < 2 * kMaxSplits; t += kNC) {
+    const int i = t / kMaxSplits, sp = t - i * kMaxSplits, g = todo[i];
+    int off = -1;
+    if (g >= 0) {
+      const int h0 = g * cph, c_lo = split_owner32(U32, nb, h0);
+      const int c_hi = split_owner32(U32, nb, h0 + cph - 1);
+      if (sp == 0 && c_hi - c_lo + 1 > kMaxSplits) raise_error(p.err, ERR_SPLITS);
+      const int c = c_lo + sp;
+      if (c <= c_hi) {
+        const int cs = part_begin(c);
+        if (part_begin(c + 1) > cs) off = ((c * 2 + (cs >= h0 ? 0 : 1)) * G) * (HD + 4);
+      }
+    }
+    mbase[t] = off;
+  }
+  named_barrier(1, kNC);
+  // both heads at once; one round trip: each output loads every split's
+  // (m, l, acc) together, then combines them in split order
+  for (int t = tid; t < 2 * G * HD; t += kNC) {
+    const int i = t / (G * HD), e = t - i * G * HD;
+    const int g = todo[i];
+    if (g < 0) continue;
+    const int gg = e / HD, j = e - gg * HD;
+    const int* mb = mbase + i * kMaxSplits;
+    float mv[kMaxSplits], lv[kMaxSplits], av[kMaxSplits];
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) {
+      mv[sp] = -INFINITY;
+      lv[sp] = 0.f;
+      av[sp] = 0.f;
+      const int off = mb[sp];
+      if (off >= 0) {
+        const float* rec = p.part + off + gg * (HD + 4);
+        mv[sp] = __ldcg(rec + HD);
+        lv[sp] = __ldcg(rec + HD + 1);
+        av[sp] = __ldcg(rec + j);
+      }
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) M = fmaxf(M, mv[sp]);
+    float Lsum = 0.f, o = 0.f;
+#pragma unroll
+    for (int sp = 0; sp < kMaxSplits; ++sp) {
+      const float w = (mv[sp] == -INFINITY) ? 0.f : expf(mv[sp] - M);
+      Lsum = fmaf(lv[sp], w, Lsum);
+      o = fmaf(av[sp], w, o);
+    }
+    p.o[(size_t)(g * G + gg) * HD + j] = o / Lsum;
+  }
+  if (tid < 2 && todo[tid] >= 0) p.counters[todo[tid]] = 0;
+  named_barrier(1, kNC);
+  return ok;
+}
+
+}  // namespace tld
