@@ -64,8 +64,12 @@ enum dec_flags {
   DEC_PLAN_PERSISTENT = 8, /* the fused layer's five phases for every layer in one
                               persistent kernel per step (one CTA per SM, grid barriers
                               between phases, one weight stream through the step) */
-  DEC_NO_L2_AHEAD = 16     /* fused plan: do not prefetch the next kernel's bytes into L2
+  DEC_NO_L2_AHEAD = 16,    /* fused plan: do not prefetch the next kernel's bytes into L2
                               at the end of each kernel's stream */
+  DEC_ATTN_GLOBAL_MERGE = 32 /* fused plan: attention over a flat grid whose split heads are
+                                merged through global memory by the last CTA of each head,
+                                instead of one thread-block cluster per KV head merging in
+                                distributed shared memory */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16

@@ -14,10 +14,12 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 
-def _check(w, steps, *, unfused=False, graph=True, persistent=False, max_ctx=None):
+def _check(w, steps, *, unfused=False, graph=True, persistent=False, cluster_attn=True,
+           max_ctx=None):
     max_ctx = max_ctx or w.prefill + steps + 2
     d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=unfused, graph=graph,
-                                    persistent=persistent, keep_host=True)
+                                    persistent=persistent, cluster_attn=cluster_attn,
+                                    keep_host=True)
     xs = workload.step_inputs(w, steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -48,10 +50,12 @@ SMALL = {
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "global_merge", "unfused",
+                                  "persistent"])
 def test_small_shapes(name, mode):
     _check(SMALL[name], SMALL[name].steps, unfused=(mode == "unfused"),
-           graph=(mode != "fused_eager"), persistent=(mode == "persistent"))
+           graph=(mode != "fused_eager"), persistent=(mode == "persistent"),
+           cluster_attn=(mode != "global_merge"))
 
 
 @pytest.mark.parametrize("persistent", [False, True])
@@ -67,6 +71,7 @@ def test_plans_agree_and_are_deterministic():
     xs = workload.step_inputs(w, 3)
     outs = {}
     for key, kw in {"graph": {}, "graph2": {}, "eager": {"graph": False},
+                    "global_merge": {"cluster_attn": False}, "no_l2_ahead": {"l2_ahead": False},
                     "persistent": {"persistent": True},
                     "persistent_eager": {"persistent": True, "graph": False},
                     "unfused": {"unfused": True}}.items():
@@ -75,8 +80,13 @@ def test_plans_agree_and_are_deterministic():
         d.close()
     assert np.array_equal(outs["graph"], outs["graph2"]), "fused plan not run-to-run identical"
     assert np.array_equal(outs["graph"], outs["eager"]), "graph replay differs from eager launch"
-    assert np.array_equal(outs["graph"], outs["persistent"]), "persistent plan differs from fused"
+    assert np.array_equal(outs["graph"], outs["no_l2_ahead"]), "the L2 look-ahead changed results"
+    # the persistent plan shares the global-merge attention
+    assert np.array_equal(outs["global_merge"], outs["persistent"]), "persistent differs from fused"
     assert np.array_equal(outs["persistent"], outs["persistent_eager"])
+    for s in range(3):
+        for l in range(w.n_layers):
+            assert_close(outs["graph"][s, l], outs["global_merge"][s, l], f"cluster vs global {s},{l}")
     for s in range(3):
         for l in range(w.n_layers):
             assert_close(outs["graph"][s, l], outs["unfused"][s, l], f"fused vs unfused {s},{l}")

@@ -49,6 +49,7 @@ struct dec_handle {
   dec_model_desc d{};
   int n_sm = 0, G = 0;
   bool fused = true, graph = true, pdl = true, persistent = false, l2_ahead = true;
+  bool cluster_attn = true;
   std::vector<LayerDev> layers;
   std::vector<void*> allocs;
   // activations / workspace
@@ -64,6 +65,7 @@ struct dec_handle {
   float* apart = nullptr;  // attention partial records
   int* acount = nullptr;   // attention arrivals per split head
   int att_grid = 0;
+  int att_cluster = 0;  // fused plan: CTAs per KV head (cluster merge); 0 = global merge
   int* d_pos = nullptr;
   int* d_err = nullptr;
   float2* rope = nullptr;
@@ -236,6 +238,11 @@ AttnParams k2_params(const dec_handle* h, int l) {
   return p;
 }
 
+// The fused plan's attention grid: nkv clusters, or the global-merge grid.
+int fused_att_grid(const dec_handle* h) {
+  return h->att_cluster > 0 ? h->d.n_kv_heads * h->att_cluster : h->att_grid;
+}
+
 GemvParams k3_params(const dec_handle* h, int l) {
   GemvParams p = gemv_base(h, h->layers[l].o);
   p.x = h->o;
@@ -294,7 +301,8 @@ L2Ahead l2_ahead_of(const dec_handle* h, int kernel, int l) {
       a.hd = h->d.head_dim;
       a.max_ctx = h->d.max_ctx;
       a.pos = h->d_pos;
-      a.grid = h->att_grid;
+      a.grid = fused_att_grid(h);
+      a.cluster = h->att_cluster;
       a.cap = kL2AheadBytes;
       break;
     case 1: rows(L.o); break;
@@ -336,7 +344,8 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
       AttnParams p = k2_params(h, l);
       p.tl = tl;
       p.ahead = l2_ahead_of(h, 1, l);
-      e = launch_attn(h->d.head_dim, h->G, p, h->att_grid, h->attn_smem, s, h->pdl);
+      p.cluster = h->att_cluster;
+      e = launch_attn(h->d.head_dim, h->G, p, fused_att_grid(h), h->attn_smem, s, h->pdl);
       break;
     }
     case 2: {
@@ -605,7 +614,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   if (d.weight_fmt == DEC_W_Q4B32 &&
       (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64))
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
-  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD))
+  if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
+                  DEC_ATTN_GLOBAL_MERGE))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -616,6 +626,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->graph = !(d.flags & DEC_NO_GRAPH);
   h->pdl = !(d.flags & DEC_NO_PDL);
   h->l2_ahead = !(d.flags & DEC_NO_L2_AHEAD);
+  h->cluster_attn = !(d.flags & DEC_ATTN_GLOBAL_MERGE);
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -722,6 +733,31 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
     h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+  }
+  if (h->fused && !h->persistent && h->cluster_attn) {
+    // one cluster per KV head, as many CTAs per head as the SMs allow with every
+    // cluster resident at once (one wave)
+    int C = h->n_sm / nkv;
+    if (C > kMaxCluster) C = kMaxCluster;
+    if (C < 1) C = 1;
+    const void* fn = attn_kernel_ptr(hd, G, true);
+    for (; C > 1; --C) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(nkv * C);
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = h->attn_smem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int active = 0;
+      if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) == cudaSuccess && active >= nkv) break;
+      cudaGetLastError();  // a size the device refuses is not an error of the handle
+    }
+    h->att_cluster = C;
   }
   if (h->persistent) {
     // one ring for every phase: slots as large as the largest stage; the work

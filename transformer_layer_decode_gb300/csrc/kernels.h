@@ -46,6 +46,7 @@ constexpr int kTimelineSlots = 8;       // u64 per launch of the timeline probe
 // Most attention CTAs one KV head may be split over (bounds the merge).
 constexpr int kMaxSplits = 32;
 constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
+constexpr int kMaxCluster = 16;            // CTAs per KV head in the cluster attention
 constexpr int kStageTiles = 2 * kConsumerWarps;  // two tiles per consumer warp per stage
 constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
 constexpr int kTileBytes = kTileR * kTileK * 2;                          // 2 KB
@@ -117,6 +118,7 @@ struct L2Ahead {
   int n_units, grid, cap;  // unit count, the next kernel's grid, bytes per CTA at most
   int kv, nkv, hd, max_ctx;
   const int* pos;
+  int cluster;  // attention next: its cluster size (0: global-merge grid)
 };
 
 enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
@@ -167,6 +169,7 @@ struct AttnParams {
   float scale;
   uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
   L2Ahead ahead;
+  int cluster;   // > 0: grid = nkv clusters of this many CTAs, merged in shared memory
 };
 
 // ---- the persistent per-token kernel ---------------------------------------
@@ -219,10 +222,11 @@ size_t attn_smem_bytes(int hd, int G, int nstages);
 // the previous one on the stream finishes; it waits before reading its inputs).
 cudaError_t launch_gemv(int pro, int epi, bool q4, const GemvParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
+// p.cluster > 0: a cluster launch, grid = nkv * p.cluster.
 cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl);
+const void* attn_kernel_ptr(int hd, int G, bool cluster);
 const void* gemv_kernel_ptr(int pro, int epi, bool q4);
-const void* attn_kernel_ptr(int hd, int G);
 cudaError_t set_smem_limits();
 
 // Load-time repack of a row-major [rows][K] bf16 block into the tiled layout

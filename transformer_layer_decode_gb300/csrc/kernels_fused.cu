@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
   }
 }
 
-template <int HD, int G>
+template <int HD, int G, bool CL>
 __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * kAttnStageBytes),
@@ -100,7 +100,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
   // the previous step's final kernel, and this kernel can only launch after the
   // preceding kernel's CTAs have all passed their own wait, i.e. after that
   // final kernel completed.
-  const AttnSplit S = attn_split<HD>(*p.pos, p.nkv, b, nb);
+  const int pos = *p.pos;
+  const AttnSplit S = CL ? attn_split_cluster<HD>(pos, p.nkv, b, p.cluster)
+                         : attn_split<HD>(pos, p.nkv, b, nb);
   if (tid == 0) ring_init(R);
   __syncthreads();
 
@@ -109,6 +111,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
       RingPos P{0, 0, 0};
       attn_produce<HD>(p, p.kc, p.vc, R, P, S, policy_evict_first(), [] { pdl_wait(); });
       l2_ahead(p.ahead, b);
+    }
+    if (CL) {  // the producer warp takes part in the consumers' two cluster barriers
+      __syncwarp();
+      cluster_sync_all();
+      cluster_sync_all();
     }
     return;
   }
@@ -119,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
     tl_mark_max(p.tl, 3);
   }
   RingPos P{0, 0, 0};
-  const bool ok = attn_main<HD, G>(p, work, R, P, S, b, nb, tid);
+  const bool ok = attn_main<HD, G, CL>(p, work, R, P, S, b, nb, tid);
   if (p.tl) {
     named_barrier(1, kNC);
     if (tid == 0) {
@@ -141,9 +148,10 @@ const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
   return nullptr;
 }
 
-const void* attn_kernel_ptr(int hd, int G) {
-#define TLD_ATTN(H_, G_) \
-  if (hd == H_ && G == G_) return (const void*)attn_decode<H_, G_>;
+const void* attn_kernel_ptr(int hd, int G, bool cluster) {
+#define TLD_ATTN(H_, G_)                                                              \
+  if (hd == H_ && G == G_)                                                           \
+    return cluster ? (const void*)attn_decode<H_, G_, true> : (const void*)attn_decode<H_, G_, false>;
   TLD_ATTN(64, 1) TLD_ATTN(64, 2) TLD_ATTN(64, 4) TLD_ATTN(64, 8)
   TLD_ATTN(128, 1) TLD_ATTN(128, 2) TLD_ATTN(128, 4) TLD_ATTN(128, 8)
 #undef TLD_ATTN
@@ -163,26 +171,40 @@ cudaError_t set_smem_limits() {
     if (e != cudaSuccess) return e;
   }
   for (int hd : {64, 128})
-    for (int G : {1, 2, 4, 8}) {
-      cudaError_t e = cudaFuncSetAttribute(attn_kernel_ptr(hd, G),
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-      if (e != cudaSuccess) return e;
-    }
+    for (int G : {1, 2, 4, 8})
+      for (bool cl : {false, true}) {
+        const void* k = attn_kernel_ptr(hd, G, cl);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e == cudaSuccess && cl)
+          e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
 static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s,
-                              bool pdl) {
+                              bool pdl, int cluster = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 0) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = n;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -197,11 +219,13 @@ cudaError_t launch_gemv(int pro, int epi, bool q4, const GemvParams& p, int grid
 
 cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t smem,
                         cudaStream_t s, bool pdl) {
-  const void* fn = attn_kernel_ptr(hd, G);
+  const void* fn = attn_kernel_ptr(hd, G, p.cluster > 0);
   if (!fn) return cudaErrorInvalidValue;
+  if (p.cluster > 0 && (p.cluster > kMaxCluster || grid != p.nkv * p.cluster))
+    return cudaErrorInvalidValue;
   AttnParams copy = p;
   void* args[] = {&copy};
-  return launch_pdl(fn, args, grid, smem, s, pdl);
+  return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster);
 }
 
 // ---- load-time repack ------------------------------------------------------------

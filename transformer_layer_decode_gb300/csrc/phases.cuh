@@ -539,21 +539,28 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   return true;
 }
 
+constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
+
 // ---- attention ---------------------------------------------------------------
 // One unit = one chunk of CH cached positions of one KV head (its K rows, then
 // its V rows, 16 KB each).  The grid splits the units of all KV heads evenly;
 // every CTA serves all G query heads of the KV heads it touches, so each K/V
 // byte is read once.  Within a CTA the 8 consumer warps take interleaved
 // positions of each chunk and keep a running (max, sum, acc) per query head;
-// warps are merged at the end of each head segment, and a head cut between
-// CTAs is merged, after its loop, by the last of its CTAs to finish.
+// warps are merged at the end of each head segment.  A head cut between CTAs
+// is merged in one of two ways: (global) each CTA leaves a record in global
+// memory and the last of the head's CTAs to finish merges them; (cluster) the
+// grid is one thread-block cluster per KV head, its CTAs split that head's
+// chunks, leave their records in their own shared memory, and every CTA of
+// the cluster merges a slice of the head's outputs through distributed shared
+// memory.
 
-// Work area of an attention phase: per-warp states | merge scratch.
+// Work area of an attention phase: per-warp states | this CTA's record
+// (cluster merge) | merge scratch (global merge).
 struct AttnLayout {
   int hd, G;
-  __host__ __device__ size_t merge_off() const {
-    return 4 * (size_t)kConsumerWarps * G * (hd + 2);
-  }
+  __host__ __device__ size_t rec_off() const { return 4 * (size_t)kConsumerWarps * G * (hd + 2); }
+  __host__ __device__ size_t merge_off() const { return rec_off() + 4 * (size_t)G * (hd + 2); }
   // the record offsets of the splits of two heads, then the heads to merge
   __host__ __device__ size_t total() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
 };
@@ -576,10 +583,27 @@ __device__ __forceinline__ AttnSplit attn_split(int pos, int nkv, int b, int nb)
   return S;
 }
 
+// Cluster split: cluster g = b / C serves KV head g; its CTA of rank r takes a
+// contiguous share of that head's chunks.
+template <int HD>
+__device__ __forceinline__ AttnSplit attn_split_cluster(int pos, int nkv, int b, int C) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
+  AttnSplit S;
+  S.n = pos + 1;
+  S.cph = (S.n + CH - 1) / CH;
+  S.U = nkv * S.cph;
+  const int g = b / C, r = b - g * C;
+  S.u0 = g * S.cph + split_begin32(S.cph, C, r);
+  S.u1 = g * S.cph + split_begin32(S.cph, C, r + 1);
+  S.nu = S.u1 - S.u0;
+  return S;
+}
+
 template <int HD>
 __device__ void l2_ahead_kv(const L2Ahead& a, int b) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
-  const AttnSplit S = attn_split<HD>(*a.pos, a.nkv, b, a.grid);
+  const AttnSplit S = a.cluster ? attn_split_cluster<HD>(*a.pos, a.nkv, b, a.cluster)
+                                : attn_split<HD>(*a.pos, a.nkv, b, a.grid);
   int left = a.cap;
   int u = S.u0;
   while (u < S.u1 && left > 0) {
@@ -655,19 +679,32 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
 
 // Consumer part of an attention phase (q must be ready).  Returns false if a
 // wait ran out.
-template <int HD, int G>
+template <int HD, int G, bool CL = false>
 __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, const Ring& R, RingPos& P,
                           const AttnSplit& S, int b, int nb, int tid) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);  // positions per chunk (16 KB of K)
   constexpr int PW = CH / kConsumerWarps;              // positions per warp per chunk
   constexpr int SUB = 4;                               // positions per online-softmax update
   constexpr int DL = HD / 32;                          // dims per lane
+  // Fast form (PW * G <= 32 partial dots per lane): one reduce-scatter
+  // butterfly sums all of a chunk's dots, leaving lane l the total of dot
+  // number (l >> SH) & (V - 1), dot v = (head gg, position i) at v = gg*PW + i;
+  // each lane then runs the online softmax for its own (position, head), and
+  // the running max / sum of head gg live in the lanes of that head.
+  constexpr int V = PW * G;
+  constexpr bool FAST = V <= 32;
+  constexpr int LV = FAST ? ilog2(V) : 0, LPW = ilog2(PW), SH = 5 - LV;
   const int warp = tid >> 5, lane = tid & 31;
   float* ws = reinterpret_cast<float*>(work);  // [warp][G][HD+2]
+  float* crec = reinterpret_cast<float*>(work + AttnLayout{HD, G}.rec_off());  // [G][HD+2]
   const int n = S.n, cph = S.cph, U = S.U, u0 = S.u0, u1 = S.u1, nu = S.nu;
   float m[G], l[G], acc[G][DL];
+  float m_mine = -INFINITY, l_mine = 0.f;  // fast form: this lane's head
+  const int my_v = (lane >> SH) & (V - 1), my_i = my_v % PW;
   int cur_g = -1, seg_idx = 0;
   auto reset = [&]() {
+    m_mine = -INFINITY;
+    l_mine = 0.f;
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       m[gg] = -INFINITY;
@@ -682,6 +719,13 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   // (acc, m, l), merged after the loop by the last CTA of the head to finish.
   int split_heads[2] = {-1, -1};
   auto end_segment = [&](int g) {
+    if (FAST) {
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        m[gg] = __shfl_sync(0xffffffffu, m_mine, (gg * PW) << SH);
+        l[gg] = __shfl_sync(0xffffffffu, l_mine, (gg * PW) << SH);
+      }
+    }
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
       float* w = ws + ((size_t)warp * G + gg) * (HD + 2);
@@ -694,8 +738,8 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
     named_barrier(1, kNC);
     const int64_t h0 = (int64_t)g * cph, h1 = h0 + cph;
-    const bool whole = h0 >= u0 && h1 <= u1;
-    if (!whole) split_heads[seg_idx == 0 ? 0 : 1] = g;
+    const bool whole = !CL && h0 >= u0 && h1 <= u1;
+    if (!CL && !whole) split_heads[seg_idx == 0 ? 0 : 1] = g;
     float* rec = p.part + ((size_t)b * 2 + (seg_idx == 0 ? 0 : 1)) * G * (HD + 4);
     for (int i = tid; i < G * HD; i += kNC) {
       const int gg = i / HD, j = i % HD;
@@ -708,7 +752,14 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         A += wr[j] * e;
         Ls += wr[HD + 1] * e;
       }
-      if (whole) {
+      if (CL) {  // this CTA's record, in its own shared memory
+        float* cr = crec + gg * (HD + 2);
+        cr[j] = A;
+        if (j == 0) {
+          cr[HD] = M;
+          cr[HD + 1] = Ls;
+        }
+      } else if (whole) {
         p.o[(size_t)(g * G + gg) * HD + j] = A / Ls;
       } else {
         rec[gg * (HD + 4) + j] = A;
@@ -725,6 +776,9 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   };
 
   reset();
+  if (CL && nu == 0) {  // no chunk of the head: an empty record
+    for (int i = tid; i < G * (HD + 2); i += kNC) crec[i] = (i % (HD + 2) == HD) ? -INFINITY : 0.f;
+  }
   bool ok = true;
   int g = u0 / cph, c = u0 - g * cph;
   for (int s = 0; s < nu; ++s) {
@@ -759,8 +813,67 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&R.empty[P.slot]);
+    if (FAST) {
+      // partial dots of every (head, position) of this warp, then one butterfly
+      float x[FAST ? V : 1];
 #pragma unroll
-    for (int i0 = 0; i0 < PW; i0 += SUB) {
+      for (int i = 0; i < PW; ++i) {
+        float kv[DL];
+        kr[i].unpack(kv);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          float d = 0.f;
+#pragma unroll
+          for (int j = 0; j < DL; ++j) d = fmaf(qr[gg][j], kv[j], d);
+          x[(gg * PW + i) % (FAST ? V : 1)] = d;
+        }
+      }
+#pragma unroll
+      for (int st = 0; st < LV; ++st) {  // halve the values held, lane bit 4 - st
+        const int o = 16 >> st, half = V >> (st + 1);
+        const bool upper = lane & o;
+#pragma unroll
+        for (int k = 0; k < half; ++k) {
+          const float send = upper ? x[k] : x[k + half];
+          const float keep = upper ? x[k + half] : x[k];
+          x[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+#pragma unroll
+      for (int o = 16 >> LV; o > 0; o >>= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
+      const float sc = (warp + my_i * kConsumerWarps < rows) ? x[0] : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int bt = 0; bt < LPW; ++bt) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1 << (SH + bt)));
+      const float m_new = fmaxf(m_mine, mx);
+      const float pr = (sc == -INFINITY) ? 0.f : expf(sc - m_new);
+      const float alpha = (m_mine == -INFINITY) ? 0.f : expf(m_mine - m_new);
+      float ps = pr;
+#pragma unroll
+      for (int bt = 0; bt < LPW; ++bt) ps += __shfl_xor_sync(0xffffffffu, ps, 1 << (SH + bt));
+      l_mine = l_mine * alpha + ps;
+      m_mine = m_new;
+#pragma unroll
+      for (int gg = 0; gg < G; ++gg) {
+        const float a = __shfl_sync(0xffffffffu, alpha, (gg * PW) << SH);
+#pragma unroll
+        for (int j = 0; j < DL; ++j) acc[gg][j] *= a;
+      }
+#pragma unroll
+      for (int i = 0; i < PW; ++i) {
+        if (warp + i * kConsumerWarps >= rows) break;  // warp-uniform
+        float vv[DL];
+        vr[i].unpack(vv);
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+          const float pi = __shfl_sync(0xffffffffu, pr, (gg * PW + i) << SH);
+#pragma unroll
+          for (int j = 0; j < DL; ++j) acc[gg][j] = fmaf(pi, vv[j], acc[gg][j]);
+        }
+      }
+    }
+#pragma unroll
+    for (int i0 = 0; i0 < (FAST ? 0 : PW); i0 += SUB) {
       if (warp + i0 * kConsumerWarps >= rows) break;  // warp-uniform
       float sc[SUB][G];
 #pragma unroll
@@ -812,6 +925,42 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     tl_mark_max(p.tl, 6);
   }
   if (cur_g >= 0) end_segment(cur_g);
+
+  if (CL) {
+    // ---- the cluster merges its head: CTA r finishes a slice of the G x HD outputs
+    cluster_sync_all();  // every CTA's record is in its shared memory
+    const int C = p.cluster, r = (int)cluster_rank(), gh = b / C;
+    const int e0 = split_begin32(G * HD, C, r), e1 = split_begin32(G * HD, C, r + 1);
+    for (int e = e0 + tid; e < e1; e += kNC) {
+      const int gg = e / HD, j = e - gg * HD;
+      float mv[kMaxCluster], lv[kMaxCluster], av[kMaxCluster];
+#pragma unroll
+      for (int c2 = 0; c2 < kMaxCluster; ++c2) {
+        mv[c2] = -INFINITY;
+        lv[c2] = 0.f;
+        av[c2] = 0.f;
+        if (c2 < C) {
+          const uint32_t a = dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2);
+          mv[c2] = dsmem_ld(a + 4 * HD);
+          lv[c2] = dsmem_ld(a + 4 * (HD + 1));
+          av[c2] = dsmem_ld(a + 4 * j);
+        }
+      }
+      float M = -INFINITY;
+#pragma unroll
+      for (int c2 = 0; c2 < kMaxCluster; ++c2) M = fmaxf(M, mv[c2]);
+      float Lsum = 0.f, o = 0.f;
+#pragma unroll
+      for (int c2 = 0; c2 < kMaxCluster; ++c2) {
+        const float w = (mv[c2] == -INFINITY) ? 0.f : expf(mv[c2] - M);
+        Lsum = fmaf(lv[c2], w, Lsum);
+        o = fmaf(av[c2], w, o);
+      }
+      p.o[(size_t)(gh * G + gg) * HD + j] = o / Lsum;
+    }
+    cluster_sync_all();  // the records stay until every CTA of the cluster has read them
+    return ok;
+  }
 
   // ---- heads split over CTAs: the last CTA to finish merges them --------------
   // (tickets are taken after this CTA's whole loop, so merging never stalls it;

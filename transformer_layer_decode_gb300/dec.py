@@ -20,7 +20,7 @@ DEC_OK, DEC_ERR_ARG, DEC_ERR_SHAPE, DEC_ERR_STATE = 0, -1, -2, -3
 DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6, -7, -8
 DEC_W_BF16, DEC_W_Q4B32 = 0, 1
 DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL, DEC_PLAN_PERSISTENT = 0, 1, 2, 4, 8
-DEC_NO_L2_AHEAD = 16
+DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE = 16, 32
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
@@ -150,12 +150,14 @@ class Decoder:
     """One decode handle: weights, KV cache and the captured step graph."""
 
     def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True,
-                 pdl: bool = True, persistent: bool = False, l2_ahead: bool = True):
+                 pdl: bool = True, persistent: bool = False, l2_ahead: bool = True,
+                 cluster_attn: bool = True):
         self.lib = load_library()
         self.shape = shape
         flags = ((DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
                  | (0 if pdl else DEC_NO_PDL) | (DEC_PLAN_PERSISTENT if persistent else 0)
-                 | (0 if l2_ahead else DEC_NO_L2_AHEAD))
+                 | (0 if l2_ahead else DEC_NO_L2_AHEAD)
+                 | (0 if cluster_attn else DEC_ATTN_GLOBAL_MERGE))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
                               shape.max_ctx, shape.weight_fmt, flags)
