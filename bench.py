@@ -45,7 +45,31 @@ def parse():
                     help="fused five-kernel layer, the persistent per-token kernel, or the "
                          "one-kernel-per-op ablation")
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="fused plan: no programmatic dependent launch between kernels")
+    ap.add_argument("--no-l2-ahead", action="store_true",
+                    help="fused plan: no L2 prefetch of the next kernel's bytes")
+    ap.add_argument("--global-merge", action="store_true",
+                    help="fused plan: flat attention grid merged through global memory "
+                         "instead of one cluster per KV head")
     return ap.parse_args()
+
+
+def slowest_rank_ms(ms: float, world: int) -> float:
+    """The step time of the whole job: the maximum over ranks (every rank calls this)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_tok_s(world: int, steps: int, ms_max: float) -> float:
+    """Whole-job throughput of `world` independent replicas, each decoding `steps` tokens."""
+    return world * steps / (ms_max * 1e-3)
 
 
 def dist_env():
@@ -309,7 +333,9 @@ def run_ours(args, w, rank, world, local_rank):
     unfused = args.plan == "unfused"
     persistent = args.plan == "persistent"
     d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=want_cpu, unfused=unfused,
-                                    persistent=persistent, graph=not args.eager)
+                                    persistent=persistent, graph=not args.eager,
+                                    pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
+                                    cluster_attn=not args.global_merge)
     info = d.info()
     H = w.hidden
     xs = torch.from_numpy(workload.step_inputs(w, max(K, W))).to(dev)
@@ -348,11 +374,7 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     clocks.mark(tw0, tw1)
     d.sync_status()
-    ms = ev0.elapsed_time(ev1)
-    t_max = torch.tensor([ms], device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms = float(t_max.item())
+    ms = slowest_rank_ms(ev0.elapsed_time(ev1), world)
 
     # ---- end to end: host input -> device, step, device -> host each step ------
     d.truncate_kv(w.prefill)
@@ -372,11 +394,7 @@ def run_ours(args, w, rank, world, local_rank):
     tw1 = time.time()
     barrier()
     clocks.mark(tw0, tw1)
-    ms_e2e = ev0.elapsed_time(ev1)
-    t_e2e = torch.tensor([ms_e2e], device=dev)
-    if world > 1:
-        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-    ms_e2e = float(t_e2e.item())
+    ms_e2e = slowest_rank_ms(ev0.elapsed_time(ev1), world)
     assert np.all(np.isfinite(host_out.numpy())), "non-finite decode output"
 
     # ---- dominant kernel alone: back to back over all layers' weights ----------
@@ -408,8 +426,8 @@ def run_ours(args, w, rank, world, local_rank):
     clocks.stop()
     traffic = profiled_traffic(w.name) if args.plan == "fused" else None
 
-    tok_s = world * K / (ms * 1e-3)
-    tok_s_e2e = world * K / (ms_e2e * 1e-3)
+    tok_s = replica_tok_s(world, K, ms)
+    tok_s_e2e = replica_tok_s(world, K, ms_e2e)
     bpt = bytes_per_token(w, w.prefill + (K + 1) / 2.0)
 
     result = {
@@ -422,9 +440,13 @@ def run_ours(args, w, rank, world, local_rank):
                    "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
                    "ffn": w.ffn, "prefill": w.prefill, "batch": 1,
                    "parallelism": "replicas" if world > 1 else "single-gpu",
-                   "plan": f"{args.plan}, {'eager' if args.eager else 'CUDA graph'}",
+                   "plan": ", ".join([args.plan, "eager" if args.eager else "CUDA graph"]
+                                     + (["no PDL"] if args.no_pdl else [])
+                                     + (["no L2 look-ahead"] if args.no_l2_ahead else [])
+                                     + (["global-merge attention"] if args.global_merge else [])),
                    "kernels_per_layer": info.kernels_per_layer,
                    "kernels_per_token": info.kernels_per_token,
+                   "attn_ctas": info.attn_grid, "attn_cluster": info.attn_cluster,
                    "l2": "no flush: each step streams %.1f GB of weights + KV (> 129 MB L2)"
                          % (bpt["total"] / 1e9)},
         "hbm": {"bytes_per_token": bpt["total"], "achieved_gbs": bpt["total"] * tok_s / world / 1e9,

@@ -109,6 +109,9 @@ typedef struct dec_info {
   int64_t weight_bytes;       /* device bytes of all layers' weights as stored */
   int64_t kv_bytes;           /* device bytes of the KV cache (both K and V) */
   int64_t workspace_bytes;    /* device bytes of activations + split-K workspace */
+  int32_t attn_grid;          /* CTAs of the attention launch (fused plan) */
+  int32_t attn_cluster;       /* CTAs per KV head in one thread-block cluster, or 0 for
+                                 the flat grid merged through global memory */
 } dec_info;
 
 typedef struct dec_handle dec_handle; /* opaque */

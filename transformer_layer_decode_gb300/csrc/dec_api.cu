@@ -972,6 +972,8 @@ int dec_get_info(const dec_handle* h, dec_info* info) {
   info->weight_bytes = h->weight_bytes;
   info->kv_bytes = h->kv_bytes;
   info->workspace_bytes = h->ws_bytes;
+  info->attn_grid = h->fused && !h->persistent ? fused_att_grid(h) : h->att_grid;
+  info->attn_cluster = h->fused && !h->persistent ? h->att_cluster : 0;
   return DEC_OK;
 }
 

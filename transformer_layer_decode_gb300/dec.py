@@ -51,7 +51,8 @@ class Info(ctypes.Structure):
     _fields_ = [("kernels_per_layer", ctypes.c_int32), ("kernels_per_token", ctypes.c_int32),
                 ("n_sm", ctypes.c_int32), ("kv_len", ctypes.c_int32),
                 ("weight_bytes", ctypes.c_int64), ("kv_bytes", ctypes.c_int64),
-                ("workspace_bytes", ctypes.c_int64)]
+                ("workspace_bytes", ctypes.c_int64), ("attn_grid", ctypes.c_int32),
+                ("attn_cluster", ctypes.c_int32)]
 
 
 _lib = None
