@@ -128,7 +128,7 @@ def kernel_source_sha() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_layer_decode_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        if f.startswith("kernels_fused") or f in ("common.cuh", "kernels.h"):
+        if f.startswith("kernels_fused") or f in ("common.cuh", "kernels.h", "phases.cuh"):
             h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

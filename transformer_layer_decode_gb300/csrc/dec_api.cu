@@ -313,65 +313,64 @@ L2Ahead l2_ahead_of(const dec_handle* h, int kernel, int l) {
   return a;
 }
 
+// Parameters of fused GEMV kernel `kernel` (0: QKV, 2: o-proj, 3: gate/up,
+// 4: down) of layer l.  in_step: part of a dec_step (first / last layer I/O,
+// taps, timeline); otherwise a standalone launch on the workspaces.  The graph
+// capture and the later pointer patching both build their nodes from here.
+GemvParams fused_gemv_params(const dec_handle* h, int kernel, int l, const float* emb, float* out,
+                             bool in_step) {
+  const bool first = in_step && l == 0;
+  const bool last = l == h->d.n_layers - 1;
+  GemvParams p{};
+  int slot = 0;
+  switch (kernel) {
+    case 0: p = k1_params(h, l, first ? emb : h->X, first); slot = 0; break;
+    case 2: p = k3_params(h, l); slot = 1; break;
+    case 3: p = k4_params(h, l); slot = 2; break;
+    default: p = k5_params(h, l, (in_step && last) ? out : h->X, in_step && last); slot = 3; break;
+  }
+  p.tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + kernel) : nullptr;
+  p.ahead = l2_ahead_of(h, kernel, l);
+  if (in_step && h->qtap) {  // int8 input taps: q, o, gate and down projections of layer l
+    const int km = max_k(h->d);
+    p.qtap = h->qtap + ((size_t)l * 4 + slot) * km;
+    p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
+  }
+  if (in_step && h->dot_tap && h->dot_layer == l && h->dot_kernel == kernel) p.dots = h->dot_tap;
+  return p;
+}
+
 int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, float* out,
                          bool in_step, cudaStream_t s) {
   const int nb = h->n_sm;
   const LayerDev& L = h->layers[l];
-  const bool first = in_step && l == 0;
-  const bool last = l == h->d.n_layers - 1;
-  uint64_t* tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + kernel) : nullptr;
   const bool q4 = h->d.weight_fmt == DEC_W_Q4B32;
-  // int8 input taps: q, o, gate and down projections of layer l
-  const int km = max_k(h->d);
-  auto qtaps = [&](GemvParams& p, int slot) {
-    if (in_step && h->qtap) {
-      p.qtap = h->qtap + ((size_t)l * 4 + slot) * km;
-      p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
-    }
-    if (in_step && h->dot_tap && h->dot_layer == l && h->dot_kernel == kernel) p.dots = h->dot_tap;
-  };
   cudaError_t e = cudaSuccess;
   switch (kernel) {
-    case 0: {
-      GemvParams p = k1_params(h, l, first ? emb : h->X, first);
-      p.tl = tl;
-      p.ahead = l2_ahead_of(h, 0, l);
-      qtaps(p, 0);
-      e = launch_gemv(PRO_NORM, EPI_QKV, q4, p, nb, L.qkv.smem, s, h->pdl);
+    case 0:
+      e = launch_gemv(PRO_NORM, EPI_QKV, q4, fused_gemv_params(h, 0, l, emb, out, in_step), nb,
+                      L.qkv.smem, s, h->pdl);
       break;
-    }
     case 1: {
       AttnParams p = k2_params(h, l);
-      p.tl = tl;
+      p.tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 1) : nullptr;
       p.ahead = l2_ahead_of(h, 1, l);
       p.cluster = h->att_cluster;
       e = launch_attn(h->d.head_dim, h->G, p, fused_att_grid(h), h->attn_smem, s, h->pdl);
       break;
     }
-    case 2: {
-      GemvParams p = k3_params(h, l);
-      p.tl = tl;
-      p.ahead = l2_ahead_of(h, 2, l);
-      qtaps(p, 1);
-      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.o.smem, s, h->pdl);
+    case 2:
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, fused_gemv_params(h, 2, l, emb, out, in_step), nb,
+                      L.o.smem, s, h->pdl);
       break;
-    }
-    case 3: {
-      GemvParams p = k4_params(h, l);
-      p.tl = tl;
-      p.ahead = l2_ahead_of(h, 3, l);
-      qtaps(p, 2);
-      e = launch_gemv(PRO_NORM, EPI_SWIGLU, q4, p, nb, L.gu.smem, s, h->pdl);
+    case 3:
+      e = launch_gemv(PRO_NORM, EPI_SWIGLU, q4, fused_gemv_params(h, 3, l, emb, out, in_step), nb,
+                      L.gu.smem, s, h->pdl);
       break;
-    }
-    case 4: {
-      GemvParams p = k5_params(h, l, (in_step && last) ? out : h->X, in_step && last);
-      p.tl = tl;
-      p.ahead = l2_ahead_of(h, 4, l);
-      qtaps(p, 3);
-      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, p, nb, L.down.smem, s, h->pdl);
+    case 4:
+      e = launch_gemv(PRO_PLAIN, EPI_RESID, q4, fused_gemv_params(h, 4, l, emb, out, in_step), nb,
+                      L.down.smem, s, h->pdl);
       break;
-    }
     default:
       return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
   }
@@ -517,15 +516,6 @@ int capture(dec_handle* h, const float* emb, float* out) {
 }
 
 // The taps a captured launch of kernel k (0 QKV, 4 down) of layer l carries.
-void set_captured_taps(const dec_handle* h, GemvParams& p, int l, int k) {
-  const int km = max_k(h->d), slot = k == 0 ? 0 : 3;
-  if (h->qtap) {
-    p.qtap = h->qtap + ((size_t)l * 4 + slot) * km;
-    p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
-  }
-  if (h->dot_tap && h->dot_layer == l && h->dot_kernel == k) p.dots = h->dot_tap;
-}
-
 // Points the captured graph at new input / output buffers.
 int patch_io(dec_handle* h, const float* emb, float* out) {
   if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
@@ -546,9 +536,7 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
     return DEC_OK;
   }
   if (emb != h->cap_emb) {
-    GemvParams p = k1_params(h, 0, emb, true);
-    p.tl = h->timeline;
-    set_captured_taps(h, p, 0, 0);
+    GemvParams p = fused_gemv_params(h, 0, 0, emb, out, true);
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
     kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_NORM, EPI_QKV, h->d.weight_fmt == DEC_W_Q4B32));
@@ -561,9 +549,7 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
   }
   if (out != h->cap_out) {
     const int l = h->d.n_layers - 1;
-    GemvParams p = k5_params(h, l, out, true);
-    p.tl = h->timeline ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 4) : nullptr;
-    set_captured_taps(h, p, l, 4);
+    GemvParams p = fused_gemv_params(h, 4, l, emb, out, true);
     void* args[] = {&p};
     cudaKernelNodeParams kp{};
     kp.func = const_cast<void*>(gemv_kernel_ptr(PRO_PLAIN, EPI_RESID, h->d.weight_fmt == DEC_W_Q4B32));
