@@ -259,26 +259,40 @@ typedef struct orc_layer {
 
 enum { W_Q = 0, W_K, W_V, W_O, W_GATE, W_UP, W_DOWN };
 
-/* Optional per-layer capture of the int8 GEMV inputs: n1, o, n2, a. */
+/* The int8 codes of the four GEMV inputs of a layer (n1, o, n2, a).  given = 0:
+ * the layer's own codes are copied out.  given != 0: the layer uses these codes
+ * instead of quantizing; the configs' integer dots are defined on whatever codes
+ * the quantizer decided, and a decision made on fp32 values elsewhere may differ
+ * by one from this fp64 chain's where a value sits on a rounding boundary. */
 typedef struct orc_qtap {
   int8_t* q[4];
   float* d[4];
+  int32_t given;
 } orc_qtap;
 
-static void project(const orc_dims* D, const orc_layer* L, int which, int N, int K,
-                    const double* x, double* y, int8_t* qbuf, float* dbuf) {
-  if (!D->q4) {
-    orc_gemv_bf16(L->w[which], N, K, x, y);
-  } else {
-    orc_quantize_act(x, K, qbuf, dbuf);
-    orc_gemv_q4(L->q[which], L->s[which], N, K, qbuf, dbuf, y);
+/* The quantized form of GEMV input `slot` (bf16 weights: nothing to do). */
+static void quantize_input(const orc_dims* D, orc_qtap* tap, int slot, const double* z, int K,
+                           int8_t* qbuf, float* dbuf) {
+  if (!D->q4) return;
+  if (tap && tap->given && tap->q[slot]) {
+    memcpy(qbuf, tap->q[slot], (size_t)K);
+    memcpy(dbuf, tap->d[slot], sizeof(float) * (size_t)(K / 32));
+    return;
+  }
+  orc_quantize_act(z, K, qbuf, dbuf);
+  if (tap && tap->q[slot]) {
+    memcpy(tap->q[slot], qbuf, (size_t)K);
+    memcpy(tap->d[slot], dbuf, sizeof(float) * (size_t)(K / 32));
   }
 }
 
-static void keep_q(orc_qtap* tap, int slot, const int8_t* q, const float* d, int K) {
-  if (!tap || !tap->q[slot]) return;
-  memcpy(tap->q[slot], q, (size_t)K);
-  memcpy(tap->d[slot], d, sizeof(float) * (size_t)(K / 32));
+/* y = W x: bf16 weights on x itself, q4 weights on x's quantized form. */
+static void project(const orc_dims* D, const orc_layer* L, int which, int N, int K,
+                    const double* x, double* y, const int8_t* qbuf, const float* dbuf) {
+  if (!D->q4)
+    orc_gemv_bf16(L->w[which], N, K, x, y);
+  else
+    orc_gemv_q4(L->q[which], L->s[which], N, K, qbuf, dbuf, y);
 }
 
 /* x[H] -> out[H] at position pos; appends this token's k, v to row pos. */
@@ -305,8 +319,8 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   /* input RMSNorm + weight multiply */
   orc_rmsnorm(x, L->attn_norm, H, D->rms_eps, n1);
   /* q, k, v projections */
+  quantize_input(D, tap, 0, n1, H, qb, db);
   project(D, L, W_Q, nq * d, H, n1, q, qb, db);
-  keep_q(tap, 0, qb, db, H);
   project(D, L, W_K, nkv * d, H, n1, k, qb, db);
   project(D, L, W_V, nkv * d, H, n1, v, qb, db);
   /* RoPE on q and k */
@@ -328,19 +342,19 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
     orc_attention_head(q + (size_t)hq * d, Kh, Vh, pos + 1, d, o + (size_t)hq * d);
   }
   /* output projection + residual */
+  quantize_input(D, tap, 1, o, nq * d, qb, db);
   project(D, L, W_O, H, nq * d, o, y, qb, db);
-  keep_q(tap, 1, qb, db, nq * d);
   for (int i = 0; i < H; ++i) h1[i] = x[i] + y[i];
   /* post-attention RMSNorm + multiply */
   orc_rmsnorm(h1, L->ffn_norm, H, D->rms_eps, n2);
   /* gate, up, SwiGLU */
+  quantize_input(D, tap, 2, n2, H, qb, db);
   project(D, L, W_GATE, F, H, n2, g, qb, db);
-  keep_q(tap, 2, qb, db, H);
   project(D, L, W_UP, F, H, n2, u, qb, db);
   orc_swiglu(g, u, F, a);
   /* down projection + residual */
+  quantize_input(D, tap, 3, a, F, qb, db);
   project(D, L, W_DOWN, H, F, a, y, qb, db);
-  keep_q(tap, 3, qb, db, F);
   for (int i = 0; i < H; ++i) out[i] = (g_mutation == MUT_NO_RESIDUAL2) ? y[i] : h1[i] + y[i];
 
   free(n1); free(q); free(k); free(v); free(o); free(h1); free(y); free(n2);

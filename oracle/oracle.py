@@ -49,7 +49,7 @@ class Layer(ctypes.Structure):
 
 
 class QTap(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p * 4), ("d", ctypes.c_void_p * 4)]
+    _fields_ = [("q", ctypes.c_void_p * 4), ("d", ctypes.c_void_p * 4), ("given", ctypes.c_int32)]
 
 
 _lib = None
@@ -280,13 +280,22 @@ class OracleStack:
         self.kv_len = pos + 1
         return (out, taps) if per_layer else out
 
-    def layer_step(self, layer: int, x, pos: int, qtap: bool = False):
-        """One layer alone (does not advance kv_len); optional int8 input capture."""
+    def layer_step(self, layer: int, x, pos: int, qtap: bool = False, qgiven=None):
+        """One layer alone (does not advance kv_len).  qtap: also return the int8
+        codes and scales of the four GEMV inputs.  qgiven: four (codes, scales)
+        pairs the q4 layer uses instead of quantizing its own GEMV inputs."""
         x = _f64(x)
         out = np.empty(self.hidden, dtype=np.float64)
         tap = None
         tap_arrays = None
-        if qtap:
+        if qgiven is not None:
+            tap_arrays = [(np.ascontiguousarray(qq, np.int8), np.ascontiguousarray(dd, np.float32))
+                          for qq, dd in qgiven]
+            tap = QTap()
+            tap.given = 1
+            for i, (qq, dd) in enumerate(tap_arrays):
+                tap.q[i], tap.d[i] = _p(qq), _p(dd)
+        elif qtap:
             H, F = self.hidden, self.dims.ffn
             qd = self.dims.n_q_heads * self.dims.head_dim
             tap_arrays = [(np.empty(K, np.int8), np.empty(K // 32, np.float32))

@@ -73,3 +73,23 @@ def run_oracle(st: orc.OracleStack, w: synth.Workload, inputs: np.ndarray):
         _, per_layer = st.step(x, w.prefill + s, per_layer=True)
         res.append(per_layer)
     return np.stack(res)
+
+
+def tiled_rows_to_abi(w: synth.Workload, kernel: int):
+    """(tensor id, ABI row) of every tiled row of a fused GEMV, in tiled order:
+    QKV rows pair-interleaved per q / k head then v; gate / up rows alternating."""
+    hd, nq, nkv = w.head_dim, w.n_q_heads, w.n_kv_heads
+    out = []
+    if kernel == 0:
+        for t, heads in ((synth.T_WQ, nq), (synth.T_WK, nkv)):
+            for R in range(heads * hd):
+                head, j = divmod(R, hd)
+                out.append((t, head * hd + (j // 2 if j % 2 == 0 else j // 2 + hd // 2)))
+        out += [(synth.T_WV, r) for r in range(nkv * hd)]
+    elif kernel == 3:
+        for R in range(2 * w.ffn):
+            out.append((synth.T_WGATE if R % 2 == 0 else synth.T_WUP, R // 2))
+    else:
+        t = synth.T_WO if kernel == 2 else synth.T_WDOWN
+        out += [(t, r) for r in range(w.shape(t)[0])]
+    return out

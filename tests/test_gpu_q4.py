@@ -10,7 +10,7 @@
 import numpy as np
 import pytest
 
-from harness import assert_close, oracle_stack, run_gpu, run_oracle
+from harness import assert_close, oracle_stack, run_gpu, run_oracle, tiled_rows_to_abi
 from oracle import oracle as orc
 from transformer_layer_decode_gb300 import dec, synth, workload
 
@@ -47,25 +47,6 @@ def test_q4_layers_match_oracle(name, mode):
             assert_close(got[s, l], ref[s, l], f"{name} {mode} step {s} layer {l}")
 
 
-def _tiled_to_abi(w, kernel):
-    """(tensor id, ABI row) of every tiled row of a fused GEMV."""
-    hd, nq, nkv = w.head_dim, w.n_q_heads, w.n_kv_heads
-    out = []
-    if kernel == 0:
-        for sec, t, heads in ((0, synth.T_WQ, nq), (1, synth.T_WK, nkv)):
-            for R in range(heads * hd):
-                head, j = divmod(R, hd)
-                out.append((t, head * hd + (j // 2 if j % 2 == 0 else j // 2 + hd // 2)))
-        out += [(synth.T_WV, r) for r in range(nkv * hd)]
-    elif kernel == 3:
-        for R in range(2 * w.ffn):
-            out.append((synth.T_WGATE if R % 2 == 0 else synth.T_WUP, R // 2))
-    else:
-        t = synth.T_WO if kernel == 2 else synth.T_WDOWN
-        out += [(t, r) for r in range(w.shape(t)[0])]
-    return out
-
-
 @pytest.mark.parametrize("persistent", [False, True])
 @pytest.mark.parametrize("kernel", [0, 2, 3, 4])
 def test_q4_integer_block_dots_bit_exact(kernel, persistent):
@@ -77,7 +58,7 @@ def test_q4_integer_block_dots_bit_exact(kernel, persistent):
     qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
     qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")
     K = {0: w.hidden, 2: w.n_q_heads * w.head_dim, 3: w.hidden, 4: w.ffn}[kernel]
-    rows = _tiled_to_abi(w, kernel)
+    rows = tiled_rows_to_abi(w, kernel)
     dots = torch.full((len(rows), K // 32), -2**31, dtype=torch.int32, device="cuda")
     d.set_tap(None, qact, qsc)
     d.set_dot_tap(layer, kernel, dots)

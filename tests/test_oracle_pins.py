@@ -352,6 +352,18 @@ def pin_q4_layer():
     q_proj = orc.gemv_q4(q4[0][0], q4[0][1], taps[0][0], taps[0][1])
     _close(q_proj, deq[0] @ xq, 1e-13, "q4 projection")
     assert np.all(np.isfinite(out))
+    # given codes: its own codes reproduce the layer exactly; one code of the
+    # down projection's input raised by one moves output j by exactly
+    # scale * dx_b * w[j][k] (the residual and everything before stay put)
+    again = st.layer_step(0, x, 0, qgiven=taps)
+    assert np.array_equal(again, out)
+    k = 37
+    qa = taps[3][0].copy()
+    assert abs(int(qa[k])) < 127
+    qa[k] += 1
+    moved = st.layer_step(0, x, 0, qgiven=[taps[0], taps[1], taps[2], (qa, taps[3][1])])
+    step = 0.0625 * float(taps[3][1][k // 32]) * deq[6][:, k] / 0.0625
+    _close(moved - out, step, 1e-9, "one int8 code of the down input")
 
 
 PINS = [pin_storage_formats, pin_rmsnorm, pin_gemv, pin_rope, pin_attention, pin_swiglu,

@@ -136,7 +136,7 @@ __device__ __forceinline__ GemvIO gemv_io(const TokenParams& P, int l, int slot,
 // thread, where each standalone fused kernel spills nothing.  That is why this
 // plan's phases run slower than the five-kernel plan's kernels.
 template <int HD, int G, bool Q4>
-__device__ __noinline__ bool layer_phases(const TokenParams* Pp, int l, int pos, PhaseCtx* cxp) {
+__device__ __forceinline__ bool layer_phases(const TokenParams* Pp, int l, int pos, PhaseCtx* cxp) {
   const TokenParams& Q = *Pp;
   PhaseCtx cx = *cxp;
   const int nb = cx.nb, k0 = 5 * l, L = Q.n_layers;
