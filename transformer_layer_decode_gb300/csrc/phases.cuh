@@ -203,49 +203,70 @@ __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
 // q = 0 when dx == 0.  Eight lanes serve a block, four elements each.  The int8
 // values are stored for dp4a against packed nibbles: in each group of eight,
 // the even elements first, then the odd ones.  sx holds each block's sum of q.
+// The int8 code of z at block scale d (rd = 1/d): round-half-even of the IEEE
+// fp32 quotient z / d, clamped to +-127.  The quotient is formed first with the
+// reciprocal (relative error a few 2^-24, so at most ~2e-5 off for |z/d| <= 127);
+// only where that lands within 1e-3 of a rounding boundary (k + 1/2) does the
+// IEEE division decide, so the codes are exactly those of the division.
+__device__ __forceinline__ int quant_code(float z, float d, float rd) {
+  const float qa = z * rd;
+  const float f = qa - floorf(qa);
+  const float q = fabsf(f - 0.5f) < 1e-3f ? __fdiv_rn(z, d) : qa;
+  const int v = __float2int_rn(q);
+  return v > 127 ? 127 : (v < -127 ? -127 : v);
+}
+
+// Per-32-block absmax quantization of xs[0..K) * scale into the dp4a layout of
+// qx (per 8 elements: the four even ones, then the four odd ones), the block
+// scales dx (fp32, amax / 127) and the code sums sx; optionally also the codes in
+// natural order (qtap) and the scales (qstap).
 __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, float* dx, int* sx,
-                                int8_t* qtap, float* qstap, int tid, int NC) {
-  const int lane = tid & 31, sub = lane & 7, warp = tid >> 5;
+                                       int8_t* qtap, float* qstap, int tid, int NC, float scale) {
+  const int lane = tid & 31, sub = lane & 3, warp = tid >> 5;
   const int nblk = K / 32;
-  // Four blocks per warp per round; the round count is the same for all lanes
-  // of a warp (the shuffles below name the whole warp).
-  for (int base = warp * 4; base < nblk; base += (NC >> 5) * 4) {
-    const int blk = base + (lane >> 3);
+  // Eight blocks per warp per round, four lanes per block, eight elements per
+  // lane; the round count is the same for all lanes of a warp (the shuffles
+  // below name the whole warp).
+  for (int base = warp * 8; base < nblk; base += (NC >> 5) * 8) {
+    const int blk = base + (lane >> 2);
     const bool live = blk < nblk;
-    const int e = blk * 32 + sub * 4;
-    const float4 z = live ? *reinterpret_cast<const float4*>(xs + e) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float amax = fmaxf(fmaxf(fabsf(z.x), fabsf(z.y)), fmaxf(fabsf(z.z), fabsf(z.w)));
+    const int e = blk * 32 + sub * 8;
+    float z[8];
+    if (live) {
+      const float4 a = *reinterpret_cast<const float4*>(xs + e);
+      const float4 b = *reinterpret_cast<const float4*>(xs + e + 4);
+      z[0] = a.x * scale; z[1] = a.y * scale; z[2] = a.z * scale; z[3] = a.w * scale;
+      z[4] = b.x * scale; z[5] = b.y * scale; z[6] = b.z * scale; z[7] = b.w * scale;
+    } else {
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float d = __fdiv_rn(amax, 127.0f);
-    int q[4];
-    const float zz[4] = {z.x, z.y, z.z, z.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      int v = 0;
-      if (d != 0.0f) {
-        v = __float2int_rn(__fdiv_rn(zz[i], d));
-        v = v > 127 ? 127 : (v < -127 ? -127 : v);
-      }
-      q[i] = v;
+      for (int i = 0; i < 8; ++i) z[i] = 0.f;
     }
-    int sum = q[0] + q[1] + q[2] + q[3];
+    float amax = 0.f;
 #pragma unroll
-    for (int o = 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(z[i]));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float rd = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.f;
+    int q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = d != 0.0f ? quant_code(z[i], d, rd) : 0;
+    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
+    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     if (!live) continue;
-    // elements e..e+3 = 8g + 4h + {0,1,2,3}: evens go to bytes 8g+2h, 8g+2h+1,
-    // odds to bytes 8g+4+2h, 8g+4+2h+1
-    const int g8 = e & ~7, h = (e >> 2) & 1;
-    *reinterpret_cast<uint16_t*>(qx + g8 + 2 * h) = (uint16_t)((q[0] & 0xff) | ((q[2] & 0xff) << 8));
-    *reinterpret_cast<uint16_t*>(qx + g8 + 4 + 2 * h) =
-        (uint16_t)((q[1] & 0xff) | ((q[3] & 0xff) << 8));
+    const uint32_t ev = (uint32_t)(q[0] & 0xff) | (uint32_t)(q[2] & 0xff) << 8 |
+                        (uint32_t)(q[4] & 0xff) << 16 | (uint32_t)(q[6] & 0xff) << 24;
+    const uint32_t od = (uint32_t)(q[1] & 0xff) | (uint32_t)(q[3] & 0xff) << 8 |
+                        (uint32_t)(q[5] & 0xff) << 16 | (uint32_t)(q[7] & 0xff) << 24;
+    *reinterpret_cast<uint2*>(qx + e) = make_uint2(ev, od);
     if (sub == 0) {
       dx[blk] = d;
       sx[blk] = sum;
     }
     if (qtap) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) qtap[e + i] = (int8_t)q[i];
+      for (int i = 0; i < 8; ++i) qtap[e + i] = (int8_t)q[i];
       if (sub == 0) qstap[blk] = d;
     }
   }
@@ -347,7 +368,7 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     // the input vector was written by another phase: read it from L2
     const float4* x4 = reinterpret_cast<const float4*>(io.x);
     float ss = 0.f;
-    constexpr int PB = 4;  // loads in flight per thread
+    constexpr int PB = 12;  // loads in flight per thread: K up to 12288 in one round trip
     for (int base = tid; base < K4; base += kNC * PB) {
       float4 v[PB];
 #pragma unroll
@@ -392,19 +413,10 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     rnorm = 1.0f / sqrtf(tot / (float)K + p.eps);
   }
   if (Q4) {
-    if (PRO == PRO_NORM) {
-      for (int k4 = tid; k4 < K4; k4 += kNC) {
-        float4 v = reinterpret_cast<float4*>(xs)[k4];
-        v.x *= rnorm;
-        v.y *= rnorm;
-        v.z *= rnorm;
-        v.w *= rnorm;
-        reinterpret_cast<float4*>(xs)[k4] = v;
-      }
-      named_barrier(1, kNC);
-      rnorm = 1.f;
-    }
-    quantize_blocks(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid, kNC);
+    // the normalised vector itself is quantised: the codes carry the RMS scale
+    quantize_blocks(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid, kNC,
+                    rnorm);
+    rnorm = 1.f;
     named_barrier(1, kNC);
   }
 
