@@ -211,7 +211,8 @@ __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
 __device__ __forceinline__ int quant_code(float z, float d, float rd) {
   const float qa = z * rd;
   const float f = qa - floorf(qa);
-  const float q = fabsf(f - 0.5f) < 1e-3f ? __fdiv_rn(z, d) : qa;
+  // (not >=): a block so small that 1/d overflows gives NaN here and divides too
+  const float q = !(fabsf(f - 0.5f) >= 1e-3f) ? __fdiv_rn(z, d) : qa;
   const int v = __float2int_rn(q);
   return v > 127 ? 127 : (v < -127 ? -127 : v);
 }
