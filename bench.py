@@ -289,12 +289,12 @@ def run_reference(args, w, rank, world):
     st = oracle_for(w, host, w.prefill + 2)
     import ctypes
     cur = np.ascontiguousarray(x0, dtype=np.float64)
-    out = np.empty(w.hidden, dtype=np.float64)
     times = []
     for s in range(args.warmup + args.steps):
         t0 = time.perf_counter()
+        x = cur
         for l in range(n_layers):
-            out = st.layer_step(l, cur, w.prefill)
+            x = st.layer_step(l, x, w.prefill)  # each layer feeds the next, as in a token
         dt = time.perf_counter() - t0
         if s >= args.warmup:
             times.append(dt)
@@ -311,7 +311,8 @@ def run_reference(args, w, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "layers": w.n_layers, "hidden": w.hidden,
                    "heads": f"{w.n_q_heads}/{w.n_kv_heads}", "head_dim": w.head_dim,
-                   "ffn": w.ffn, "prefill": w.prefill, "batch": 1},
+                   "ffn": w.ffn, "prefill": w.prefill, "batch": 1,
+                   "parallelism": "single-gpu", "plan": "fp64 CPU oracle (unfused chain)"},
         "cpu_baseline": {"value": value, "unit": "tok/s", "cores": oracle_cores(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0,
