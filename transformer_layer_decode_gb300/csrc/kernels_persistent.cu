@@ -130,11 +130,12 @@ __device__ __forceinline__ GemvIO gemv_io(const TokenParams& P, int l, int slot,
   return io;
 }
 
-// The five phases of one layer, a separate function called once per layer.
-// Five phases in one body (inlined in the layer loop or not) make the compiler
-// keep values of several phases live at once: it spills about a kilobyte per
-// thread, where each standalone fused kernel spills nothing.  That is why this
-// plan's phases run slower than the five-kernel plan's kernels.
+// The five phases of one layer, inlined into the layer loop.  With five phases
+// in one loop body the compiler keeps values of several phases live at once and
+// spills about a kilobyte per thread (a non-inlined layer or phase function
+// spills as much and runs slower still), where each standalone fused kernel
+// spills nothing.  That is why this plan's phases run slower than the
+// five-kernel plan's kernels.
 template <int HD, int G, bool Q4>
 __device__ __forceinline__ bool layer_phases(const TokenParams* Pp, int l, int pos, PhaseCtx* cxp) {
   const TokenParams& Q = *Pp;
