@@ -715,10 +715,11 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return DEC_ERR_CUDA;
   }
   {
-    const size_t fixed = attn_smem_bytes(hd, G, 0);
+    const bool cl = h->fused && !h->persistent && h->cluster_attn;
+    const size_t fixed = attn_smem_bytes(hd, G, 0, cl);
     int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
     h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
-    h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages);
+    h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages, cl);
   }
   if (h->fused && !h->persistent && h->cluster_attn) {
     // one cluster per KV head, as many CTAs per head as the SMs allow with every
@@ -730,7 +731,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     for (; C > 1; --C) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(nkv * C);
-      cfg.blockDim = dim3(kThreads);
+      cfg.blockDim = dim3((attn_consumer_warps(G, true) + 1) * 32);
       cfg.dynamicSmemBytes = h->attn_smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -32,8 +32,13 @@ size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
          GemvLayout{K, max_rb_local, q4}.total();
 }
 
-size_t attn_smem_bytes(int hd, int G, int nstages) {
-  return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages + AttnLayout{hd, G}.total();
+// Consumer warps of the attention kernel: 16 for the cluster kernels of GQA
+// groups up to 2 (their registers allow 17 warps a CTA), else 8.
+int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 2 ? 16 : kConsumerWarps; }
+
+size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster) {
+  return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages +
+         AttnLayout{hd, G, attn_consumer_warps(G, cluster)}.total();
 }
 
 template <int PRO, int EPI, bool Q4>
@@ -86,8 +91,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_fused(const GemvParams p) {
   }
 }
 
-template <int HD, int G, bool CL>
-__global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
+template <int HD, int G, bool CL, int NW>
+__global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * kAttnStageBytes),
                reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * kAttnStageBytes) + p.nstages,
@@ -103,10 +108,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
   const int pos = *p.pos;
   const AttnSplit S = CL ? attn_split_cluster<HD>(pos, p.nkv, b, p.cluster)
                          : attn_split<HD>(pos, p.nkv, b, nb);
-  if (tid == 0) ring_init(R);
+  if (tid == 0) ring_init(R, NW);
   __syncthreads();
 
-  if (warp == kConsumerWarps) {
+  if (warp == NW) {
     if (lane == 0) {
       RingPos P{0, 0, 0};
       attn_produce<HD>(p, p.kc, p.vc, R, P, S, policy_evict_first(), [] { pdl_wait(); });
@@ -126,9 +131,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_decode(const AttnParams p) {
     tl_mark_max(p.tl, 3);
   }
   RingPos P{0, 0, 0};
-  const bool ok = attn_main<HD, G, CL>(p, work, R, P, S, b, nb, tid);
+  const bool ok = attn_main<HD, G, CL, NW>(p, work, R, P, S, b, nb, tid);
   if (p.tl) {
-    named_barrier(1, kNC);
+    named_barrier(1, NW * 32);
     if (tid == 0) {
       tl_mark_max(p.tl, 1);
       tl_mark_min(p.tl, 7);
@@ -149,9 +154,10 @@ const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
 }
 
 const void* attn_kernel_ptr(int hd, int G, bool cluster) {
-#define TLD_ATTN(H_, G_)                                                              \
-  if (hd == H_ && G == G_)                                                           \
-    return cluster ? (const void*)attn_decode<H_, G_, true> : (const void*)attn_decode<H_, G_, false>;
+#define TLD_ATTN(H_, G_)                                                                       \
+  if (hd == H_ && G == G_)                                                                    \
+    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 2 ? 16 : kConsumerWarps)>  \
+                   : (const void*)attn_decode<H_, G_, false, kConsumerWarps>;
   TLD_ATTN(64, 1) TLD_ATTN(64, 2) TLD_ATTN(64, 4) TLD_ATTN(64, 8)
   TLD_ATTN(128, 1) TLD_ATTN(128, 2) TLD_ATTN(128, 4) TLD_ATTN(128, 8)
 #undef TLD_ATTN
@@ -183,10 +189,10 @@ cudaError_t set_smem_limits() {
 }
 
 static cudaError_t launch_pdl(const void* fn, void** args, int grid, size_t smem, cudaStream_t s,
-                              bool pdl, int cluster = 0) {
+                              bool pdl, int cluster = 0, int threads = kThreads) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -225,7 +231,8 @@ cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t sme
     return cudaErrorInvalidValue;
   AttnParams copy = p;
   void* args[] = {&copy};
-  return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster);
+  return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster,
+                    (attn_consumer_warps(G, p.cluster > 0) + 1) * 32);
 }
 
 // ---- load-time repack ------------------------------------------------------------

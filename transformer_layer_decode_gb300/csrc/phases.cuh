@@ -40,10 +40,10 @@ struct RingPos {
   }
 };
 
-__device__ __forceinline__ void ring_init(const Ring& R) {
+__device__ __forceinline__ void ring_init(const Ring& R, int consumer_warps = kConsumerWarps) {
   for (int s = 0; s < R.n; ++s) {
     mbar_init(&R.full[s], 1);
-    mbar_init(&R.empty[s], kConsumerWarps);
+    mbar_init(&R.empty[s], consumer_warps);
   }
   fence_mbar_init();
 }
@@ -558,7 +558,7 @@ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 // One unit = one chunk of CH cached positions of one KV head (its K rows, then
 // its V rows, 16 KB each).  The grid splits the units of all KV heads evenly;
 // every CTA serves all G query heads of the KV heads it touches, so each K/V
-// byte is read once.  Within a CTA the 8 consumer warps take interleaved
+// byte is read once.  Within a CTA the consumer warps take interleaved
 // positions of each chunk and keep a running (max, sum, acc) per query head;
 // warps are merged at the end of each head segment.  A head cut between CTAs
 // is merged in one of two ways: (global) each CTA leaves a record in global
@@ -571,8 +571,8 @@ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 // Work area of an attention phase: per-warp states | this CTA's record
 // (cluster merge) | merge scratch (global merge).
 struct AttnLayout {
-  int hd, G;
-  __host__ __device__ size_t rec_off() const { return 4 * (size_t)kConsumerWarps * G * (hd + 2); }
+  int hd, G, nw = kConsumerWarps;  // nw: consumer warps of the kernel
+  __host__ __device__ size_t rec_off() const { return 4 * (size_t)nw * G * (hd + 2); }
   __host__ __device__ size_t merge_off() const { return rec_off() + 4 * (size_t)G * (hd + 2); }
   // the record offsets of the splits of two heads, then the heads to merge
   __host__ __device__ size_t total() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
@@ -692,11 +692,12 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
 
 // Consumer part of an attention phase (q must be ready).  Returns false if a
 // wait ran out.
-template <int HD, int G, bool CL = false>
+template <int HD, int G, bool CL = false, int NW = kConsumerWarps>
 __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, const Ring& R, RingPos& P,
                           const AttnSplit& S, int b, int nb, int tid) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);  // positions per chunk (16 KB of K)
-  constexpr int PW = CH / kConsumerWarps;              // positions per warp per chunk
+  constexpr int NC = NW * 32;                          // consumer threads
+  constexpr int PW = CH / NW;                          // positions per warp per chunk
   constexpr int SUB = 4;                               // positions per online-softmax update
   constexpr int DL = HD / 32;                          // dims per lane
   // Fast form (PW * G <= 32 partial dots per lane): one reduce-scatter
@@ -709,7 +710,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   constexpr int LV = FAST ? ilog2(V) : 0, LPW = ilog2(PW), SH = 5 - LV;
   const int warp = tid >> 5, lane = tid & 31;
   float* ws = reinterpret_cast<float*>(work);  // [warp][G][HD+2]
-  float* crec = reinterpret_cast<float*>(work + AttnLayout{HD, G}.rec_off());  // [G][HD+2]
+  float* crec = reinterpret_cast<float*>(work + AttnLayout{HD, G, NW}.rec_off());  // [G][HD+2]
   const int n = S.n, cph = S.cph, U = S.U, u0 = S.u0, u1 = S.u1, nu = S.nu;
   float m[G], l[G], acc[G][DL];
   float m_mine = -INFINITY, l_mine = 0.f;  // fast form: this lane's head
@@ -749,17 +750,17 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         w[HD + 1] = l[gg];
       }
     }
-    named_barrier(1, kNC);
+    named_barrier(1, NC);
     const int64_t h0 = (int64_t)g * cph, h1 = h0 + cph;
     const bool whole = !CL && h0 >= u0 && h1 <= u1;
     if (!CL && !whole) split_heads[seg_idx == 0 ? 0 : 1] = g;
     float* rec = p.part + ((size_t)b * 2 + (seg_idx == 0 ? 0 : 1)) * G * (HD + 4);
-    for (int i = tid; i < G * HD; i += kNC) {
+    for (int i = tid; i < G * HD; i += NC) {
       const int gg = i / HD, j = i % HD;
       float M = -INFINITY;
-      for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, ws[(w * G + gg) * (HD + 2) + HD]);
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, ws[(w * G + gg) * (HD + 2) + HD]);
       float A = 0.f, Ls = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) {
+      for (int w = 0; w < NW; ++w) {
         const float* wr = ws + (w * G + gg) * (HD + 2);
         const float e = (wr[HD] == -INFINITY) ? 0.f : expf(wr[HD] - M);
         A += wr[j] * e;
@@ -784,13 +785,13 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
     // The records are released to the other CTAs by the ticket below: this
     // barrier orders every thread's writes before thread 0's gpu-scope release.
-    named_barrier(1, kNC);
+    named_barrier(1, NC);
     ++seg_idx;
   };
 
   reset();
   if (CL && nu == 0) {  // no chunk of the head: an empty record
-    for (int i = tid; i < G * (HD + 2); i += kNC) crec[i] = (i % (HD + 2) == HD) ? -INFINITY : 0.f;
+    for (int i = tid; i < G * (HD + 2); i += NC) crec[i] = (i % (HD + 2) == HD) ? -INFINITY : 0.f;
   }
   bool ok = true;
   int g = u0 / cph, c = u0 - g * cph;
@@ -818,7 +819,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     RowSlice<DL> kr[PW], vr[PW];
 #pragma unroll
     for (int i = 0; i < PW; ++i) {
-      const int t = warp + i * kConsumerWarps;
+      const int t = warp + i * NW;
       if (t < rows) {
         kr[i].load(kb + ((size_t)t * HD + lane * DL) * 2);
         vr[i].load(vb + ((size_t)t * HD + lane * DL) * 2);
@@ -854,7 +855,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       }
 #pragma unroll
       for (int o = 16 >> LV; o > 0; o >>= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
-      const float sc = (warp + my_i * kConsumerWarps < rows) ? x[0] : -INFINITY;
+      const float sc = (warp + my_i * NW < rows) ? x[0] : -INFINITY;
       float mx = sc;
 #pragma unroll
       for (int bt = 0; bt < LPW; ++bt) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1 << (SH + bt)));
@@ -874,7 +875,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       }
 #pragma unroll
       for (int i = 0; i < PW; ++i) {
-        if (warp + i * kConsumerWarps >= rows) break;  // warp-uniform
+        if (warp + i * NW >= rows) break;  // warp-uniform
         float vv[DL];
         vr[i].unpack(vv);
 #pragma unroll
@@ -887,11 +888,11 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
 #pragma unroll
     for (int i0 = 0; i0 < (FAST ? 0 : PW); i0 += SUB) {
-      if (warp + i0 * kConsumerWarps >= rows) break;  // warp-uniform
+      if (warp + i0 * NW >= rows) break;  // warp-uniform
       float sc[SUB][G];
 #pragma unroll
       for (int i = 0; i < SUB; ++i) {
-        const int t = warp + (i0 + i) * kConsumerWarps;
+        const int t = warp + (i0 + i) * NW;
         float kv[DL];
         kr[i0 + i].unpack(kv);
 #pragma unroll
@@ -914,7 +915,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         for (int j = 0; j < DL; ++j) acc[gg][j] *= alpha;
 #pragma unroll
         for (int i = 0; i < SUB; ++i) {
-          const int t = warp + (i0 + i) * kConsumerWarps;
+          const int t = warp + (i0 + i) * NW;
           if (t >= rows) continue;
           const float pi = expf(sc[i][gg] - mx);
           ls += pi;
@@ -944,7 +945,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     cluster_sync_all();  // every CTA's record is in its shared memory
     const int C = p.cluster, r = (int)cluster_rank(), gh = b / C;
     const int e0 = split_begin32(G * HD, C, r), e1 = split_begin32(G * HD, C, r + 1);
-    for (int e = e0 + tid; e < e1; e += kNC) {
+    for (int e = e0 + tid; e < e1; e += NC) {
       const int gg = e / HD, j = e - gg * HD;
       float mv[kMaxCluster], lv[kMaxCluster], av[kMaxCluster];
 #pragma unroll
@@ -978,7 +979,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   // ---- heads split over CTAs: the last CTA to finish merges them --------------
   // (tickets are taken after this CTA's whole loop, so merging never stalls it;
   // the split arithmetic is 32-bit: units * grid stays far below 2^31)
-  int* mbase = reinterpret_cast<int*>(work + AttnLayout{HD, G}.merge_off());  // [2][kMaxSplits]
+  int* mbase = reinterpret_cast<int*>(work + AttnLayout{HD, G, NW}.merge_off());  // [2][kMaxSplits]
   int* todo = mbase + 2 * kMaxSplits;                                         // [2]: head, splits
   const int U32 = U;
   auto part_begin = [&](int c) { return split_begin32(U32, nb, c); };
@@ -995,9 +996,9 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
     todo[tid] = head;
   }
-  named_barrier(1, kNC);
+  named_barrier(1, NC);
   // record offset of every split of the heads to merge
-  for (int t = tid; t < 2 * kMaxSplits; t += kNC) {
+  for (int t = tid; t < 2 * kMaxSplits; t += NC) {
     const int i = t / kMaxSplits, sp = t - i * kMaxSplits, g = todo[i];
     int off = -1;
     if (g >= 0) {
@@ -1012,10 +1013,10 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     }
     mbase[t] = off;
   }
-  named_barrier(1, kNC);
+  named_barrier(1, NC);
   // both heads at once; one round trip: each output loads every split's
   // (m, l, acc) together, then combines them in split order
-  for (int t = tid; t < 2 * G * HD; t += kNC) {
+  for (int t = tid; t < 2 * G * HD; t += NC) {
     const int i = t / (G * HD), e = t - i * G * HD;
     const int g = todo[i];
     if (g < 0) continue;
@@ -1048,7 +1049,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     p.o[(size_t)(g * G + gg) * HD + j] = o / Lsum;
   }
   if (tid < 2 && todo[tid] >= 0) p.counters[todo[tid]] = 0;
-  named_barrier(1, kNC);
+  named_barrier(1, NC);
   return ok;
 }
 
