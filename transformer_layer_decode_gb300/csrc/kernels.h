@@ -45,6 +45,10 @@ constexpr int kAttnStageBytes = 32768;  // K chunk + V chunk, 16 KB each
 constexpr int kTimelineSlots = 8;       // u64 per launch of the timeline probe
 // Most attention CTAs one KV head may be split over (bounds the merge).
 constexpr int kMaxSplits = 32;
+#ifndef TLD_COPIES_PER_STAGE
+#define TLD_COPIES_PER_STAGE 4
+#endif
+constexpr int kCopiesPerStage = TLD_COPIES_PER_STAGE;  // bulk copies a GEMV stage is issued as
 constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
 constexpr int kMaxCluster = 16;            // CTAs per KV head in the cluster attention
 constexpr int kStageTiles = 2 * kConsumerWarps;  // two tiles per consumer warp per stage

@@ -289,6 +289,19 @@ __device__ __forceinline__ int q4_block_dot(const uint4 w, const uint4 x0, const
   return d - 8 * sx;
 }
 
+// One stage as kCopiesPerStage bulk copies of about equal size on the same
+// barrier: several copies in flight move a stage into shared memory faster than
+// one large copy (measured: +1.7 % on the 7B-shape stack with four).
+__device__ __forceinline__ void bulk_g2s_split(uint8_t* dst, const uint8_t* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t pol) {
+  const uint32_t part = (bytes / kCopiesPerStage) & ~15u;
+  uint32_t o = 0;
+  if (part > 0)
+#pragma unroll
+    for (int k = 0; k < kCopiesPerStage - 1; ++k, o += part) bulk_g2s_hint(dst + o, src + o, part, bar, pol);
+  bulk_g2s_hint(dst + o, src + o, bytes - o, bar, pol);
+}
+
 // Producer of a GEMV phase: this CTA's slab, whole row blocks [rb0, rb1).
 __device__ __forceinline__ void gemv_produce(const GemvParams& p, const uint8_t* w, const Ring& R,
                                              RingPos& P, int rb0, int rb1, uint64_t pol) {
@@ -304,7 +317,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, const uint8_t*
     const int64_t ob = (s == nst - 1) ? end_off : cur.offset(geo);
     const uint32_t bytes = (uint32_t)(ob - oa);
     mbar_arrive_expect_tx(&R.full[P.slot], bytes);
-    bulk_g2s_hint(R.slot(P.slot), w + oa, bytes, &R.full[P.slot], pol);
+    bulk_g2s_split(R.slot(P.slot), w + oa, bytes, &R.full[P.slot], pol);
     P.next(R.n);
   }
 }
