@@ -92,3 +92,14 @@ def test_missing_library_fails_loudly(tmp_path):
             dec.load_library(str(tmp_path / "nope.so"))
     finally:
         dec._lib = saved
+
+
+def test_quantizer_rounding_matches_ieee_division(tmp_path):
+    """The int8 quantizer's quotients from the reciprocal with one FMA correction
+    equal the IEEE fp32 division (scales, quotients and codes)."""
+    exe = tmp_path / "quant_rounding_check"
+    subprocess.run(["g++", "-O1", "-std=c++17", "-ffp-contract=off",
+                    os.path.join(ROOT, "tests", "host", "quant_rounding_check.cpp"), "-o", str(exe)],
+                   check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0 and "OK" in r.stdout, r.stdout

@@ -203,72 +203,102 @@ __device__ __forceinline__ float warp_reduce4(const float a[4], int lane) {
 // q = 0 when dx == 0.  Eight lanes serve a block, four elements each.  The int8
 // values are stored for dp4a against packed nibbles: in each group of eight,
 // the even elements first, then the odd ones.  sx holds each block's sum of q.
-// The int8 code of z at block scale d (rd = 1/d): round-half-even of the IEEE
-// fp32 quotient z / d, clamped to +-127.  The quotient is formed first with the
-// reciprocal (relative error a few 2^-24, so at most ~2e-5 off for |z/d| <= 127);
-// only where that lands within 1e-3 of a rounding boundary (k + 1/2) does the
-// IEEE division decide, so the codes are exactly those of the division.
-__device__ __forceinline__ int quant_code(float z, float d, float rd) {
-  const float qa = z * rd;
-  const float f = qa - floorf(qa);
-  // (not >=): a block so small that 1/d overflows gives NaN here and divides too
-  const float q = !(fabsf(f - 0.5f) >= 1e-3f) ? __fdiv_rn(z, d) : qa;
-  const int v = __float2int_rn(q);
-  return v > 127 ? 127 : (v < -127 ? -127 : v);
+// Correctly rounded fp32 quotient a / b from rb = RN(1/b): q = RN(a rb), the
+// exact remainder r = a - b q (one FMA), then RN(q + r rb) (Markstein's
+// correction, "Computation of elementary functions on the IBM RISC System/6000
+// processor", 1990).  Normal operands; equal to the IEEE division on every
+// case of the host check (random and next to k + 1/2 quotients).
+__device__ __forceinline__ float div_rn_from_rcp(float a, float b, float rb) {
+  const float q = a * rb;
+  const float r = fmaf(-q, b, a);
+  return fmaf(r, rb, q);
 }
 
 // Per-32-block absmax quantization of xs[0..K) * scale into the dp4a layout of
 // qx (per 8 elements: the four even ones, then the four odd ones), the block
 // scales dx (fp32, amax / 127) and the code sums sx; optionally also the codes in
-// natural order (qtap) and the scales (qstap).
+// natural order (qtap) and the scales (qstap).  A code is round-half-even of the
+// fp32 quotient z / d, clamped to +-127, formed from the block's reciprocal as
+// above (three operations instead of a division).  Eight lanes a block, four
+// elements a lane; each lane group takes kQuantBlocks blocks at once so that
+// their shuffle and arithmetic chains overlap.
+constexpr int kQuantBlocks = 4;
+
 __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, float* dx, int* sx,
                                        int8_t* qtap, float* qstap, int tid, int NC, float scale) {
-  const int lane = tid & 31, sub = lane & 3, warp = tid >> 5;
+  const int lane = tid & 31, sub = lane & 7, warp = tid >> 5;
   const int nblk = K / 32;
-  // Eight blocks per warp per round, four lanes per block, eight elements per
-  // lane; the round count is the same for all lanes of a warp (the shuffles
-  // below name the whole warp).
-  for (int base = warp * 8; base < nblk; base += (NC >> 5) * 8) {
-    const int blk = base + (lane >> 2);
-    const bool live = blk < nblk;
-    const int e = blk * 32 + sub * 8;
-    float z[8];
-    if (live) {
-      const float4 a = *reinterpret_cast<const float4*>(xs + e);
-      const float4 b = *reinterpret_cast<const float4*>(xs + e + 4);
-      z[0] = a.x * scale; z[1] = a.y * scale; z[2] = a.z * scale; z[3] = a.w * scale;
-      z[4] = b.x * scale; z[5] = b.y * scale; z[6] = b.z * scale; z[7] = b.w * scale;
-    } else {
+  constexpr int R = kQuantBlocks;
+  const float r127 = 1.0f / 127.0f;
+  // the trip count is the same for all lanes of a warp (the shuffles name the whole warp)
+  for (int base = warp * 4 * R; base < nblk; base += (NC >> 5) * 4 * R) {
+    float4 z[R];
+    float amax[R];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) z[i] = 0.f;
+    for (int r = 0; r < R; ++r) {
+      const int blk = base + r * 4 + (lane >> 3);
+      z[r] = blk < nblk ? *reinterpret_cast<const float4*>(xs + blk * 32 + sub * 4)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      z[r].x *= scale;
+      z[r].y *= scale;
+      z[r].z *= scale;
+      z[r].w *= scale;
+      amax[r] = fmaxf(fmaxf(fabsf(z[r].x), fabsf(z[r].y)), fmaxf(fabsf(z[r].z), fabsf(z[r].w)));
     }
-    float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(z[i]));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float rd = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.f;
-    int q[8];
+    for (int o = 4; o > 0; o >>= 1)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = d != 0.0f ? quant_code(z[i], d, rd) : 0;
-    int sum = q[0] + q[1] + q[2] + q[3] + q[4] + q[5] + q[6] + q[7];
-    sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-    if (!live) continue;
-    const uint32_t ev = (uint32_t)(q[0] & 0xff) | (uint32_t)(q[2] & 0xff) << 8 |
-                        (uint32_t)(q[4] & 0xff) << 16 | (uint32_t)(q[6] & 0xff) << 24;
-    const uint32_t od = (uint32_t)(q[1] & 0xff) | (uint32_t)(q[3] & 0xff) << 8 |
-                        (uint32_t)(q[5] & 0xff) << 16 | (uint32_t)(q[7] & 0xff) << 24;
-    *reinterpret_cast<uint2*>(qx + e) = make_uint2(ev, od);
-    if (sub == 0) {
-      dx[blk] = d;
-      sx[blk] = sum;
+      for (int r = 0; r < R; ++r) amax[r] = fmaxf(amax[r], __shfl_xor_sync(0xffffffffu, amax[r], o));
+    int q[R][4], sum[R];
+    float dd[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float zz[4] = {z[r].x, z[r].y, z[r].z, z[r].w};
+      float d;
+      if (amax[r] >= 1e-30f) {
+        d = div_rn_from_rcp(amax[r], 127.0f, r127);  // amax / 127
+        const float rd = __frcp_rn(d);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int v = __float2int_rn(div_rn_from_rcp(zz[i], d, rd));
+          q[r][i] = v > 127 ? 127 : (v < -127 ? -127 : v);
+        }
+      } else {  // a block so small that 1/d would overflow (or all zero): IEEE divisions
+        d = __fdiv_rn(amax[r], 127.0f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int v = d != 0.0f ? __float2int_rn(__fdiv_rn(zz[i], d)) : 0;
+          q[r][i] = v > 127 ? 127 : (v < -127 ? -127 : v);
+        }
+      }
+      sum[r] = q[r][0] + q[r][1] + q[r][2] + q[r][3];
+      dd[r] = d;
     }
-    if (qtap) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) qtap[e + i] = (int8_t)q[i];
-      if (sub == 0) qstap[blk] = d;
+    for (int o = 4; o > 0; o >>= 1)
+#pragma unroll
+      for (int r = 0; r < R; ++r) sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], o);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int blk = base + r * 4 + (lane >> 3);
+      if (blk >= nblk) continue;
+      const int e = blk * 32 + sub * 4;
+      // elements e..e+3 = 8g + 4h + {0,1,2,3}: evens go to bytes 8g+2h, 8g+2h+1,
+      // odds to bytes 8g+4+2h, 8g+4+2h+1
+      const int g8 = e & ~7, h = (e >> 2) & 1;
+      *reinterpret_cast<uint16_t*>(qx + g8 + 2 * h) =
+          (uint16_t)((q[r][0] & 0xff) | ((q[r][2] & 0xff) << 8));
+      *reinterpret_cast<uint16_t*>(qx + g8 + 4 + 2 * h) =
+          (uint16_t)((q[r][1] & 0xff) | ((q[r][3] & 0xff) << 8));
+      if (sub == 0) {
+        dx[blk] = dd[r];
+        sx[blk] = sum[r];
+      }
+      if (qtap) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) qtap[e + i] = (int8_t)q[r][i];
+        if (sub == 0) qstap[blk] = dd[r];
+      }
     }
   }
 }
