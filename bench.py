@@ -5,7 +5,12 @@ dim 128, FFN 11008) with the KV cache prefilled to 2047 positions, through the
 library's C ABI (captured CUDA graph, fused plan).  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--no-cpu-baseline]
+                  [--workload NAME] [--no-cpu-baseline] [--layers L]
+                  [--plan fused|persistent|unfused] [--eager]
+                  [--no-pdl] [--no-l2-ahead] [--global-merge]
+
+The last five select the ablations of the default plan (fused kernels, CUDA
+graph, programmatic dependent launch, L2 look-ahead, cluster attention).
 
 --impl reference times the fp64 CPU oracle on the host cores on the same
 workload (the slow reference arm).  Under torchrun each rank decodes its own
@@ -17,6 +22,7 @@ import argparse
 import hashlib
 import json
 import os
+import re
 import subprocess
 import sys
 import threading
@@ -124,12 +130,20 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(src: str) -> str:
+    """C++ source without comments and blank lines (comment edits do not change a kernel)."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_sha() -> str:
+    """Hash of the fused kernels' code (the sources the profiled traffic was taken on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "transformer_layer_decode_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.startswith("kernels_fused") or f in ("common.cuh", "kernels.h", "phases.cuh"):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+            h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -5,8 +5,10 @@
 // removes the barrier by removing the write"):
 //   K1 gemv<PRO_NORM,  EPI_QKV>    RMSNorm*w, [Wq;Wk;Wv] GEMV, RoPE on q and k
 //                                  and the k/v append in the epilogue
-//   K2 attn_decode                 GQA split-KV attention; a head split over
-//                                  CTAs is merged by the last one to finish
+//   K2 attn_decode                 GQA split-KV attention: one thread-block
+//                                  cluster per KV head, merged in distributed
+//                                  shared memory (or a flat grid whose split
+//                                  heads the last CTA of each merges)
 //   K3 gemv<PRO_PLAIN, EPI_RESID>  Wo GEMV + residual add
 //   K4 gemv<PRO_NORM,  EPI_SWIGLU> RMSNorm*w, interleaved gate/up GEMV,
 //                                  silu(g)*u in the epilogue (g, u never stored)

@@ -4,9 +4,9 @@
 //
 // Every phase streams its bytes (weights, or K/V rows) through one ring of
 // shared-memory stages: a producer thread fills stages with 1-D bulk copies
-// (TMA) that complete on the stage's "full" mbarrier; the eight consumer warps
-// copy their part of a stage to registers, arrive on its "empty" mbarrier and
-// compute.  A ring position counts stages since the ring was initialised, so
+// (TMA) that complete on the stage's "full" mbarrier; the consumer warps (eight;
+// sixteen in some attention kernels) copy their part of a stage to registers,
+// arrive on its "empty" mbarrier and compute.  A ring position counts stages since the ring was initialised, so
 // one ring can carry the stages of many phases back to back.
 #pragma once
 #include <cuda_fp16.h>
