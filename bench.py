@@ -340,6 +340,10 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     from transformer_layer_decode_gb300 import build as tld_build
     from transformer_layer_decode_gb300 import dec, synth, workload
+    if world > 1:  # one rank compiles (if anything is stale); the others wait for it
+        if rank == 0:
+            tld_build.build()
+        dist.barrier()
     tld_build.build()
     dev = torch.device("cuda", local_rank)
     K, W = args.steps, args.warmup
