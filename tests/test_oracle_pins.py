@@ -366,9 +366,82 @@ def pin_q4_layer():
     _close(moved - out, step, 1e-9, "one int8 code of the down input")
 
 
+def pin_layer_brute_force():
+    """The hidden-8 toy layer written out as explicit scalar sums in plain Python
+    (no matrix routine): two q heads sharing one KV head, head dim 4, FFN 16,
+    three decode steps from an empty cache."""
+    H, nq, nkv, d, Fd, eps, theta = 8, 2, 1, 4, 16, 1e-6, 1e4
+    lw = _toy_layer(H, nq, nkv, d, Fd)
+    st = orc.OracleStack(hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=d, ffn=Fd,
+                         max_ctx=4, layers=[lw], rms_eps=eps, rope_theta=theta)
+    W = [_bf16_f64(w).tolist() for w in lw["w"]]
+    g_in, g_post = _bf16_f64(lw["attn_norm"]).tolist(), _bf16_f64(lw["ffn_norm"]).tolist()
+
+    def bf16(v):  # the cache's storage rounding (fp32, then round-to-nearest-even bf16)
+        return float(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).to(torch.float64)[0])
+
+    def rms(v, g):
+        ms = 0.0
+        for e in v:
+            ms += e * e
+        r = 1.0 / math.sqrt(ms / len(v) + eps)
+        return [v[i] * r * g[i] for i in range(len(v))]
+
+    def mv(M, v):
+        out = []
+        for row in M:
+            acc = 0.0
+            for i in range(len(v)):
+                acc += row[i] * v[i]
+            out.append(acc)
+        return out
+
+    def rope(v, pos):
+        out = list(v)
+        for h in range(len(v) // d):
+            for i in range(d // 2):
+                ang = pos * theta ** (-2.0 * i / d)
+                a, b = v[h * d + i], v[h * d + i + d // 2]
+                out[h * d + i] = a * math.cos(ang) - b * math.sin(ang)
+                out[h * d + i + d // 2] = a * math.sin(ang) + b * math.cos(ang)
+        return out
+
+    Kc, Vc = [], []
+    for step in range(3):
+        pos = step
+        x = RNG.normal(0, 1, H).tolist()
+        n1 = rms(x, g_in)
+        q, k, v = rope(mv(W[0], n1), pos), rope(mv(W[1], n1), pos), mv(W[2], n1)
+        Kc.append([bf16(e) for e in k])
+        Vc.append([bf16(e) for e in v])
+        o = []
+        for h in range(nq):  # both q heads read KV head 0
+            s = []
+            for t in range(pos + 1):
+                dot = 0.0
+                for i in range(d):
+                    dot += q[h * d + i] * Kc[t][i]
+                s.append(dot / math.sqrt(d))
+            m = max(s)
+            e = [math.exp(z - m) for z in s]
+            tot = sum(e)
+            for i in range(d):
+                acc = 0.0
+                for t in range(pos + 1):
+                    acc += e[t] / tot * Vc[t][i]
+                o.append(acc)
+        h1 = [x[i] + y for i, y in enumerate(mv(W[3], o))]
+        n2 = rms(h1, g_post)
+        gt, up = mv(W[4], n2), mv(W[5], n2)
+        a = [gt[j] / (1.0 + math.exp(-gt[j])) * up[j] for j in range(Fd)]
+        ref = [h1[i] + y for i, y in enumerate(mv(W[6], a))]
+        got = st.step(np.array(x), pos)
+        _close(got, np.array(ref), 1e-12, f"hidden-8 brute force, step {step}")
+
+
 PINS = [pin_storage_formats, pin_rmsnorm, pin_gemv, pin_rope, pin_attention, pin_swiglu,
         pin_quant, pin_q4_dots, pin_layer, pin_residual_wiring, pin_kv_append_closed_form,
-        pin_q4_layer]
+        pin_q4_layer, pin_layer_brute_force]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
