@@ -51,6 +51,9 @@ enum {
   MUT_GEMV_TRANSPOSE = 9,   /* weight read as [in][out] */
   MUT_Q4_NO_OFFSET = 10,    /* nibble read without the -8 offset */
   MUT_ATTN_SKIP_LAST = 11,  /* new token does not attend to itself */
+  MUT_Q4_STALE_N1 = 12,     /* gate/up input reuses the int8 codes of n1 */
+  MUT_Q4_O_TENSOR_SCALE = 13, /* o quantized with one scale over the whole vector */
+  MUT_Q4_A_NO_DX = 14,      /* down projection drops the block scales of a */
 };
 
 /* ---- storage formats ---------------------------------------------------- */
@@ -279,7 +282,20 @@ static void quantize_input(const orc_dims* D, orc_qtap* tap, int slot, const dou
     memcpy(dbuf, tap->d[slot], sizeof(float) * (size_t)(K / 32));
     return;
   }
-  orc_quantize_act(z, K, qbuf, dbuf);
+  if (g_mutation == MUT_Q4_O_TENSOR_SCALE && slot == 1) {
+    /* planted mistake: one absmax over all of o instead of one per block */
+    double amax = 0.0;
+    for (int i = 0; i < K; ++i)
+      if (fabs(z[i]) > amax) amax = fabs(z[i]);
+    float d = (float)amax / 127.0f;
+    for (int i = 0; i < K; ++i) {
+      int q = d != 0.0f ? (int)nearbyintf((float)z[i] / d) : 0;
+      qbuf[i] = (int8_t)(q > 127 ? 127 : (q < -127 ? -127 : q));
+    }
+    for (int b = 0; b < K / 32; ++b) dbuf[b] = d;
+  } else {
+    orc_quantize_act(z, K, qbuf, dbuf);
+  }
   if (tap && tap->q[slot]) {
     memcpy(tap->q[slot], qbuf, (size_t)K);
     memcpy(tap->d[slot], dbuf, sizeof(float) * (size_t)(K / 32));
@@ -289,10 +305,17 @@ static void quantize_input(const orc_dims* D, orc_qtap* tap, int slot, const dou
 /* y = W x: bf16 weights on x itself, q4 weights on x's quantized form. */
 static void project(const orc_dims* D, const orc_layer* L, int which, int N, int K,
                     const double* x, double* y, const int8_t* qbuf, const float* dbuf) {
-  if (!D->q4)
+  if (!D->q4) {
     orc_gemv_bf16(L->w[which], N, K, x, y);
-  else
+  } else if (g_mutation == MUT_Q4_A_NO_DX && which == W_DOWN) {
+    /* planted mistake: the block scales of a left out of the down projection */
+    float* ones = (float*)malloc(sizeof(float) * (size_t)(K / 32));
+    for (int b = 0; b < K / 32; ++b) ones[b] = 1.0f;
+    orc_gemv_q4(L->q[which], L->s[which], N, K, qbuf, ones, y);
+    free(ones);
+  } else {
     orc_gemv_q4(L->q[which], L->s[which], N, K, qbuf, dbuf, y);
+  }
 }
 
 /* x[H] -> out[H] at position pos; appends this token's k, v to row pos. */
@@ -315,11 +338,17 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   double* a = (double*)malloc(sizeof(double) * F);
   int8_t* qb = (int8_t*)malloc((size_t)Kmax);
   float* db = (float*)malloc(sizeof(float) * (size_t)(Kmax / 32 + 1));
+  int8_t* qb_n1 = (int8_t*)malloc((size_t)H);               /* planted-mistake hook only */
+  float* db_n1 = (float*)malloc(sizeof(float) * (size_t)(H / 32 + 1));
 
   /* input RMSNorm + weight multiply */
   orc_rmsnorm(x, L->attn_norm, H, D->rms_eps, n1);
   /* q, k, v projections */
   quantize_input(D, tap, 0, n1, H, qb, db);
+  if (D->q4) {
+    memcpy(qb_n1, qb, (size_t)H);
+    memcpy(db_n1, db, sizeof(float) * (size_t)(H / 32));
+  }
   project(D, L, W_Q, nq * d, H, n1, q, qb, db);
   project(D, L, W_K, nkv * d, H, n1, k, qb, db);
   project(D, L, W_V, nkv * d, H, n1, v, qb, db);
@@ -349,6 +378,10 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   orc_rmsnorm(h1, L->ffn_norm, H, D->rms_eps, n2);
   /* gate, up, SwiGLU */
   quantize_input(D, tap, 2, n2, H, qb, db);
+  if (D->q4 && g_mutation == MUT_Q4_STALE_N1) {  /* planted mistake: n1's codes reused */
+    memcpy(qb, qb_n1, (size_t)H);
+    memcpy(db, db_n1, sizeof(float) * (size_t)(H / 32));
+  }
   project(D, L, W_GATE, F, H, n2, g, qb, db);
   project(D, L, W_UP, F, H, n2, u, qb, db);
   orc_swiglu(g, u, F, a);
@@ -358,7 +391,7 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   for (int i = 0; i < H; ++i) out[i] = (g_mutation == MUT_NO_RESIDUAL2) ? y[i] : h1[i] + y[i];
 
   free(n1); free(q); free(k); free(v); free(o); free(h1); free(y); free(n2);
-  free(g); free(u); free(a); free(qb); free(db);
+  free(g); free(u); free(a); free(qb); free(db); free(qb_n1); free(db_n1);
   return 0;
 }
 

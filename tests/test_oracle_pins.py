@@ -439,9 +439,152 @@ def pin_layer_brute_force():
         _close(got, np.array(ref), 1e-12, f"hidden-8 brute force, step {step}")
 
 
+def _quantize_block_py(z):
+    """One 32-block of a GEMV input quantized to int8, written from the reading
+    (absmax scale in fp32, fp32 quotient, round half to even, clamp to +-127),
+    with numpy float32 scalars for the fp32 steps and Python's round (ties to
+    even) for the rounding; independent of the oracle's C quantizer."""
+    amax = 0.0
+    for v in z:
+        amax = max(amax, abs(v))
+    d = np.float32(np.float32(amax) / np.float32(127.0))
+    q = []
+    for v in z:
+        if d == 0:
+            q.append(0)
+        else:
+            r = round(float(np.float32(np.float32(v) / d)))
+            q.append(max(-127, min(127, r)))
+    return q, float(d)
+
+
+def _q4_layer_py(x, lw, pos, Kc, Vc, nq, nkv, d, eps, theta):
+    """One int4-weight / int8-activation layer as explicit scalar sums in plain
+    Python.  Kc, Vc: the layer's cache rows so far ([nkv] lists of rows of
+    floats); this token's k, v rows are appended.  Returns (out, codes) with
+    codes the four GEMV inputs' int8 codes (n1, o, n2, a)."""
+    H = len(x)
+
+    def deq_mv(packed, scales, z):
+        qz, dz = [], []
+        for b in range(len(z) // 32):
+            qb, db = _quantize_block_py(z[32 * b: 32 * b + 32])
+            qz += qb
+            dz.append(db)
+        out = []
+        for j in range(packed.shape[0]):
+            acc = 0.0
+            for b in range(len(z) // 32):
+                idot = 0
+                for i in range(32):
+                    k = 32 * b + i
+                    byte = int(packed[j, k // 2])
+                    nib = (byte >> 4) if k % 2 else (byte & 15)
+                    idot += (nib - 8) * qz[k]
+                sw = float(np.uint16(scales[j, b]).view(np.float16))
+                acc += sw * dz[b] * idot
+            out.append(acc)
+        return out, qz
+
+    def rms(v, g):
+        ms = 0.0
+        for e in v:
+            ms += e * e
+        r = 1.0 / math.sqrt(ms / len(v) + eps)
+        return [v[i] * r * g[i] for i in range(len(v))]
+
+    def rope(v):
+        out = list(v)
+        for h in range(len(v) // d):
+            for i in range(d // 2):
+                ang = pos * theta ** (-2.0 * i / d)
+                a, b = v[h * d + i], v[h * d + i + d // 2]
+                out[h * d + i] = a * math.cos(ang) - b * math.sin(ang)
+                out[h * d + i + d // 2] = a * math.sin(ang) + b * math.cos(ang)
+        return out
+
+    def bf16(v):  # cache storage rounding (torch's cast)
+        return float(torch.tensor([v], dtype=torch.float64).to(torch.bfloat16).to(torch.float64)[0])
+
+    W = lw["q4"]
+    g_in, g_post = _bf16_f64(lw["attn_norm"]).tolist(), _bf16_f64(lw["ffn_norm"]).tolist()
+    n1 = rms(x, g_in)
+    q, c0 = deq_mv(*W[0], n1)
+    k, _ = deq_mv(*W[1], n1)
+    v, _ = deq_mv(*W[2], n1)
+    q, k = rope(q), rope(k)
+    for g in range(nkv):
+        Kc[g].append([bf16(e) for e in k[g * d:(g + 1) * d]])
+        Vc[g].append([bf16(e) for e in v[g * d:(g + 1) * d]])
+    o = []
+    for h in range(nq):
+        g = h * nkv // nq
+        s = []
+        for t in range(len(Kc[g])):
+            dot = 0.0
+            for i in range(d):
+                dot += q[h * d + i] * Kc[g][t][i]
+            s.append(dot / math.sqrt(d))
+        m = max(s)
+        e = [math.exp(z - m) for z in s]
+        tot = sum(e)
+        for i in range(d):
+            acc = 0.0
+            for t in range(len(s)):
+                acc += e[t] / tot * Vc[g][t][i]
+            o.append(acc)
+    y, c1 = deq_mv(*W[3], o)
+    h1 = [x[i] + y[i] for i in range(H)]
+    n2 = rms(h1, g_post)
+    gt, c2 = deq_mv(*W[4], n2)
+    up, _ = deq_mv(*W[5], n2)
+    a = [gt[j] / (1.0 + math.exp(-gt[j])) * up[j] for j in range(len(gt))]
+    y, c3 = deq_mv(*W[6], a)
+    return [h1[i] + y[i] for i in range(H)], (c0, c1, c2, c3)
+
+
+def _q4_toy_layer(H, nq, nkv, d, Fd, scale_std):
+    shapes = [(nq * d, H), (nkv * d, H), (nkv * d, H), (H, nq * d), (Fd, H), (Fd, H), (H, Fd)]
+    q4 = []
+    for o, i in shapes:
+        qw = RNG.integers(-8, 8, (o, i))
+        sc = np.abs(RNG.normal(0, scale_std, (o, i // 32))).astype(np.float16).view(np.uint16)
+        q4.append((_pack_q4(qw), sc))
+    return dict(attn_norm=_rand_bf16(H, 0.1, 1.0), ffn_norm=_rand_bf16(H, 0.1, 1.0), q4=q4)
+
+
+def pin_q4_layer_restated():
+    """Whole int4/int8 layers against the plain-Python restatement above: every
+    GEMV input's int8 codes equal and every layer output within 1e-12, over
+    consecutive steps with a prefilled cache.  Shapes: o shorter than the hidden
+    vector (MHA) and o as long as it (GQA 2), FFN of three and two blocks."""
+    for H, nq, nkv, d, Fd, prefill, steps, sstd in ((64, 2, 2, 16, 96, 3, 2, 0.05),
+                                                     (96, 4, 2, 16, 64, 0, 2, 0.03)):
+        eps, theta = 1e-6, 1e4
+        lw = _q4_toy_layer(H, nq, nkv, d, Fd, sstd)
+        st = orc.OracleStack(hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=d, ffn=Fd,
+                             max_ctx=prefill + steps + 1, layers=[lw], rms_eps=eps,
+                             rope_theta=theta, q4=True)
+        Kp, Vp = _rand_bf16((nkv, prefill, d)), _rand_bf16((nkv, prefill, d))
+        if prefill:
+            st.load_kv(0, Kp, Vp)
+        Kc = [[list(r) for r in _bf16_f64(Kp[g])] for g in range(nkv)]
+        Vc = [[list(r) for r in _bf16_f64(Vp[g])] for g in range(nkv)]
+        for s in range(steps):
+            pos = prefill + s
+            x = RNG.normal(0, 1, H).tolist()
+            out, taps = st.layer_step(0, np.array(x), pos, qtap=True)
+            ref, codes = _q4_layer_py(x, lw, pos, Kc, Vc, nq, nkv, d, eps, theta)
+            for slot in range(4):
+                assert np.array_equal(taps[slot][0].astype(np.int64), np.array(codes[slot])), \
+                    f"q4 layer H={H} pos={pos}: int8 codes of GEMV input {slot} differ"
+            _close(out, np.array(ref), 1e-12, f"q4 layer H={H} pos={pos}")
+            st.kv_len = pos + 1
+
+
 PINS = [pin_storage_formats, pin_rmsnorm, pin_gemv, pin_rope, pin_attention, pin_swiglu,
         pin_quant, pin_q4_dots, pin_layer, pin_residual_wiring, pin_kv_append_closed_form,
-        pin_q4_layer, pin_layer_brute_force]
+        pin_q4_layer, pin_layer_brute_force, pin_q4_layer_restated]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
