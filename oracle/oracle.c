@@ -262,22 +262,31 @@ typedef struct orc_layer {
 
 enum { W_Q = 0, W_K, W_V, W_O, W_GATE, W_UP, W_DOWN };
 
-/* The int8 codes of the four GEMV inputs of a layer (n1, o, n2, a).  given = 0:
- * the layer's own codes are copied out.  given != 0: the layer uses these codes
- * instead of quantizing; the configs' integer dots are defined on whatever codes
- * the quantizer decided, and a decision made on fp32 values elsewhere may differ
- * by one from this fp64 chain's where a value sits on a rounding boundary. */
+/* The int8 codes of the four GEMV inputs of a layer (n1, o, n2, a), slot by
+ * slot.  Bit s of `given` clear: slot s is quantized here and, if q[s] is set,
+ * its codes and scales are copied out.  Bit s set: slot s uses q[s], d[s]
+ * instead of quantizing.  z[s], if set, receives the fp64 vector slot s
+ * quantizes (or would quantize).  The integer dots are defined on whatever
+ * codes the quantizer decided; a decision made on fp32 values elsewhere may
+ * differ by one from this fp64 chain's where a value sits on a rounding
+ * boundary, and feeding one side's codes to the other separates that from the
+ * arithmetic around it. */
 typedef struct orc_qtap {
   int8_t* q[4];
   float* d[4];
+  double* z[4];
+  double* kz;        /* optional: this token's rotated k [n_kv*d], fp64, before storage */
+  double* vz;        /* optional: this token's v [n_kv*d], fp64, before storage */
   int32_t given;
+  int32_t kv_given;  /* nonzero: the cache row pos already holds this token's k, v */
 } orc_qtap;
 
 /* The quantized form of GEMV input `slot` (bf16 weights: nothing to do). */
 static void quantize_input(const orc_dims* D, orc_qtap* tap, int slot, const double* z, int K,
                            int8_t* qbuf, float* dbuf) {
   if (!D->q4) return;
-  if (tap && tap->given && tap->q[slot]) {
+  if (tap && tap->z[slot]) memcpy(tap->z[slot], z, sizeof(double) * (size_t)K);
+  if (tap && ((tap->given >> slot) & 1) && tap->q[slot]) {
     memcpy(qbuf, tap->q[slot], (size_t)K);
     memcpy(dbuf, tap->d[slot], sizeof(float) * (size_t)(K / 32));
     return;
@@ -355,13 +364,17 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   /* RoPE on q and k */
   orc_rope(q, nq, d, pos, D->rope_theta);
   orc_rope(k, nkv, d, pos, D->rope_theta);
-  /* KV append at row pos */
-  for (int hh = 0; hh < nkv; ++hh)
-    for (int i = 0; i < d; ++i) {
-      size_t at = ((size_t)hh * D->max_ctx + pos) * d + i;
-      L->kcache[at] = orc_bf16_round(k[hh * d + i]);
-      L->vcache[at] = orc_bf16_round(v[hh * d + i]);
-    }
+  if (tap && tap->kz) memcpy(tap->kz, k, sizeof(double) * (size_t)nkv * d);
+  if (tap && tap->vz) memcpy(tap->vz, v, sizeof(double) * (size_t)nkv * d);
+  /* KV append at row pos (storage rounding to bf16 is itself a decision made
+     on floating point; a test may hand the row in instead, see orc_qtap) */
+  if (!(tap && tap->kv_given))
+    for (int hh = 0; hh < nkv; ++hh)
+      for (int i = 0; i < d; ++i) {
+        size_t at = ((size_t)hh * D->max_ctx + pos) * d + i;
+        L->kcache[at] = orc_bf16_round(k[hh * d + i]);
+        L->vcache[at] = orc_bf16_round(v[hh * d + i]);
+      }
   /* attention over rows 0..pos */
 #pragma omp parallel for schedule(static)
   for (int hq = 0; hq < nq; ++hq) {

@@ -50,7 +50,9 @@ class Layer(ctypes.Structure):
 
 
 class QTap(ctypes.Structure):
-    _fields_ = [("q", ctypes.c_void_p * 4), ("d", ctypes.c_void_p * 4), ("given", ctypes.c_int32)]
+    _fields_ = [("q", ctypes.c_void_p * 4), ("d", ctypes.c_void_p * 4),
+                ("z", ctypes.c_void_p * 4), ("kz", ctypes.c_void_p), ("vz", ctypes.c_void_p),
+                ("given", ctypes.c_int32), ("kv_given", ctypes.c_int32)]
 
 
 _lib = None
@@ -281,31 +283,52 @@ class OracleStack:
         self.kv_len = pos + 1
         return (out, taps) if per_layer else out
 
-    def layer_step(self, layer: int, x, pos: int, qtap: bool = False, qgiven=None):
-        """One layer alone (does not advance kv_len).  qtap: also return the int8
-        codes and scales of the four GEMV inputs.  qgiven: four (codes, scales)
-        pairs the q4 layer uses instead of quantizing its own GEMV inputs."""
+    def layer_step(self, layer: int, x, pos: int, qtap: bool = False, qgiven=None,
+                   zout: bool = False, kv_given: bool = False, kvz: bool = False):
+        """One layer alone (does not advance kv_len).
+
+        For q4 stacks: qtap returns, with the output, the int8 codes and scales
+        of the four GEMV inputs (n1, o, n2, a) as a list of (codes, scales)
+        pairs, or (codes, scales, z) triples with zout, z being the fp64 vector
+        each slot quantizes.  qgiven: four entries, each a (codes, scales) pair
+        the layer uses for that GEMV input instead of quantizing it, or None to
+        quantize it here.  Any stack: kv_given leaves the cache row pos as it
+        is (the caller wrote this token's k, v there) instead of appending;
+        kvz also returns this token's rotated k and v in fp64 ([n_kv][d] each),
+        before the storage rounding.  Returns out, (out, codes), (out, kv) or
+        (out, codes, kv) accordingly."""
         x = _f64(x)
         out = np.empty(self.hidden, dtype=np.float64)
-        tap = None
-        tap_arrays = None
-        if qgiven is not None:
-            tap_arrays = [(np.ascontiguousarray(qq, np.int8), np.ascontiguousarray(dd, np.float32))
-                          for qq, dd in qgiven]
-            tap = QTap()
-            tap.given = 1
-            for i, (qq, dd) in enumerate(tap_arrays):
-                tap.q[i], tap.d[i] = _p(qq), _p(dd)
-        elif qtap:
+        tap = QTap()
+        arrays = None
+        if qtap or zout or qgiven is not None:
             H, F = self.hidden, self.dims.ffn
             qd = self.dims.n_q_heads * self.dims.head_dim
-            tap_arrays = [(np.empty(K, np.int8), np.empty(K // 32, np.float32))
-                          for K in (H, qd, H, F)]
-            tap = QTap()
-            for i, (qq, dd) in enumerate(tap_arrays):
-                tap.q[i], tap.d[i] = _p(qq), _p(dd)
+            arrays = []
+            for i, K in enumerate((H, qd, H, F)):
+                g = qgiven[i] if qgiven is not None else None
+                if g is not None:
+                    qq = np.ascontiguousarray(g[0], np.int8)
+                    dd = np.ascontiguousarray(g[1], np.float32)
+                    tap.given |= 1 << i
+                else:
+                    qq, dd = np.empty(K, np.int8), np.empty(K // 32, np.float32)
+                zz = np.empty(K, np.float64) if zout else None
+                tap.q[i], tap.d[i], tap.z[i] = _p(qq), _p(dd), _p(zz)
+                arrays.append((qq, dd, zz) if zout else (qq, dd))
+        kv = None
+        if kvz:
+            nkv, d = self.dims.n_kv_heads, self.dims.head_dim
+            kv = (np.empty((nkv, d), np.float64), np.empty((nkv, d), np.float64))
+            tap.kz, tap.vz = _p(kv[0]), _p(kv[1])
+        tap.kv_given = int(bool(kv_given))
         rc = lib().orc_layer_step(ctypes.byref(self.dims), ctypes.byref(self._layers[layer]), pos,
-                                  _p(x), _p(out), ctypes.byref(tap) if tap is not None else None)
+                                  _p(x), _p(out), ctypes.byref(tap))
         if rc != 0:
             raise ValueError(f"oracle layer step failed (rc={rc})")
-        return (out, tap_arrays) if qtap else out
+        res = (out,)
+        if qtap or zout:
+            res += (arrays,)
+        if kvz:
+            res += (kv,)
+        return res[0] if len(res) == 1 else res

@@ -325,6 +325,14 @@ def pin_kv_append_closed_form():
     assert np.all(st.kcache[0, :, 1:] == 0xABCD) and np.all(st.vcache[0, :, 1:] == 0xABCD)
     # the bf16 of x/sqrt(1.25) by hand: 1/sqrt(1.25) = 0.894427..., bf16 -> 0.89453125
     assert orc.bf16_value(orc.bf16_round(r)) == 0.89453125
+    # the fp64 k, v before the storage rounding come out and round to the row;
+    # with the row handed in, the layer leaves it as it is and attends to it
+    out, (kz, vz) = st.layer_step(0, x, 0, kvz=True)
+    _close(kz, (x[: nkv * d] * r).reshape(nkv, d), 1e-15, "pre-rounding k")
+    _close(vz, (x[: nkv * d][::-1] * r).reshape(nkv, d), 1e-15, "pre-rounding v")
+    st.vcache[0, :, 0] = 0
+    moved = st.layer_step(0, x, 0, kv_given=True)
+    assert np.all(st.vcache[0, :, 0] == 0) and not np.array_equal(moved, out)
 
 
 def pin_q4_layer():
@@ -357,6 +365,15 @@ def pin_q4_layer():
     # scale * dx_b * w[j][k] (the residual and everything before stay put)
     again = st.layer_step(0, x, 0, qgiven=taps)
     assert np.array_equal(again, out)
+    # slot by slot: the first slot's own codes given, the rest quantized here,
+    # reproduce the layer; each slot's fp64 input vector comes out and
+    # quantizes to that slot's codes
+    part, trip = st.layer_step(0, x, 0, qgiven=[taps[0], None, None, None], zout=True)
+    assert np.array_equal(part, out)
+    _close(trip[0][2], n1, 0, "z of the q projection's input")
+    for slot in range(4):
+        qz, dz = orc.quantize_act(trip[slot][2])
+        assert np.array_equal(qz, trip[slot][0]) and np.array_equal(dz, trip[slot][1]), slot
     k = 37
     qa = taps[3][0].copy()
     assert abs(int(qa[k])) < 127
