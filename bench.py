@@ -2,15 +2,18 @@
 
 One step = one token through all 32 layers (hidden 4096, 32 heads MHA, head
 dim 128, FFN 11008) with the KV cache prefilled to 2047 positions, through the
-library's C ABI (captured CUDA graph, fused plan).  Prints one JSON line.
+library's C ABI (captured CUDA graph, fused plan of five kernels per layer).
+Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--no-cpu-baseline] [--layers L]
-                  [--plan fused|persistent|unfused] [--eager]
+                  [--plan fused|three|persistent|unfused] [--eager]
                   [--no-pdl] [--no-l2-ahead] [--global-merge]
 
-The last five select the ablations of the default plan (fused kernels, CUDA
-graph, programmatic dependent launch, L2 look-ahead, cluster attention).
+The last five select the ablations of the default plan (five fused kernels a
+layer, CUDA graph, programmatic dependent launch, L2 look-ahead, attention as
+one cluster per KV head); --plan three runs three kernels a layer (attention +
+o-proj and gate/up + down each one launch of two phases).
 
 --impl reference times the fp64 CPU oracle on the host cores on the same
 workload (the slow reference arm).  Under torchrun each rank decodes its own
@@ -34,7 +37,9 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
-DOMINANT_KERNEL = 3  # norm + gate/up + SwiGLU: the largest weight stream of the layer
+# the kernel with the largest stream of the layer, per plan (index within the layer)
+DOMINANT_KERNEL = {"three": 2, "fused": 3}  # gate/up (+ down in the three-kernel plan)
+DOMINANT_NAME = {"three": "norm_gateup_swiglu_down_residual", "fused": "norm_gateup_swiglu"}
 
 
 def parse():
@@ -47,9 +52,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only)")
-    ap.add_argument("--plan", default="fused", choices=["fused", "persistent", "unfused"],
-                    help="fused five-kernel layer, the persistent per-token kernel, or the "
-                         "one-kernel-per-op ablation")
+    ap.add_argument("--plan", default="fused", choices=["fused", "three", "persistent", "unfused"],
+                    help="fused five-kernel layer, the three-kernel layer, the persistent "
+                         "per-token kernel, or the one-kernel-per-op ablation")
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--no-pdl", action="store_true",
                     help="fused plan: no programmatic dependent launch between kernels")
@@ -95,10 +100,16 @@ def bytes_per_token(w, n_ctx_avg: float) -> dict:
             "total": weights + kv_read + kv_append}
 
 
-def kernel_bytes(w, kernel: int, n_ctx: int) -> int:
+def kernel_bytes(w, kernel: int, n_ctx: int, plan: str = "fused") -> int:
     """Algorithmic bytes of one launch of a fused kernel (weights, norm vector,
-    input and output vectors; for attention the K/V rows read and q, o)."""
+    input and output vectors; for attention the K/V rows read and q, o).
+    kernel: index within the layer of the five-kernel plan, or of the
+    three-kernel plan (0 QKV, 1 attention + o-proj, 2 gate/up + down)."""
     H, F, hd, nq, nkv = w.hidden, w.ffn, w.head_dim, w.n_q_heads, w.n_kv_heads
+    if plan == "three" and kernel > 0:
+        parts = (1, 2) if kernel == 1 else (3, 4)
+        # the phases' shared vector (o, a) is written once and read once
+        return sum(kernel_bytes(w, k, n_ctx) for k in parts)
     bpp = 2.0 if w.weight_fmt == "bf16" else 0.5 + 2.0 / 32  # bytes per weight
     if kernel == 0:
         return int(bpp * (nq + 2 * nkv) * hd * H) + 2 * H + 4 * H + 4 * nq * hd + 2 * 2 * nkv * hd
@@ -147,10 +158,10 @@ def kernel_source_sha() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", f"traffic_{workload}.json")
+    p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
     if not os.path.exists(p):
         return None
     try:
@@ -354,7 +365,7 @@ def run_ours(args, w, rank, world, local_rank):
     d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=want_cpu, unfused=unfused,
                                     persistent=persistent, graph=not args.eager,
                                     pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
-                                    cluster_attn=not args.global_merge)
+                                    cluster_attn=not args.global_merge, three=args.plan == "three")
     info = d.info()
     H = w.hidden
     xs = torch.from_numpy(workload.step_inputs(w, max(K, W))).to(dev)
@@ -418,7 +429,8 @@ def run_ours(args, w, rank, world, local_rank):
 
     # ---- dominant kernel alone: back to back over all layers' weights ----------
     n_ctx = w.prefill + K  # KV length after the timed steps
-    kb = kernel_bytes(w, DOMINANT_KERNEL, n_ctx)
+    dom = DOMINANT_KERNEL.get(args.plan, 3)
+    kb = kernel_bytes(w, dom, n_ctx, args.plan)
     peak, peak_kind = measured_peaks()
     if persistent:
         # one kernel per step: its launches are exactly the timed region's steps
@@ -426,13 +438,13 @@ def run_ours(args, w, rank, world, local_rank):
         k_ms = ms / K
         achieved = kb / (k_ms * 1e-3) / 1e9
     elif not unfused:
-        d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)  # warm
+        d.launch_kernel(dom, 0, w.n_layers)  # warm
         reps = 3
         torch.cuda.synchronize()
         tw0 = time.time()
         ev0.record(stream)
         for _ in range(reps):
-            d.launch_kernel(DOMINANT_KERNEL, 0, w.n_layers)
+            d.launch_kernel(dom, 0, w.n_layers)
         ev1.record(stream)
         torch.cuda.synchronize()
         tw1 = time.time()
@@ -443,7 +455,8 @@ def run_ours(args, w, rank, world, local_rank):
     else:
         k_ms, achieved = None, None
     clocks.stop()
-    traffic = profiled_traffic(w.name) if args.plan == "fused" else None
+    kname = ("token_persistent" if persistent else DOMINANT_NAME.get(args.plan, "none"))
+    traffic = profiled_traffic(w.name, kname) if args.plan in DOMINANT_NAME else None
 
     tok_s = replica_tok_s(world, K, ms)
     tok_s_e2e = replica_tok_s(world, K, ms_e2e)
@@ -473,7 +486,7 @@ def run_ours(args, w, rank, world, local_rank):
                 "frac": bpt["total"] * tok_s / world / 1e9 / peak},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak if achieved else None, "traffic": traffic,
-                     "kernel": "token_persistent" if persistent else "norm_gateup_swiglu",
+                     "kernel": kname,
                      "bytes_per_launch": kb,
                      "avg_launch_ms": k_ms, "peak_kind": peak_kind},
         "e2e": {"value": tok_s_e2e, "unit": "tok/s", "h2d_bytes_per_step": 4 * H,

@@ -56,7 +56,9 @@ enum dec_weight_fmt {
 };
 
 enum dec_flags {
-  DEC_PLAN_FUSED = 0,    /* five kernels per layer (default) */
+  DEC_PLAN_FUSED = 0,    /* five kernels per layer (default): norm + QKV + RoPE + KV append;
+                            attention; o-proj + residual; norm + gate/up + SwiGLU;
+                            down + residual */
   DEC_PLAN_UNFUSED = 1,  /* one kernel per op: the ablation / reference chain */
   DEC_NO_GRAPH = 2,      /* launch eagerly instead of replaying a CUDA graph */
   DEC_NO_PDL = 4,        /* fused plan: launch without programmatic dependent launch,
@@ -66,10 +68,19 @@ enum dec_flags {
                               between phases, one weight stream through the step) */
   DEC_NO_L2_AHEAD = 16,    /* fused plan: do not prefetch the next kernel's bytes into L2
                               at the end of each kernel's stream */
-  DEC_ATTN_GLOBAL_MERGE = 32 /* fused plan: attention over a flat grid whose split heads are
-                                merged through global memory by the last CTA of each head,
-                                instead of one thread-block cluster per KV head merging in
-                                distributed shared memory */
+  DEC_ATTN_GLOBAL_MERGE = 32, /* five-kernel plan: attention over a flat grid whose split heads
+                                 are merged through global memory by the last CTA of each head,
+                                 instead of one thread-block cluster per KV head merging in
+                                 distributed shared memory */
+  DEC_PLAN_THREE = 64,        /* fused plan with three kernels per layer: norm + QKV + RoPE +
+                                 KV append; attention + o-proj + residual; norm + gate/up +
+                                 SwiGLU + down + residual (each of the last two one launch of
+                                 two phases separated by a grid barrier) */
+  DEC_DEBUG_GUARDS = 128      /* memory-safety checks that need no sanitizer: every device
+                                 buffer between guard bands of a known pattern, its bytes
+                                 poisoned with 0xFF (NaN as fp32 and bf16) until written, KV
+                                 rows past the KV length kept poisoned; dec_check_guards
+                                 verifies them */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
@@ -116,28 +127,55 @@ typedef struct dec_info {
 
 typedef struct dec_handle dec_handle; /* opaque */
 
-/* Validates the shape and allocates every device buffer (weights, KV cache,
+/* Source: "Vulkan Command Buffer Reuse vs CUDA Graphs: RDNA4 Decode Overhead",
+ * section "Why NVIDIA got a free 14 percent" (build the launch structure once,
+ * reuse it every token); the shapes are those of a Llama-style decoder layer
+ * ("RDNA4 Decode Kernel Fusion", section "Decode is where the bubble has
+ * nowhere to go").
+ * Validates the shape and allocates every device buffer (weights, KV cache,
  * workspaces) on the current CUDA device.  Supported: head_dim 64 or 128,
  * n_q_heads a multiple of n_kv_heads, hidden and ffn multiples of 8 (of 32
  * for DEC_W_Q4B32), 1 <= max_ctx <= 65536.  *out is NULL on failure. */
 int dec_create(const dec_model_desc* desc, dec_handle** out);
 
-/* Copies one tensor of one layer (host or device src, `bytes` long, layout as
+/* Source: the layer's weights as the op chain names them ("RDNA4 Decode Kernel
+ * Fusion", section "Decode is where the bubble has nowhere to go"), in bf16 or
+ * in int4 blocks of 32 with an fp16 scale (the block-quantized workload this
+ * library is measured on).
+ * Copies one tensor of one layer (host or device src, `bytes` long, layout as
  * in enum dec_tensor) into library-owned device memory, repacking it into the
  * kernels' tiled layout.  Blocks until done.  The caller keeps src. */
 int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size_t bytes);
 
-/* Loads the first n_pos cache rows of one layer: k and v are host or device
+/* Source: none on the pages; an addition the measured workloads force (every
+ * one starts from a KV cache prefilled to 127, 1023, 2047 or 4095 positions).
+ * Loads the first n_pos cache rows of one layer: k and v are host or device
  * bf16 [n_kv_heads][n_pos][head_dim] (k already rotated by RoPE at its own
  * position, v raw).  Sets that layer's KV length to n_pos.  Blocks until done
  * and waits for all queued work of the device first. */
 int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16, int n_pos);
 
-/* Rewinds every layer's KV length to n_pos (<= the current length); rows past
+/* Source: none on the pages; an addition the parity check of the KV append
+ * forces (the rows the QKV kernel wrote are compared with the reference chain's).
+ * Copies rows [first_pos, first_pos + n_pos) of one layer's cache into k_bf16
+ * and v_bf16, host or device bf16 [n_kv_heads][n_pos][head_dim] each (the
+ * layout dec_load_kv takes).  Rows past the KV length hold whatever was last
+ * written there.  Waits for all queued work of the device first; blocks until
+ * done. */
+int dec_read_kv(dec_handle* h, int layer, void* k_bf16, void* v_bf16, int first_pos, int n_pos);
+
+/* Source: none on the pages; an addition for repeated measurement from the
+ * same prefilled state.
+ * Rewinds every layer's KV length to n_pos (<= the current length); rows past
  * it are overwritten by later steps.  Waits for the device first. */
 int dec_truncate_kv(dec_handle* h, int n_pos);
 
-/* One decode step, queued on `stream`, returns after enqueue.
+/* Source: "RDNA4 Decode Kernel Fusion", section "Decode is where the bubble
+ * has nowhere to go" (one token through every layer's chain) and "Vulkan
+ * Command Buffer Reuse vs CUDA Graphs", section "Why NVIDIA got a free 14
+ * percent" (the KV length grows by one each token; only it changes between
+ * replays of the captured token).
+ * One decode step, queued on `stream`, returns after enqueue.
  * token_embedding: device fp32 [hidden], the stack's input at this position.
  * out_hidden: device fp32 [hidden], the last layer's output (no final norm,
  * no LM head).  pos must equal the current KV length (strictly sequential);
@@ -147,7 +185,11 @@ int dec_truncate_kv(dec_handle* h, int n_pos);
 int dec_step(dec_handle* h, const float* token_embedding, int pos, float* out_hidden,
              dec_stream_t stream);
 
-/* Debug taps (both may be NULL): per_layer_out, device fp32 [n_layers][hidden],
+/* Source: none on the pages; an addition the per-layer parity check forces
+ * (the hidden state after every layer is compared with the reference chain,
+ * "Backend-Specific Kernel Fusion", section "Where it breaks": define
+ * tolerances and test them).
+ * Debug taps (both may be NULL): per_layer_out, device fp32 [n_layers][hidden],
  * receives every layer's output at each step; qact_tap (DEC_W_Q4B32 only),
  * device int8 [n_layers][4][max(hidden, ffn, n_q_heads*head_dim)], receives
  * the int8 inputs of the q, o, gate and down projections, and qscale_tap,
@@ -155,8 +197,10 @@ int dec_step(dec_handle* h, const float* token_embedding, int pos, float* out_hi
  * discards the captured graph; it is recaptured at the next step. */
 int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qscale_tap);
 
-/* Integer block-dot tap (fused plan, DEC_W_Q4B32): at the next steps, the
- * GEMV of `kernel` (0 = QKV, 2 = o-proj, 3 = gate/up, 4 = down) in `layer`
+/* Source: none on the pages; an addition the bit-exact check of the integer
+ * block dots of the int4/int8 path forces.
+ * Integer block-dot tap (fused plans, DEC_W_Q4B32): at the next steps, the
+ * GEMV `kernel` (0 = QKV, 2 = o-proj, 3 = gate/up, 4 = down) in `layer`
  * writes every int32 block dot sum_{i<32} q_w * q_x into dots, device int32
  * [rows][K/32], rows in the library's tiled order (QKV: q heads then k heads
  * with dims (i, i + head_dim/2) adjacent, then v; gate/up: gate and up rows
@@ -164,12 +208,17 @@ int dec_set_tap(dec_handle* h, float* per_layer_out, int8_t* qact_tap, float* qs
  * bit-exact check of the integer path against the int8 input tap. */
 int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots);
 
-/* GPU timeline probe of the fused plan (NULL turns it off): buf is device
- * uint64 [kernels_per_token][8]; at every step, launch i (layer * 5 + kernel)
- * records, in %globaltimer nanoseconds as atomic min / max: [0] earliest CTA
- * start, [1] latest CTA end, [2] / [3] earliest / latest return from
- * griddepcontrol.wait, [4] latest arrival of a CTA's first stage, [5] / [6]
- * earliest / latest end of a CTA's streaming loop, [7] earliest CTA end.
+/* Source: "RDNA4 Decode Kernel Fusion", section "What I am building next"
+ * (measure with GPU timestamps rather than trusting the model).
+ * GPU timeline probe of the fused plans (NULL turns it off): buf is device
+ * uint64 [n_layers * 5][8], one row per phase of a layer (row layer * 5 + p, p
+ * = 0 QKV, 1 attention, 2 o-proj, 3 gate/up, 4 down, whichever kernel runs
+ * it); at every step each row records, in %globaltimer nanoseconds as atomic
+ * min / max: [0] earliest CTA start (second phase of a two-phase kernel:
+ * earliest arrival at its grid barrier), [1] latest end of the phase, [2] /
+ * [3] earliest / latest return from griddepcontrol.wait (second phase: from
+ * the grid barrier), [4] latest arrival of a CTA's first stage, [5] / [6]
+ * earliest / latest end of a CTA's streaming loop, [7] earliest end.
  * The caller initialises the min slots (0, 2, 5, 7) to UINT64_MAX and the max
  * slots (1, 3, 4, 6) to 0.  With DEC_PLAN_PERSISTENT, row i is phase i of the
  * step (layer * 5 + phase) and records [0] / [1] the earliest / latest return
@@ -179,17 +228,39 @@ int dec_set_dot_tap(dec_handle* h, int layer, int kernel, int32_t* dots);
  * Decode Kernel Fusion", section "What I am building next": GPU timestamps). */
 int dec_set_timeline(dec_handle* h, uint64_t* buf);
 
-/* Waits for `stream` and reports DEC_ERR_DEVICE if any kernel raised its
- * error flag (a bounded wait ran out); the flag is cleared. */
+/* Source: none on the pages; the library's bounded waits report here.
+ * Waits for `stream` and reports DEC_ERR_DEVICE if any kernel raised its
+ * error flag (a bounded wait ran out); the flag is cleared.  With h == NULL it
+ * reports the flag of dec_attention_noalloc on the current device instead
+ * (read and cleared with cudaMemcpyFromSymbol / ToSymbol, which allocate
+ * nothing); its message is then read with dec_last_error(NULL). */
 int dec_sync_status(dec_handle* h, dec_stream_t stream);
 
-/* Fills *info; never fails on a valid handle. */
+/* Source: "Backend-Specific Kernel Fusion", section "Where it breaks" (test
+ * the boundary cases); it stands in for a memory checker where none can run.
+ * Waits for the device, then checks every guard band of a handle created
+ * with DEC_DEBUG_GUARDS and that every KV cache row past the KV length still
+ * holds its poison.  Returns DEC_OK, DEC_ERR_DEVICE (the message names the
+ * buffer and byte, or the layer, head and row), DEC_ERR_STATE (no guards) or
+ * DEC_ERR_CUDA.  Index checks inside the kernels are compiled into the debug
+ * build of the library (TLD_DEBUG_CHECKS): a failed check skips the access,
+ * raises the error flag and is reported by dec_sync_status with its source
+ * line. */
+int dec_check_guards(dec_handle* h);
+
+/* Source: "Backend-Specific Kernel Fusion", section "What you can do this
+ * week" (record dispatch counts alongside latency).
+ * Fills *info; never fails on a valid handle. */
 int dec_get_info(const dec_handle* h, dec_info* info);
 
-/* Launches `count` times the fused plan's kernel `kernel` (0 = norm+QKV+RoPE+
- * append, 1 = attention, 2 = o-proj+residual, 3 = norm+gate/up+SwiGLU,
- * 4 = down+residual) for layers first_layer, first_layer+1, ... (mod
- * n_layers), back to back on `stream`, on the activations the last step left.
+/* Source: none on the pages; an addition for timing one fused kernel against
+ * its bandwidth roofline.
+ * Launches `count` times the fused plan's kernel `kernel` of a layer (three-
+ * kernel plan: 0 = norm+QKV+RoPE+append, 1 = attention+o-proj+residual, 2 =
+ * norm+gate/up+SwiGLU+down+residual; DEC_PLAN_FIVE: 0 = norm+QKV+RoPE+append,
+ * 1 = attention, 2 = o-proj+residual, 3 = norm+gate/up+SwiGLU, 4 =
+ * down+residual) for layers first_layer, first_layer+1, ... (mod n_layers),
+ * back to back on `stream`, on the activations the last step left.
  * For timing one kernel alone; the KV length does not change and the next
  * dec_step overwrites whatever these launches wrote. */
 int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream);
@@ -221,16 +292,22 @@ int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec
  * n_kv_heads in {1, 2, 4, 8}, the records of one call within the array (a
  * call that would exceed it returns DEC_ERR_SHAPE), ctx_stride <= 65536.
  * Returns DEC_ERR_ARG / DEC_ERR_SHAPE for bad arguments (nothing is queued)
- * and DEC_ERR_CUDA if a launch fails. */
+ * and DEC_ERR_CUDA if a launch fails.  The first-call set-up is guarded per
+ * device, so concurrent first calls from several host threads are safe.  A
+ * wait inside the kernel that gives up (a fault elsewhere, never in normal
+ * operation) leaves o partly unwritten and sets the array's error flag; the
+ * next call clears it, so read it first with dec_sync_status(NULL, stream). */
 int dec_attention_noalloc(const float* q, const void* k_cache, const void* v_cache, int n_q_heads,
                           int n_kv_heads, int head_dim, int ctx_stride, int n, float* o,
                           dec_stream_t stream);
 
-/* Frees every device buffer and the graph; accepts NULL and partially
+/* Source: none on the pages (resource lifetime of the C ABI).
+ * Frees every device buffer and the graph; accepts NULL and partially
  * created handles.  Waits for the device first. */
 int dec_destroy(dec_handle* h);
 
-/* Message of the last failed call on h ("" if none); h may be NULL, in which
+/* Source: none on the pages (error reporting of the C ABI).
+ * Message of the last failed call on h ("" if none); h may be NULL, in which
  * case the message of the last failed dec_create of this thread is returned. */
 const char* dec_last_error(const dec_handle* h);
 

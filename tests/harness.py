@@ -93,3 +93,93 @@ def tiled_rows_to_abi(w: synth.Workload, kernel: int):
         t = synth.T_WO if kernel == 2 else synth.T_WDOWN
         out += [(t, r) for r in range(w.shape(t)[0])]
     return out
+
+
+# ---- the int4 / int8 path: integer decisions ---------------------------------
+
+Q4_SLOTS = ("n1 (q/k/v input)", "o (o-proj input)", "n2 (gate/up input)", "a (down input)")
+
+
+def q4_slot_ks(w: synth.Workload) -> tuple[int, int, int, int]:
+    return (w.hidden, w.n_q_heads * w.head_dim, w.hidden, w.ffn)
+
+
+def bf16_flips(z: np.ndarray, gpu_bits: np.ndarray, rel_tol: float = 1e-5):
+    """The GPU's stored bf16 values against the oracle's own rounding of its fp64
+    values z ([heads][d]).  Storage rounding decides a discrete value from
+    floating point; the GPU rounds its fp32 value, whose arithmetic error is
+    absolute (relative to the magnitudes summed, not to the element), so next
+    to a rounding midpoint the two may store neighbouring values, and a value
+    near zero may differ by more than one bf16 step.  Every difference must
+    still be a correct rounding of a value within rel_tol x (the head's RMS)
+    of z: |stored - z| <= half the stored value's bf16 step + rel_tol x RMS.
+    Returns (number of differing elements, largest excess of |stored - z| over
+    its half step, in units of rel_tol x RMS)."""
+    z = np.asarray(z, np.float64)
+    gpu = np.asarray(gpu_bits, np.uint16).reshape(z.shape)
+    own = np.array([orc.bf16_round(float(v)) for v in z.ravel()], np.uint16).reshape(z.shape)
+    diff = own != gpu
+    if not diff.any():
+        return 0, 0.0
+    rms = np.sqrt(np.mean(z * z, axis=-1, keepdims=True)) * np.ones_like(z)
+    vg = (gpu.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    # the bf16 step at the stored value: 2^(exponent - 7)
+    _, e = np.frexp(vg)
+    half_step = np.ldexp(1.0, e - 9)
+    excess = (np.abs(vg - z) - half_step)[diff] / (rel_tol * rms[diff])
+    return int(diff.sum()), float(max(excess.max(), 0.0))
+
+
+def kv_row_flips(st: orc.OracleStack, layer: int, x, pos: int, k_row: np.ndarray,
+                 v_row: np.ndarray):
+    """The GPU's appended KV row (bf16 bits [n_kv][d] each) against the oracle's
+    own storage rounding of this token's k and v, the layer taking the GPU's
+    layer input x; the oracle's cache is left as it is.  Returns (differing
+    elements, largest excess over the tolerance of bf16_flips, elements)."""
+    _, (kz, vz) = st.layer_step(layer, x, pos, kv_given=True, kvz=True)
+    nk, dk = bf16_flips(kz, k_row)
+    nv, dv = bf16_flips(vz, v_row)
+    return nk + nv, max(dk, dv), kz.size + vz.size
+
+
+def q4_code_flips(st: orc.OracleStack, w: synth.Workload, layer: int, x, pos: int,
+                  gpu_codes: np.ndarray, gpu_scales: np.ndarray, k_row: np.ndarray,
+                  v_row: np.ndarray):
+    """The GPU's integer decisions of one layer against the oracle's, one at a
+    time: the int8 codes of the four GEMV inputs and the bf16 KV row.  For
+    slot s the oracle layer takes the GPU's layer input x, the GPU's codes for
+    the slots before s and, from slot 1 on, the GPU's appended KV row (so the
+    vector it quantizes follows the same decisions) and quantizes slot s itself.
+    Where floating point decides an integer the two sides' values differ in
+    their last bits, so a code may differ by one where the value sits next to
+    a rounding boundary; every difference must be such a flip: |diff| = 1 and
+    the oracle's fp32 quotient z/dx within a small distance of a half-integer.
+
+    Returns {"slots": per slot (flips, largest distance of a flip's quotient
+    from the half-integer, K), "kv": (flips, largest excess over the tolerance
+    of bf16_flips (<= 1 passes), elements)}.  Leaves the GPU's KV row in the
+    oracle's cache at pos."""
+    Ks = q4_slot_ks(w)
+    res = {"slots": []}
+    st.kcache[layer, :, pos] = k_row
+    st.vcache[layer, :, pos] = v_row
+    for s, K in enumerate(Ks):
+        given = [(gpu_codes[i, :Ks[i]], gpu_scales[i, :Ks[i] // 32]) if i < s else None
+                 for i in range(4)]
+        out = st.layer_step(layer, x, pos, qgiven=given, zout=True, kv_given=True, kvz=(s == 1))
+        trip = out[1]
+        if s == 1:  # this token's k, v from the GPU's n1 codes, before the storage rounding
+            kz, vz = out[2]
+            nk, dk = bf16_flips(kz, k_row)
+            nv, dv = bf16_flips(vz, v_row)
+            res["kv"] = (nk + nv, max(dk, dv), kz.size + vz.size)
+        own_q, own_d, z = trip[s]
+        diff = gpu_codes[s, :K].astype(np.int32) - own_q.astype(np.int32)
+        idx = np.nonzero(diff)[0]
+        assert np.all(np.abs(diff[idx]) == 1), \
+            f"layer {layer} {Q4_SLOTS[s]}: codes differ by more than one"
+        quot = z[idx].astype(np.float32) / own_d[idx // 32]
+        frac = np.abs(quot.astype(np.float64) - np.trunc(quot.astype(np.float64)))
+        dist = float(np.max(np.abs(frac - 0.5))) if idx.size else 0.0
+        res["slots"].append((int(idx.size), dist, K))
+    return res

@@ -15,11 +15,11 @@ if not torch.cuda.is_available():
 
 
 def _check(w, steps, *, unfused=False, graph=True, persistent=False, cluster_attn=True,
-           max_ctx=None):
+           three=False, max_ctx=None):
     max_ctx = max_ctx or w.prefill + steps + 2
     d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=unfused, graph=graph,
                                     persistent=persistent, cluster_attn=cluster_attn,
-                                    keep_host=True)
+                                    three=three, keep_host=True)
     xs = workload.step_inputs(w, steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -49,21 +49,29 @@ SMALL = {
 }
 
 
+MODES = {
+    "fused_graph": {},                                   # five kernels, cluster attention
+    "fused_eager": {"graph": False},
+    "global_merge": {"cluster_attn": False},
+    "three": {"three": True},                            # three kernels per layer
+    "three_eager": {"three": True, "graph": False},
+    "unfused": {"unfused": True},
+    "persistent": {"persistent": True},
+}
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "global_merge", "unfused",
-                                  "persistent"])
+@pytest.mark.parametrize("mode", sorted(MODES))
 def test_small_shapes(name, mode):
-    _check(SMALL[name], SMALL[name].steps, unfused=(mode == "unfused"),
-           graph=(mode != "fused_eager"), persistent=(mode == "persistent"),
-           cluster_attn=(mode != "global_merge"))
+    _check(SMALL[name], SMALL[name].steps, **MODES[mode])
 
 
-@pytest.mark.parametrize("persistent", [False, True])
-def test_stack16_h2048_all_steps(persistent):
+@pytest.mark.parametrize("mode", ["fused_graph", "three", "persistent"])
+def test_stack16_h2048_all_steps(mode):
     """16-layer 1B-shape stack, 64 steps from pos 1023, every layer at every step."""
     w = synth.WORKLOADS["stack16_h2048"]
-    _, worst = _check(w, w.steps, persistent=persistent)
-    print("stack16 worst max|err| %.3e rel-L2 %.3e" % worst)
+    _, worst = _check(w, w.steps, **MODES[mode])
+    print("stack16 (%s) worst max|err| %.3e rel-L2 %.3e" % ((mode,) + worst))
 
 
 def test_plans_agree_and_are_deterministic():
@@ -71,7 +79,9 @@ def test_plans_agree_and_are_deterministic():
     xs = workload.step_inputs(w, 3)
     outs = {}
     for key, kw in {"graph": {}, "graph2": {}, "eager": {"graph": False},
-                    "global_merge": {"cluster_attn": False}, "no_l2_ahead": {"l2_ahead": False},
+                    "no_l2_ahead": {"l2_ahead": False}, "no_pdl": {"pdl": False},
+                    "global_merge": {"cluster_attn": False},
+                    "three": {"three": True}, "three_eager": {"three": True, "graph": False},
                     "persistent": {"persistent": True},
                     "persistent_eager": {"persistent": True, "graph": False},
                     "unfused": {"unfused": True}}.items():
@@ -81,12 +91,16 @@ def test_plans_agree_and_are_deterministic():
     assert np.array_equal(outs["graph"], outs["graph2"]), "fused plan not run-to-run identical"
     assert np.array_equal(outs["graph"], outs["eager"]), "graph replay differs from eager launch"
     assert np.array_equal(outs["graph"], outs["no_l2_ahead"]), "the L2 look-ahead changed results"
-    # the persistent plan shares the global-merge attention
-    assert np.array_equal(outs["global_merge"], outs["persistent"]), "persistent differs from fused"
+    assert np.array_equal(outs["graph"], outs["no_pdl"]), "dependent launch changed results"
+    assert np.array_equal(outs["three"], outs["three_eager"])
+    # the three-kernel plan, the five-kernel plan with global-merge attention and
+    # the persistent plan run the same split and the same per-phase arithmetic
+    assert np.array_equal(outs["three"], outs["global_merge"]), "three vs five kernels differ"
+    assert np.array_equal(outs["three"], outs["persistent"]), "persistent differs from fused"
     assert np.array_equal(outs["persistent"], outs["persistent_eager"])
     for s in range(3):
         for l in range(w.n_layers):
-            assert_close(outs["graph"][s, l], outs["global_merge"][s, l], f"cluster vs global {s},{l}")
+            assert_close(outs["graph"][s, l], outs["three"][s, l], f"cluster vs global {s},{l}")
     for s in range(3):
         for l in range(w.n_layers):
             assert_close(outs["graph"][s, l], outs["unfused"][s, l], f"fused vs unfused {s},{l}")
@@ -111,15 +125,15 @@ def test_residual_wiring_zero_projections():
             assert np.array_equal(got[s, l], xs[s])
 
 
-@pytest.mark.parametrize("persistent", [False, True])
-def test_io_pointers_can_change_between_steps(persistent):
+@pytest.mark.parametrize("mode", ["fused_graph", "three", "persistent"])
+def test_io_pointers_can_change_between_steps(mode):
     """The captured graph is re-pointed when the caller passes new buffers."""
     w = SMALL["ragged_g2_empty"]
     xs = workload.step_inputs(w, 3)
-    d_ref, _ = workload.make_decoder(w, max_ctx=16, graph=False)
+    d_ref, _ = workload.make_decoder(w, max_ctx=16, **{**MODES[mode], "graph": False})
     ref = run_gpu(d_ref, w, xs, taps=False)
     d_ref.close()
-    d, _ = workload.make_decoder(w, max_ctx=16, persistent=persistent)
+    d, _ = workload.make_decoder(w, max_ctx=16, **MODES[mode])
     outs = []
     for s in range(3):
         emb = torch.from_numpy(xs[s]).cuda()          # a fresh buffer every step

@@ -64,7 +64,7 @@ def _create(lib, **kw):
     ({"max_ctx": 70000}, dec.DEC_ERR_SHAPE),
     ({"n_layers": 0}, dec.DEC_ERR_ARG),
     ({"weight_fmt": 7}, dec.DEC_ERR_ARG),
-    ({"flags": 64}, dec.DEC_ERR_ARG),
+    ({"flags": 256}, dec.DEC_ERR_ARG),
     ({"rope_theta": 0.0}, dec.DEC_ERR_ARG),
 ])
 def test_create_rejects_bad_descs_on_the_host(lib, kw, code):
@@ -85,13 +85,8 @@ def test_null_arguments_are_errors(lib):
 
 def test_missing_library_fails_loudly(tmp_path):
     """A loader pointed at a missing library raises instead of falling back."""
-    saved = dec._lib
-    dec._lib = None
-    try:
-        with pytest.raises(RuntimeError, match="not built"):
-            dec.load_library(str(tmp_path / "nope.so"))
-    finally:
-        dec._lib = saved
+    with pytest.raises(RuntimeError, match="not built"):
+        dec.load_library(str(tmp_path / "nope.so"))
 
 
 def test_quantizer_rounding_matches_ieee_division(tmp_path):

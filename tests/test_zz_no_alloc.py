@@ -1,10 +1,12 @@
-"""dec_attention_noalloc against the decoder's own attention, through the C ABI.
+"""dec_attention_noalloc against the decoder's own attention and against the
+fp64 oracle, through the C ABI.
 
 Some callers cannot call cudaMalloc (their device memory belongs to another
 allocator, or they run under a no-allocation rule after start-up), so the
 library offers the decode attention kernel with its scratch in a fixed device
-array.  This test checks that entry point's output against the attention that
-dec_step computes, on two calls in a row.
+array.  These tests check that entry point's output against the attention that
+dec_step computes and against the oracle's attention, on two calls in a row,
+and that calls whose partial records would not fit the array are refused.
 
 The decoder's attention output is made observable through dec_step: one layer
 with Wq = I, Wk = Wv = 0, Wo = I, Wdown = 0 and unit norm weights gives
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 
 from harness import assert_close
+from oracle import oracle as orc
 from transformer_layer_decode_gb300 import dec
 
 pytestmark = pytest.mark.gpu
@@ -102,3 +105,47 @@ def test_noalloc_rejects_sizes_beyond_its_limits():
     with pytest.raises(dec.DecError) as e:
         dec.attention_noalloc(q, kv, kv, 8, 128, 64, 100, 10, o)    # > 64 KV heads
     assert e.value.code == dec.DEC_ERR_SHAPE
+
+
+@pytest.mark.parametrize("nq,nkv,hd,n", [(32, 4, 128, 777), (8, 4, 64, 300), (16, 16, 128, 129)])
+def test_noalloc_attention_matches_oracle(nq, nkv, hd, n):
+    """GQA 8 at head_dim 128, GQA 2 at 64 and MHA at 128 against the oracle's
+    attention head by head, two calls in a row (the second one longer)."""
+    rng = np.random.default_rng(nq * 1000 + hd)
+    ctx = n + 8
+    kc = _bf16(rng.normal(0, 1, (nkv, ctx, hd)))
+    vc = _bf16(rng.normal(0, 1, (nkv, ctx, hd)))
+    kc_dev = torch.from_numpy(kc.view(np.int16)).cuda()
+    vc_dev = torch.from_numpy(vc.view(np.int16)).cuda()
+    o_dev = torch.empty(nq * hd, device="cuda")
+    for call, length in enumerate((n, n + 5)):
+        q = rng.normal(0, 1, (nq, hd)).astype(np.float32)
+        o_dev.fill_(float("nan"))
+        dec.attention_noalloc(torch.from_numpy(q.ravel()).cuda(), kc_dev, vc_dev, nq, nkv, hd,
+                              ctx, length, o_dev)
+        dec.noalloc_sync_status()
+        got = o_dev.cpu().numpy().reshape(nq, hd)
+        for h in range(nq):
+            g = orc.kv_head_of(h, nq, nkv)
+            ref = orc.attention_head(q[h].astype(np.float64), kc[g, :length], vc[g, :length])
+            assert_close(got[h], ref, f"no-alloc vs oracle, {nq}/{nkv} hd {hd}, call {call + 1} head {h}",
+                         max_abs=1e-4, rel_l2=1e-5)
+
+
+def test_noalloc_refuses_records_beyond_its_array():
+    """64 q / 8 KV heads at head_dim 128: the split records of one call need
+    grid * 2 * 8 * 132 floats, more than the 2^18 the array holds on a GPU with
+    more than 124 SMs; the call is refused with DEC_ERR_SHAPE and queues nothing."""
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    grid = min(n_sm, 31 * 8)
+    if grid * 2 * 8 * 132 <= 1 << 18:
+        pytest.skip("this GPU's grid fits the records")
+    q = torch.zeros(64 * 128, device="cuda")
+    kv = torch.zeros(8 * 64 * 128, dtype=torch.int16, device="cuda")
+    o = torch.full_like(q, 7.0)
+    with pytest.raises(dec.DecError) as e:
+        dec.attention_noalloc(q, kv, kv, 64, 8, 128, 64, 10, o)
+    assert e.value.code == dec.DEC_ERR_SHAPE
+    torch.cuda.synchronize()
+    assert torch.all(o == 7.0)                 # nothing ran
+    dec.noalloc_sync_status()

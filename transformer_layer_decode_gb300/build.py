@@ -11,6 +11,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtld_gb300.so")
+# debug build: the kernels' index checks compiled in (TLD_DEBUG_CHECKS)
+DEBUG_LIB = os.path.join(BUILD, "libtld_gb300_debug.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -34,23 +36,29 @@ def _deps() -> list[str]:
     return sources() + extra + [os.path.join(INCLUDE, "dec.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    """Compile every .cu in csrc/ in parallel and link the shared library."""
-    if not force and not ptxas_info and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Compile every .cu in csrc/ in parallel and link the shared library (with
+    debug=True: the debug build, index checks compiled in, in its own objects)."""
+    lib = DEBUG_LIB if debug else LIB
+    if not force and not ptxas_info and up_to_date(lib):
+        return lib
+    objdir = os.path.join(BUILD, "debug") if debug else BUILD
+    os.makedirs(objdir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra.append("-DTLD_DEBUG_CHECKS")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *CFLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -61,13 +69,14 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -20,7 +20,8 @@ enum ErrBits : int {
   ERR_EMPTY_WAIT = 2,
   ERR_DRAIN = 4,
   ERR_SPLITS = 8,
-  ERR_GRID_WAIT = 16
+  ERR_GRID_WAIT = 16,
+  ERR_BOUNDS = 32  // debug builds: an index check failed; err[1] holds the source line
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -203,6 +204,76 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ void raise_error(int* flag, int bits) {
   if (flag) atomicOr(flag, bits);
+}
+
+// Index checks of the debug build (TLD_DEBUG_CHECKS): a failed check raises
+// ERR_BOUNDS, keeps the first failing source line in err[1] and returns false,
+// and the caller skips the access.  Release builds compile every check to true.
+__device__ __noinline__ inline bool bounds_failed(int* err, int line) {
+  if (err) {
+    atomicOr(err, ERR_BOUNDS);
+    atomicCAS(err + 1, 0, line);
+  }
+  return false;
+}
+#ifdef TLD_DEBUG_CHECKS
+#define TLD_IN_BOUNDS(cond, err) ((cond) ? true : ::tld::bounds_failed((err), __LINE__))
+#else
+#define TLD_IN_BOUNDS(cond, err) true
+#endif
+
+// ---- grid-wide synchronisation inside one launch ---------------------------------
+// Only for launches whose CTAs are all resident at once (one CTA per SM, grid no
+// larger than the SM count): every wait is bounded in wall time and by the error
+// flag, so a CTA that never arrives costs a timeout and an error flag, not a hang.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Makes generic-proxy writes visible to later bulk copies (async proxy) of this thread.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Spins until *ctr >= target (bounded by wall time and by the error flag).
+__device__ __forceinline__ bool spin_until(const int* ctr, int target, int* err) {
+  if (ld_acquire_gpu(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ld_acquire_gpu(ctr) >= target) return true;
+    if ((i & 63) == 0) {
+      if (*reinterpret_cast<volatile int*>(err)) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        raise_error(err, ERR_GRID_WAIT);
+        return false;
+      }
+    }
+  }
+}
+
+// Grid barrier of the consumer threads (nthreads of each CTA, named barrier
+// `bar_id`): every CTA adds one to *ctr once its consumers are done with the
+// phase; all wait until the count reaches `target`.  The named barrier orders
+// every consumer thread's writes before thread 0's release; thread 0's acquire
+// orders the other CTAs' writes before every thread's reads after the second
+// named barrier.
+__device__ __forceinline__ void grid_sync(int* ctr, int target, int* err, int tid, int bar_id,
+                                          int nthreads, uint64_t* tl = nullptr) {
+  named_barrier(bar_id, nthreads);
+  if (tid == 0) {
+    tl_mark_min(tl, 0);
+    red_release_gpu_add(ctr, 1);
+    spin_until(ctr, target, err);
+    tl_mark_min(tl, 2);
+    tl_mark_max(tl, 3);
+  }
+  named_barrier(bar_id, nthreads);
 }
 
 }  // namespace tld

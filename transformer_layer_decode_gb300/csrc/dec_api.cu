@@ -50,8 +50,22 @@ struct dec_handle {
   int n_sm = 0, G = 0;
   bool fused = true, graph = true, pdl = true, persistent = false, l2_ahead = true;
   bool cluster_attn = true;
+  bool three = false;  // fused plan: three kernels per layer (else five)
+  // three-kernel plan: barrier counters [n_layers][2 launch sites][2 parities],
+  // and the ring / shared memory of the two-phase kernels
+  int* d_fbar = nullptr;
+  int ao_nstages = 0, ao_slot = 0, ffn_nstages = 0, ffn_slot = 0;
+  size_t ao_smem = 0, ffn_smem = 0;
   std::vector<LayerDev> layers;
   std::vector<void*> allocs;
+  // DEC_DEBUG_GUARDS: every allocation sits between guard bands of a known
+  // byte pattern, checked by dec_check_guards
+  bool guards = false;
+  struct Guard {
+    uint8_t* user;  // start of the caller-visible bytes
+    size_t bytes;
+  };
+  std::vector<Guard> guard_list;
   // activations / workspace
   float *X = nullptr, *h1 = nullptr, *q = nullptr, *o = nullptr, *a = nullptr;
   float *n1 = nullptr, *k = nullptr, *v = nullptr, *g = nullptr, *u = nullptr, *y = nullptr;
@@ -115,16 +129,33 @@ int cuda_fail(dec_handle* h, cudaError_t e, const char* what) {
     if (e_ != cudaSuccess) return cuda_fail((h), e_, #call); \
   } while (0)
 
+constexpr size_t kGuardBytes = 256;      // guard band on each side (keeps 256-byte alignment)
+constexpr uint8_t kGuardPattern = 0xA5;
+
 template <class T>
 int dev_alloc(dec_handle* h, T** p, size_t bytes, int64_t* account) {
   void* v = nullptr;
-  cudaError_t e = cudaMalloc(&v, bytes < 16 ? 16 : bytes);
+  const size_t user = bytes < 16 ? 16 : bytes;
+  const size_t total = h->guards ? user + 2 * kGuardBytes + 255 : user;
+  cudaError_t e = cudaMalloc(&v, total);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return fail(h, DEC_ERR_OOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
   }
   h->allocs.push_back(v);
   if (account) *account += (int64_t)bytes;
+  if (h->guards) {
+    // [guard | user bytes | pattern up to the next 256 and a guard]; the user
+    // bytes start poisoned (0xFF: NaN as fp32 and as bf16) so that a read of
+    // a byte nothing wrote shows up in the results
+    uint8_t* base = static_cast<uint8_t*>(v);
+    e = cudaMemset(base, kGuardPattern, total);
+    if (e == cudaSuccess) e = cudaMemset(base + kGuardBytes, 0xFF, user);
+    if (e != cudaSuccess) return cuda_fail(h, e, "guard bands");
+    h->guard_list.push_back({base + kGuardBytes, user});
+    *p = reinterpret_cast<T*>(base + kGuardBytes);
+    return DEC_OK;
+  }
   *p = static_cast<T*>(v);
   return DEC_OK;
 }
@@ -340,12 +371,55 @@ GemvParams fused_gemv_params(const dec_handle* h, int kernel, int l, const float
   return p;
 }
 
+AttnOprojParams ao_params(const dec_handle* h, int l, const float* emb, float* out, bool in_step) {
+  AttnOprojParams p{};
+  p.attn = k2_params(h, l);
+  p.attn.tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 1) : nullptr;
+  p.o = fused_gemv_params(h, 2, l, emb, out, in_step);
+  p.tl2 = p.o.tl;
+  p.bar = h->d_fbar + (size_t)l * 4;
+  p.att_grid = h->att_grid;
+  p.nstages = h->ao_nstages;
+  p.slot_bytes = h->ao_slot;
+  return p;
+}
+
+FfnParams ffn_params(const dec_handle* h, int l, const float* emb, float* out, bool in_step) {
+  FfnParams p{};
+  p.gu = fused_gemv_params(h, 3, l, emb, out, in_step);
+  p.down = fused_gemv_params(h, 4, l, emb, out, in_step);
+  p.tl2 = p.down.tl;
+  p.bar = h->d_fbar + (size_t)l * 4 + 2;
+  p.nstages = h->ffn_nstages;
+  p.slot_bytes = h->ffn_slot;
+  return p;
+}
+
 int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, float* out,
                          bool in_step, cudaStream_t s) {
   const int nb = h->n_sm;
   const LayerDev& L = h->layers[l];
   const bool q4 = h->d.weight_fmt == DEC_W_Q4B32;
   cudaError_t e = cudaSuccess;
+  if (h->three) {
+    switch (kernel) {
+      case 0:
+        e = launch_gemv(PRO_NORM, EPI_QKV, q4, fused_gemv_params(h, 0, l, emb, out, in_step), nb,
+                        L.qkv.smem, s, h->pdl);
+        break;
+      case 1:
+        e = launch_attn_oproj(h->d.head_dim, h->G, q4, ao_params(h, l, emb, out, in_step), nb,
+                              h->ao_smem, s, h->pdl);
+        break;
+      case 2:
+        e = launch_ffn(q4, ffn_params(h, l, emb, out, in_step), nb, h->ffn_smem, s, h->pdl);
+        break;
+      default:
+        return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
+    }
+    if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+    return DEC_OK;
+  }
   switch (kernel) {
     case 0:
       e = launch_gemv(PRO_NORM, EPI_QKV, q4, fused_gemv_params(h, 0, l, emb, out, in_step), nb,
@@ -483,12 +557,13 @@ int enqueue_step(dec_handle* h, const float* emb, float* out, cudaStream_t s, bo
     }
     return DEC_OK;
   }
+  const int kpl = h->three ? 3 : 5;
   for (int l = 0; l < Lc; ++l) {
-    for (int k = 0; k < 5; ++k) {
+    for (int k = 0; k < kpl; ++k) {
       int rc = enqueue_fused_kernel(h, k, l, emb, out, true, s);
       if (rc) return rc;
       if (capturing && l == 0 && k == 0) h->first_node = last_captured_node(s);
-      if (capturing && l == Lc - 1 && k == 4) h->last_node = last_captured_node(s);
+      if (capturing && l == Lc - 1 && k == kpl - 1) h->last_node = last_captured_node(s);
     }
   }
   return DEC_OK;
@@ -547,6 +622,19 @@ int patch_io(dec_handle* h, const float* emb, float* out) {
     TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->first_node, &kp));
     h->cap_emb = emb;
   }
+  if (out != h->cap_out && h->three) {
+    const int l = h->d.n_layers - 1;
+    FfnParams p = ffn_params(h, l, emb, out, true);
+    void* args[] = {&p};
+    cudaKernelNodeParams kp{};
+    kp.func = const_cast<void*>(ffn_kernel_ptr(h->d.weight_fmt == DEC_W_Q4B32));
+    kp.gridDim = dim3(h->n_sm);
+    kp.blockDim = dim3(kThreads);
+    kp.sharedMemBytes = (unsigned)h->ffn_smem;
+    kp.kernelParams = args;
+    TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->last_node, &kp));
+    h->cap_out = out;
+  }
   if (out != h->cap_out) {
     const int l = h->d.n_layers - 1;
     GemvParams p = fused_gemv_params(h, 4, l, emb, out, true);
@@ -568,6 +656,7 @@ int set_device_pos(dec_handle* h, int pos) {
   // the persistent kernel's barrier counters alternate by position parity:
   // after a jump of the position both start from zero
   if (h->d_bar) TLD_CUDA(h, cudaMemset(h->d_bar, 0, 2 * sizeof(int)));
+  if (h->d_fbar) TLD_CUDA(h, cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)h->d.n_layers));
   return DEC_OK;
 }
 
@@ -601,7 +690,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64))
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
-                  DEC_ATTN_GLOBAL_MERGE))
+                  DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -614,6 +703,9 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->l2_ahead = !(d.flags & DEC_NO_L2_AHEAD);
   h->cluster_attn = !(d.flags & DEC_ATTN_GLOBAL_MERGE);
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
+  h->three = h->fused && !h->persistent && (d.flags & DEC_PLAN_THREE);
+  h->guards = (d.flags & DEC_DEBUG_GUARDS) != 0;
+  if (h->three) h->cluster_attn = false;  // its attention phase is a flat grid
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
@@ -678,6 +770,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     A(&h->d_players, sizeof(PLayer) * (size_t)d.n_layers, &h->ws_bytes);
     A(&h->d_bar, 16, &h->ws_bytes);
   }
+  if (h->three) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
   A(&h->rope, sizeof(float2) * (size_t)d.max_ctx * (hd / 2), &h->ws_bytes);
@@ -700,6 +793,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       }
     e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
+  if (e == cudaSuccess && h->three) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
   if (e == cudaSuccess && h->persistent) {
     std::vector<PLayer> pl(d.n_layers);
     for (int l = 0; l < d.n_layers; ++l) {
@@ -720,6 +814,27 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / kAttnStageBytes);
     h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages, cl);
+  }
+  if (h->three) {
+    // ring slots hold an attention chunk or a GEMV stage; as many as the budget
+    // leaves next to the larger of the two phases' work areas
+    const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+    const int gstage = q4 ? kStageBytesQ4 : kStageBytes;
+    const LayerDev& L0 = h->layers[0];
+    auto stages = [](size_t fixed, int slot) {
+      int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / (slot + 16));
+      return ns < 2 ? 2 : (ns > 8 ? 8 : ns);
+    };
+    h->ao_slot = gstage > kAttnStageBytes ? gstage : kAttnStageBytes;
+    h->ao_nstages = stages(attn_oproj_smem_bytes(hd, G, nq * hd, L0.o.max_rb_local, q4, 0, 0),
+                           h->ao_slot);
+    h->ao_smem = attn_oproj_smem_bytes(hd, G, nq * hd, L0.o.max_rb_local, q4, h->ao_nstages,
+                                       h->ao_slot);
+    h->ffn_slot = gstage;
+    h->ffn_nstages = stages(ffn_smem_bytes(H, L0.gu.max_rb_local, F, L0.down.max_rb_local, q4, 0, 0),
+                            h->ffn_slot);
+    h->ffn_smem = ffn_smem_bytes(H, L0.gu.max_rb_local, F, L0.down.max_rb_local, q4,
+                                 h->ffn_nstages, h->ffn_slot);
   }
   if (h->fused && !h->persistent && h->cluster_attn) {
     // one cluster per KV head, as many CTAs per head as the SMs allow with every
@@ -805,9 +920,13 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
   }
   if (h->staging_bytes < want) {
     if (h->staging) {
-      cudaFree(h->staging);
+      uint8_t* user = reinterpret_cast<uint8_t*>(h->staging);
+      void* base = h->guards ? user - kGuardBytes : user;
+      cudaFree(base);
       for (auto& p : h->allocs)
-        if (p == h->staging) p = nullptr;
+        if (p == base) p = nullptr;
+      for (auto& g : h->guard_list)
+        if (g.user == user) g.bytes = 0;  // gone: nothing to check
     }
     h->staging = nullptr;
     h->staging_bytes = 0;
@@ -857,9 +976,33 @@ int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16
     TLD_CUDA(h, cudaMemcpy2D(L.kc, pitch, k_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
     TLD_CUDA(h, cudaMemcpy2D(L.vc, pitch, v_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
   }
+  if (h->guards && n_pos < d.max_ctx) {  // rows past the new length hold poison again
+    const size_t pitch = 2 * (size_t)d.max_ctx * d.head_dim, row = 2 * (size_t)d.head_dim;
+    for (uint16_t* c : {L.kc, L.vc})
+      TLD_CUDA(h, cudaMemset2D(c + (size_t)n_pos * d.head_dim, pitch, 0xFF,
+                               row * (d.max_ctx - n_pos), d.n_kv_heads));
+  }
   L.kv_len = n_pos;
   h->kv_len = n_pos;
   return set_device_pos(h, n_pos);
+}
+
+int dec_read_kv(dec_handle* h, int layer, void* k_bf16, void* v_bf16, int first_pos, int n_pos) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  const dec_model_desc& d = h->d;
+  if (layer < 0 || layer >= d.n_layers) return fail(h, DEC_ERR_ARG, "layer %d out of range", layer);
+  if (first_pos < 0 || n_pos < 0 || first_pos + n_pos > d.max_ctx)
+    return fail(h, DEC_ERR_ARG, "rows [%d, %d) outside the cache (max_ctx %d)", first_pos,
+                first_pos + n_pos, d.max_ctx);
+  if (n_pos > 0 && (!k_bf16 || !v_bf16)) return fail(h, DEC_ERR_ARG, "k or v is NULL");
+  TLD_CUDA(h, cudaDeviceSynchronize());
+  if (n_pos == 0) return DEC_OK;
+  const LayerDev& L = h->layers[layer];
+  const size_t row = 2 * (size_t)n_pos * d.head_dim, pitch = 2 * (size_t)d.max_ctx * d.head_dim;
+  const size_t off = (size_t)first_pos * d.head_dim;
+  TLD_CUDA(h, cudaMemcpy2D(k_bf16, row, L.kc + off, pitch, row, d.n_kv_heads, cudaMemcpyDefault));
+  TLD_CUDA(h, cudaMemcpy2D(v_bf16, row, L.vc + off, pitch, row, d.n_kv_heads, cudaMemcpyDefault));
+  return DEC_OK;
 }
 
 int dec_truncate_kv(dec_handle* h, int n_pos) {
@@ -868,7 +1011,16 @@ int dec_truncate_kv(dec_handle* h, int n_pos) {
     if (n_pos < 0 || n_pos > L.kv_len)
       return fail(h, DEC_ERR_POS, "truncate to %d beyond a layer's KV length %d", n_pos, L.kv_len);
   TLD_CUDA(h, cudaDeviceSynchronize());
-  for (LayerDev& L : h->layers) L.kv_len = n_pos;
+  const dec_model_desc& d = h->d;
+  for (LayerDev& L : h->layers) {
+    if (h->guards && n_pos < d.max_ctx) {  // rows past the new length hold poison again
+      const size_t pitch = 2 * (size_t)d.max_ctx * d.head_dim, row = 2 * (size_t)d.head_dim;
+      for (uint16_t* c : {L.kc, L.vc})
+        TLD_CUDA(h, cudaMemset2D(c + (size_t)n_pos * d.head_dim, pitch, 0xFF,
+                                 row * (d.max_ctx - n_pos), d.n_kv_heads));
+    }
+    L.kv_len = n_pos;
+  }
   h->kv_len = n_pos;
   return set_device_pos(h, n_pos);
 }
@@ -937,20 +1089,75 @@ int dec_set_timeline(dec_handle* h, uint64_t* buf) {
 }
 
 int dec_sync_status(dec_handle* h, dec_stream_t stream) {
-  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!h) {  // the no-alloc attention's flag (it has no handle)
+    int flag = 0;
+    const int rc = noalloc_sync_status(reinterpret_cast<cudaStream_t>(stream), &flag);
+    if (rc == DEC_ERR_DEVICE)
+      return fail(nullptr, rc, "dec_attention_noalloc gave up a bounded wait (flags 0x%x)", flag);
+    if (rc != DEC_OK) return fail(nullptr, rc, "reading the no-alloc attention's error flag failed");
+    return DEC_OK;
+  }
   TLD_CUDA(h, cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
   int flag = 0;
   TLD_CUDA(h, cudaMemcpy(&flag, h->d_err, sizeof(int), cudaMemcpyDeviceToHost));
   if (flag) {
-    TLD_CUDA(h, cudaMemset(h->d_err, 0, sizeof(int)));
+    int line = 0;
+    TLD_CUDA(h, cudaMemcpy(&line, h->d_err + 1, sizeof(int), cudaMemcpyDeviceToHost));
+    TLD_CUDA(h, cudaMemset(h->d_err, 0, 2 * sizeof(int)));
+    if (flag & ERR_BOUNDS)
+      return fail(h, DEC_ERR_DEVICE, "an index check failed (flags 0x%x, source line %d)", flag, line);
     return fail(h, DEC_ERR_DEVICE, "a kernel gave up a bounded wait (flags 0x%x)", flag);
+  }
+  return DEC_OK;
+}
+
+int dec_check_guards(dec_handle* h) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!h->guards) return fail(h, DEC_ERR_STATE, "the handle was created without DEC_DEBUG_GUARDS");
+  TLD_CUDA(h, cudaDeviceSynchronize());
+  std::vector<uint8_t> buf;
+  for (size_t i = 0; i < h->guard_list.size(); ++i) {
+    const auto& g = h->guard_list[i];
+    if (g.bytes == 0) continue;
+    // the band before, and the pattern from the end of the user bytes to the
+    // end of the band after
+    const size_t after = ((g.bytes + 255) & ~(size_t)255) - g.bytes + kGuardBytes;
+    for (int side = 0; side < 2; ++side) {
+      const size_t n = side ? after : kGuardBytes;
+      const uint8_t* src = side ? g.user + g.bytes : g.user - kGuardBytes;
+      buf.resize(n);
+      TLD_CUDA(h, cudaMemcpy(buf.data(), src, n, cudaMemcpyDeviceToHost));
+      for (size_t j = 0; j < n; ++j)
+        if (buf[j] != kGuardPattern)
+          return fail(h, DEC_ERR_DEVICE, "guard band %s allocation %zu (%zu bytes) overwritten at byte %zd",
+                      side ? "after" : "before", i, g.bytes,
+                      side ? (ssize_t)j : (ssize_t)j - (ssize_t)kGuardBytes);
+    }
+  }
+  // every cache row past the KV length still holds the poison it was created with
+  const dec_model_desc& d = h->d;
+  const size_t row = 2 * (size_t)d.head_dim;
+  for (int l = 0; l < d.n_layers; ++l) {
+    const LayerDev& L = h->layers[l];
+    const int n = d.max_ctx - L.kv_len;
+    if (n <= 0) continue;
+    buf.resize(row * n);
+    for (const uint16_t* c : {L.kc, L.vc})
+      for (int g = 0; g < d.n_kv_heads; ++g) {
+        TLD_CUDA(h, cudaMemcpy(buf.data(), c + ((size_t)g * d.max_ctx + L.kv_len) * d.head_dim,
+                               row * n, cudaMemcpyDeviceToHost));
+        for (size_t j = 0; j < buf.size(); ++j)
+          if (buf[j] != 0xFF)
+            return fail(h, DEC_ERR_DEVICE, "layer %d KV head %d: row %d past the KV length %d written",
+                        l, g, L.kv_len + (int)(j / row), L.kv_len);
+      }
   }
   return DEC_OK;
 }
 
 int dec_get_info(const dec_handle* h, dec_info* info) {
   if (!h || !info) return DEC_ERR_ARG;
-  info->kernels_per_layer = h->persistent ? 1 : h->fused ? 5
+  info->kernels_per_layer = h->persistent ? 1 : h->three ? 3 : h->fused ? 5
                             : h->d.weight_fmt == DEC_W_Q4B32 ? kUnfusedKernelsPerLayerQ4
                                                              : kUnfusedKernelsPerLayer;
   info->kernels_per_token = h->persistent ? 1 : info->kernels_per_layer * h->d.n_layers;
@@ -967,8 +1174,9 @@ int dec_get_info(const dec_handle* h, dec_info* info) {
 int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream) {
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
   if (!h->fused || h->persistent)
-    return fail(h, DEC_ERR_STATE, "single-kernel launches need the five-kernel fused plan");
-  if (kernel < 0 || kernel > 4 || count < 0 || first_layer < 0 || first_layer >= h->d.n_layers)
+    return fail(h, DEC_ERR_STATE, "single-kernel launches need a fused plan of several kernels");
+  if (kernel < 0 || kernel >= (h->three ? 3 : 5) || count < 0 || first_layer < 0 ||
+      first_layer >= h->d.n_layers)
     return fail(h, DEC_ERR_ARG, "bad kernel / layer / count");
   const uint32_t need = required_mask(h->d);
   for (const LayerDev& L : h->layers)

@@ -176,6 +176,40 @@ struct AttnParams {
   int cluster;   // > 0: grid = nkv clusters of this many CTAs, merged in shared memory
 };
 
+// ---- two-phase kernels of the three-kernel layer ------------------------------
+// One launch runs two phases separated by a grid barrier; the producer streams
+// the second phase's bytes right after the first's, so HBM keeps streaming
+// while the consumers finish the first phase and wait at the barrier.  Every
+// CTA is resident (one CTA per SM, grid = SM count).  Barrier counters: two per
+// launch site, alternating by the parity of the step position (the other one
+// is cleared for the next step).
+struct AttnOprojParams {  // attention (flat grid, global merge), then o-proj + residual
+  AttnParams attn;
+  GemvParams o;
+  int* bar;               // [2] barrier counters of this launch site
+  int att_grid;           // CTAs taking part in the attention phase (<= grid)
+  int nstages, slot_bytes;
+  uint64_t* tl2;          // timeline row of the o-proj phase or null
+};
+
+struct FfnParams {  // norm + gate/up + SwiGLU, then down + residual
+  GemvParams gu, down;
+  int* bar;
+  int nstages, slot_bytes;
+  uint64_t* tl2;          // timeline row of the down phase or null
+};
+
+size_t attn_oproj_smem_bytes(int hd, int G, int K_o, int max_rb_o, bool q4, int nstages,
+                             int slot_bytes);
+size_t ffn_smem_bytes(int K_gu, int max_rb_gu, int K_down, int max_rb_down, bool q4, int nstages,
+                      int slot_bytes);
+const void* attn_oproj_kernel_ptr(int hd, int G, bool q4);
+const void* ffn_kernel_ptr(bool q4);
+cudaError_t launch_attn_oproj(int hd, int G, bool q4, const AttnOprojParams& p, int grid,
+                              size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_ffn(bool q4, const FfnParams& p, int grid, size_t smem, cudaStream_t s,
+                       bool pdl);
+
 // ---- the persistent per-token kernel ---------------------------------------
 struct PLayer {  // per-layer pointers
   const uint8_t* wqkv;
@@ -233,6 +267,8 @@ cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t sme
 const void* attn_kernel_ptr(int hd, int G, bool cluster);
 const void* gemv_kernel_ptr(int pro, int epi, bool q4);
 cudaError_t set_smem_limits();
+// Error flag of dec_attention_noalloc on the current device (see dec_sync_status).
+int noalloc_sync_status(cudaStream_t stream, int* flag_out);
 
 // Load-time repack of a row-major [rows][K] bf16 block into the tiled layout
 // of a matrix with K columns, source row s going to tiled row map(s):

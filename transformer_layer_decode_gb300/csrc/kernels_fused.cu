@@ -144,6 +144,176 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams
   if (!ok && tid == 0) ring_drain(R, P, p.err);
 }
 
+// ---- two-phase kernels (the three-kernel layer) -------------------------------
+// Shared memory: ring (nstages x slot_bytes) | mbarriers | one work area that
+// the two phases use in turn.
+
+size_t attn_oproj_smem_bytes(int hd, int G, int K_o, int max_rb_o, bool q4, int nstages,
+                             int slot_bytes) {
+  size_t work = AttnLayout{hd, G, kConsumerWarps}.total();
+  const size_t g = GemvLayout{K_o, max_rb_o, q4}.total();
+  if (g > work) work = g;
+  return (size_t)nstages * slot_bytes + 16 * (size_t)nstages + work;
+}
+
+size_t ffn_smem_bytes(int K_gu, int max_rb_gu, int K_down, int max_rb_down, bool q4, int nstages,
+                      int slot_bytes) {
+  size_t work = GemvLayout{K_gu, max_rb_gu, q4}.total();
+  const size_t g = GemvLayout{K_down, max_rb_down, q4}.total();
+  if (g > work) work = g;
+  return (size_t)nstages * slot_bytes + 16 * (size_t)nstages + work;
+}
+
+// Attention over the KV cache (the first att_grid CTAs; a flat split of every
+// KV head's chunks, split heads merged by their last CTA through global
+// memory), grid barrier, then o-proj + residual over every CTA.  The producer
+// streams this CTA's K/V chunks and then its Wo slab without a break.
+template <int HD, int G, bool Q4>
+__global__ void __launch_bounds__(kThreads, 1) attn_oproj_fused(const AttnOprojParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.slot_bytes),
+               reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.slot_bytes) + p.nstages,
+               p.nstages, p.slot_bytes};
+  uint8_t* work = smem + (size_t)p.nstages * p.slot_bytes + 16 * (size_t)p.nstages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = gridDim.x, b = blockIdx.x;
+  if (tid == 0) tl_mark_min(p.attn.tl, 0);
+  // The step position, read before griddepcontrol.wait (see attn_decode): it
+  // selects this step's barrier counter; the other one is cleared for the next.
+  const int pos = *p.attn.pos;
+  int* ctr = p.bar + (pos & 1);
+  if (b == 0 && tid == 0) p.bar[(pos & 1) ^ 1] = 0;
+  AttnSplit S = attn_split<HD>(pos, p.attn.nkv, b < p.att_grid ? b : 0, p.att_grid);
+  if (b >= p.att_grid) S.u0 = S.u1 = S.U, S.nu = 0;
+  const int rb0 = (int)split_begin(p.o.n_rb, nb, b), rb1 = (int)split_begin(p.o.n_rb, nb, b + 1);
+  if (tid == 0) ring_init(R);
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      RingPos P{0, 0, 0};
+      const uint64_t pol = policy_evict_first();
+      attn_produce<HD>(p.attn, p.attn.kc, p.attn.vc, R, P, S, pol, [] { pdl_wait(); });
+      gemv_produce(p.o, p.o.w, R, P, rb0, rb1, pol);
+      l2_ahead(p.o.ahead, b);
+    }
+    return;
+  }
+  pdl_wait();  // q comes from the QKV kernel
+  pdl_trigger();
+  if (tid == 0) {
+    tl_mark_min(p.attn.tl, 2);
+    tl_mark_max(p.attn.tl, 3);
+  }
+  RingPos P{0, 0, 0};
+  bool ok = attn_main<HD, G, false, kConsumerWarps>(p.attn, work, R, P, S, b, p.att_grid, tid);
+  if (p.attn.tl) {
+    named_barrier(1, kNC);
+    if (tid == 0) {
+      tl_mark_max(p.attn.tl, 1);
+      tl_mark_min(p.attn.tl, 7);
+    }
+  }
+  // every head is merged into o (by its last CTA) before any CTA reads o
+  grid_sync(ctr, nb, p.attn.err, tid, 1, kNC, p.tl2);
+  const GemvWork W(work, GemvLayout{p.o.geo.K, p.o.max_rb_local, Q4});
+  gemv_pre<PRO_PLAIN>(p.o, nullptr, W, tid);
+  GemvParams po = p.o;
+  po.tl = p.tl2;
+  ok &= gemv_main<PRO_PLAIN, EPI_RESID, Q4>(po, gemv_io(po), W, R, P, rb0, rb1, tid, b == 0);
+  if (p.tl2) {
+    named_barrier(1, kNC);
+    if (tid == 0) {
+      tl_mark_max(p.tl2, 1);
+      tl_mark_min(p.tl2, 7);
+    }
+  }
+  if (!ok && tid == 0) ring_drain(R, P, p.o.err);
+}
+
+// RMSNorm x weight, gate/up GEMV and SwiGLU (a to global memory), grid
+// barrier, then the down GEMV + residual.  The producer streams this CTA's
+// gate/up slab and then its down slab without a break.
+template <bool Q4>
+__global__ void __launch_bounds__(kThreads, 1) ffn_fused(const FfnParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.slot_bytes),
+               reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.slot_bytes) + p.nstages,
+               p.nstages, p.slot_bytes};
+  uint8_t* work = smem + (size_t)p.nstages * p.slot_bytes + 16 * (size_t)p.nstages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = gridDim.x, b = blockIdx.x;
+  if (tid == 0) tl_mark_min(p.gu.tl, 0);
+  // The down phase of the last layer advances the step position; every CTA
+  // reads it here, before the grid barrier that precedes that advance.
+  const int pos = *p.gu.pos;
+  int* ctr = p.bar + (pos & 1);
+  if (b == 0 && tid == 0) p.bar[(pos & 1) ^ 1] = 0;
+  const int ra0 = (int)split_begin(p.gu.n_rb, nb, b), ra1 = (int)split_begin(p.gu.n_rb, nb, b + 1);
+  const int rd0 = (int)split_begin(p.down.n_rb, nb, b), rd1 = (int)split_begin(p.down.n_rb, nb, b + 1);
+  if (tid == 0) ring_init(R);
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      RingPos P{0, 0, 0};
+      const uint64_t pol = policy_evict_first();
+      gemv_produce(p.gu, p.gu.w, R, P, ra0, ra1, pol);
+      gemv_produce(p.down, p.down.w, R, P, rd0, rd1, pol);
+      l2_ahead(p.down.ahead, b);
+    }
+    return;
+  }
+  const GemvWork W1(work, GemvLayout{p.gu.geo.K, p.gu.max_rb_local, Q4});
+  gemv_pre<PRO_NORM>(p.gu, p.gu.norm_w, W1, tid);
+  pdl_wait();  // h1 comes from the o-proj
+  pdl_trigger();
+  if (tid == 0) {
+    tl_mark_min(p.gu.tl, 2);
+    tl_mark_max(p.gu.tl, 3);
+  }
+  RingPos P{0, 0, 0};
+  bool ok = gemv_main<PRO_NORM, EPI_SWIGLU, Q4>(p.gu, gemv_io(p.gu), W1, R, P, ra0, ra1, tid,
+                                                 b == 0);
+  if (p.gu.tl) {
+    named_barrier(1, kNC);
+    if (tid == 0) {
+      tl_mark_max(p.gu.tl, 1);
+      tl_mark_min(p.gu.tl, 7);
+    }
+  }
+  // all of a is written before any CTA reads it
+  grid_sync(ctr, nb, p.gu.err, tid, 1, kNC, p.tl2);
+  const GemvWork W2(work, GemvLayout{p.down.geo.K, p.down.max_rb_local, Q4});
+  gemv_pre<PRO_PLAIN>(p.down, nullptr, W2, tid);
+  GemvParams pd = p.down;
+  pd.tl = p.tl2;
+  ok &= gemv_main<PRO_PLAIN, EPI_RESID, Q4>(pd, gemv_io(pd), W2, R, P, rd0, rd1, tid, b == 0);
+  if (p.tl2) {
+    named_barrier(1, kNC);
+    if (tid == 0) {
+      tl_mark_max(p.tl2, 1);
+      tl_mark_min(p.tl2, 7);
+    }
+  }
+  if (!ok && tid == 0) ring_drain(R, P, p.gu.err);
+}
+
+const void* attn_oproj_kernel_ptr(int hd, int G, bool q4) {
+#define TLD_AO(H_, G_)                                                    \
+  if (hd == H_ && G == G_)                                                \
+    return q4 ? (const void*)attn_oproj_fused<H_, G_, true>               \
+              : (const void*)attn_oproj_fused<H_, G_, false>;
+  TLD_AO(64, 1) TLD_AO(64, 2) TLD_AO(64, 4) TLD_AO(64, 8)
+  TLD_AO(128, 1) TLD_AO(128, 2) TLD_AO(128, 4) TLD_AO(128, 8)
+#undef TLD_AO
+  return nullptr;
+}
+
+const void* ffn_kernel_ptr(bool q4) {
+  return q4 ? (const void*)ffn_fused<true> : (const void*)ffn_fused<false>;
+}
+
 // ---- launch plumbing -----------------------------------------------------------
 
 const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
@@ -177,6 +347,17 @@ cudaError_t set_smem_limits() {
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
+  }
+  for (bool q4 : {false, true}) {
+    cudaError_t e = cudaFuncSetAttribute(ffn_kernel_ptr(q4),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+    for (int hd : {64, 128})
+      for (int G : {1, 2, 4, 8}) {
+        e = cudaFuncSetAttribute(attn_oproj_kernel_ptr(hd, G, q4),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e != cudaSuccess) return e;
+      }
   }
   for (int hd : {64, 128})
     for (int G : {1, 2, 4, 8})
@@ -235,6 +416,22 @@ cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t sme
   void* args[] = {&copy};
   return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster,
                     (attn_consumer_warps(G, p.cluster > 0) + 1) * 32);
+}
+
+cudaError_t launch_attn_oproj(int hd, int G, bool q4, const AttnOprojParams& p, int grid,
+                              size_t smem, cudaStream_t s, bool pdl) {
+  const void* fn = attn_oproj_kernel_ptr(hd, G, q4);
+  if (!fn || p.att_grid < 1 || p.att_grid > grid) return cudaErrorInvalidValue;
+  AttnOprojParams copy = p;
+  void* args[] = {&copy};
+  return launch_pdl(fn, args, grid, smem, s, pdl);
+}
+
+cudaError_t launch_ffn(bool q4, const FfnParams& p, int grid, size_t smem, cudaStream_t s,
+                       bool pdl) {
+  FfnParams copy = p;
+  void* args[] = {&copy};
+  return launch_pdl(ffn_kernel_ptr(q4), args, grid, smem, s, pdl);
 }
 
 // ---- load-time repack ------------------------------------------------------------

@@ -14,32 +14,6 @@ namespace tld {
 
 namespace {
 
-__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Spins until *ctr >= target (bounded by wall time and by the error flag).
-__device__ bool spin_until(const int* ctr, int target, int* err) {
-  if (ld_acquire_gpu(ctr) >= target) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (ld_acquire_gpu(ctr) >= target) return true;
-    if ((i & 63) == 0) {
-      if (*reinterpret_cast<volatile int*>(err)) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        raise_error(err, ERR_GRID_WAIT);
-        return false;
-      }
-    }
-  }
-}
-
 // Grid barrier of the consumers: every CTA arrives once per phase; phase k of
 // the step is complete when the counter reaches (k + 1) * gridDim.x.
 __device__ __forceinline__ void grid_arrive(int* ctr, int tid) {

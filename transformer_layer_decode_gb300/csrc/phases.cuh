@@ -120,10 +120,13 @@ template <int EPI>
 __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO& io, int rb,
                                               const float v[kTileR]) {
   const int R0 = rb * kTileR;
+  if (!TLD_IN_BOUNDS(rb >= 0 && rb < p.n_rb, p.err)) return;
   if (EPI == EPI_QKV) {
     const int hd = p.hd, half = hd / 2;
     const int qrows = p.nq * hd, krows = p.nkv * hd;
     const int pos = *p.pos;
+    if (!TLD_IN_BOUNDS(pos >= 0 && pos < p.max_ctx && R0 + kTileR <= qrows + 2 * krows, p.err))
+      return;
     if (R0 < qrows + krows) {
       // rows (2i, 2i+1) of a head hold dims i and i + hd/2: rotate the pair
       const bool is_q = R0 < qrows;
@@ -345,6 +348,9 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, const uint8_t*
     const int64_t oa = cur.offset(geo);
     cur.advance(kStageTiles, geo.ktiles);
     const int64_t ob = (s == nst - 1) ? end_off : cur.offset(geo);
+    if (!TLD_IN_BOUNDS(oa >= 0 && ob > oa && ob <= (int64_t)p.n_rb * geo.rb_bytes &&
+                           ob - oa <= R.slot_bytes, p.err))
+      return;
     const uint32_t bytes = (uint32_t)(ob - oa);
     mbar_arrive_expect_tx(&R.full[P.slot], bytes);
     bulk_g2s_split(R.slot(P.slot), w + oa, bytes, &R.full[P.slot], pol);
@@ -370,6 +376,7 @@ __device__ __forceinline__ void l2_ahead(const L2Ahead& a, int b) {
   const int64_t start = r0 * a.unit_bytes, lead = start & 15;
   const uint8_t* src = a.base + (start - lead);
   left = (left + lead) & ~(int64_t)15;
+  if (!TLD_IN_BOUNDS(start - lead + left <= (int64_t)a.n_units * a.unit_bytes, nullptr)) return;
   for (int64_t o = 0; o < left; o += kStageBytes) {
     const int64_t n = left - o < kStageBytes ? left - o : kStageBytes;
     bulk_prefetch_l2(src + o, (uint32_t)n);
@@ -496,7 +503,9 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     for (int j = 0; j < kTilesPerWarp; ++j) {
       const int li = s * kStageTiles + warp + j * kConsumerWarps;
       const int kw = (my[j].kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
-      if (li < nloc && c < kw) {
+      if (li < nloc && c < kw &&
+          TLD_IN_BOUNDS(my[j].offset(geo) - st_off >= 0 &&
+                            my[j].offset(geo) - st_off + geo.tile_bytes <= R.slot_bytes, p.err)) {
         const uint8_t* tp = R.slot(P.slot) + (my[j].offset(geo) - st_off);
         if (Q4) {
 #pragma unroll
@@ -715,6 +724,9 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
   for (int s = 0; s < S.nu; ++s) {
     if (!ring_reserve(R, P, p.err)) return;
     const int rows = min(CH, S.n - c * CH);
+    if (!TLD_IN_BOUNDS(g >= 0 && g < p.nkv && rows > 0 && c * CH + rows <= p.max_ctx &&
+                           2 * kAttnStageBytes / 2 <= R.slot_bytes, p.err))
+      return;
     if (c == S.cph - 1 && !waited) {
       wait_pos();
       waited = true;
@@ -1049,7 +1061,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       const int c_hi = split_owner32(U32, nb, h0 + cph - 1);
       if (sp == 0 && c_hi - c_lo + 1 > kMaxSplits) raise_error(p.err, ERR_SPLITS);
       const int c = c_lo + sp;
-      if (c <= c_hi) {
+      if (c <= c_hi && TLD_IN_BOUNDS(c >= 0 && c < nb && g < p.nkv, p.err)) {
         const int cs = part_begin(c);
         if (part_begin(c + 1) > cs) off = ((c * 2 + (cs >= h0 ? 0 : 1)) * G) * (HD + 4);
       }

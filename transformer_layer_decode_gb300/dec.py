@@ -14,21 +14,27 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libtld_gb300.so")
+# the same library with the kernels' index checks compiled in (TLD_DEBUG_CHECKS)
+DEBUG_LIB_PATH = os.path.join(_HERE, "_build", "libtld_gb300_debug.so")
 
 # enum values of dec.h
 DEC_OK, DEC_ERR_ARG, DEC_ERR_SHAPE, DEC_ERR_STATE = 0, -1, -2, -3
 DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6, -7, -8
 DEC_W_BF16, DEC_W_Q4B32 = 0, 1
 DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL, DEC_PLAN_PERSISTENT = 0, 1, 2, 4, 8
-DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE = 16, 32
+DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE, DEC_PLAN_THREE, DEC_DEBUG_GUARDS = 16, 32, 64, 128
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
+# kernels of one layer, per plan
 KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
                 "norm_gateup_swiglu", "down_residual")
+KERNEL_NAMES_THREE = ("norm_qkv_rope_append", "attention_oproj_residual",
+                      "norm_gateup_swiglu_down_residual")
 
-EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_truncate_kv", "dec_step",
-            "dec_set_tap", "dec_set_dot_tap", "dec_set_timeline", "dec_sync_status", "dec_get_info", "dec_launch_kernel",
+EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_read_kv", "dec_truncate_kv", "dec_step",
+            "dec_set_tap", "dec_set_dot_tap", "dec_set_timeline", "dec_sync_status",
+            "dec_check_guards", "dec_get_info", "dec_launch_kernel",
             "dec_destroy", "dec_last_error", "dec_attention_noalloc")
 
 
@@ -55,14 +61,14 @@ class Info(ctypes.Structure):
                 ("attn_cluster", ctypes.c_int32)]
 
 
-_lib = None
+_libs: dict = {}
 
 
 def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
-    """Load libtld_gb300.so (built by ``build.build()``); raise if it is missing."""
-    global _lib
-    if _lib is not None:
-        return _lib
+    """Load libtld_gb300.so (built by ``build.build()``), or the debug build of it
+    (``DEBUG_LIB_PATH``, ``build.build(debug=True)``); raise if it is missing."""
+    if path in _libs:
+        return _libs[path]
     if not os.path.exists(path):
         raise RuntimeError(f"decode library not built: {path} is missing "
                            "(run transformer_layer_decode_gb300.build.build())")
@@ -72,12 +78,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dec_create": [ctypes.POINTER(ModelDesc), ctypes.POINTER(vp)],
         "dec_load_weights": [vp, i32, i32, vp, sz],
         "dec_load_kv": [vp, i32, vp, vp, i32],
+        "dec_read_kv": [vp, i32, vp, vp, i32, i32],
         "dec_truncate_kv": [vp, i32],
         "dec_step": [vp, vp, i32, vp, vp],
         "dec_set_tap": [vp, vp, vp, vp],
         "dec_set_timeline": [vp, vp],
         "dec_set_dot_tap": [vp, i32, i32, vp],
         "dec_sync_status": [vp, vp],
+        "dec_check_guards": [vp],
         "dec_get_info": [vp, ctypes.POINTER(Info)],
         "dec_launch_kernel": [vp, i32, i32, i32, vp],
         "dec_destroy": [vp],
@@ -89,7 +97,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         fn.restype = i32
     L.dec_last_error.argtypes = [vp]
     L.dec_last_error.restype = ctypes.c_char_p
-    _lib = L
+    _libs[path] = L
     return L
 
 
@@ -133,6 +141,15 @@ def attention_noalloc(q, k_cache, v_cache, n_q_heads: int, n_kv_heads: int, head
         raise DecError(rc, "dec_attention_noalloc rejected its arguments or failed to launch")
 
 
+def noalloc_sync_status(stream=None):
+    """Wait for `stream` and raise DecError if dec_attention_noalloc's kernel
+    gave up a bounded wait on the current device (dec_sync_status(NULL, ...))."""
+    L = load_library()
+    rc = L.dec_sync_status(None, _stream_handle(stream))
+    if rc != DEC_OK:
+        raise DecError(rc, L.dec_last_error(None).decode())
+
+
 @dataclass
 class Shape:
     n_layers: int
@@ -152,13 +169,15 @@ class Decoder:
 
     def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True,
                  pdl: bool = True, persistent: bool = False, l2_ahead: bool = True,
-                 cluster_attn: bool = True):
-        self.lib = load_library()
+                 cluster_attn: bool = True, three: bool = False, guards: bool = False,
+                 lib_path: str | None = None):
+        self.lib = load_library(lib_path or LIB_PATH)
         self.shape = shape
         flags = ((DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
                  | (0 if pdl else DEC_NO_PDL) | (DEC_PLAN_PERSISTENT if persistent else 0)
                  | (0 if l2_ahead else DEC_NO_L2_AHEAD)
-                 | (0 if cluster_attn else DEC_ATTN_GLOBAL_MERGE))
+                 | (0 if cluster_attn else DEC_ATTN_GLOBAL_MERGE)
+                 | (DEC_PLAN_THREE if three else 0) | (DEC_DEBUG_GUARDS if guards else 0))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
                               shape.max_ctx, shape.weight_fmt, flags)
@@ -179,6 +198,14 @@ class Decoder:
         n = k.shape[1] if n_pos is None else n_pos
         self._check(self.lib.dec_load_kv(self.h, layer, _ptr(k), _ptr(v), n))
 
+    def read_kv(self, layer: int, first_pos: int, n_pos: int):
+        """Rows [first_pos, first_pos + n_pos) of one layer's cache: (K, V) bf16
+        bits [n_kv_heads][n_pos][head_dim] as numpy uint16."""
+        sh = (self.shape.n_kv_heads, n_pos, self.shape.head_dim)
+        k, v = np.empty(sh, np.uint16), np.empty(sh, np.uint16)
+        self._check(self.lib.dec_read_kv(self.h, layer, _ptr(k), _ptr(v), first_pos, n_pos))
+        return k, v
+
     def truncate_kv(self, n_pos: int):
         self._check(self.lib.dec_truncate_kv(self.h, n_pos))
 
@@ -196,6 +223,9 @@ class Decoder:
 
     def sync_status(self, stream=None):
         self._check(self.lib.dec_sync_status(self.h, _stream_handle(stream)))
+
+    def check_guards(self):
+        self._check(self.lib.dec_check_guards(self.h))
 
     def info(self) -> Info:
         inf = Info()
