@@ -60,6 +60,9 @@ def parse():
                     help="fused plan: no programmatic dependent launch between kernels")
     ap.add_argument("--no-l2-ahead", action="store_true",
                     help="fused plan: no L2 prefetch of the next kernel's bytes")
+    ap.add_argument("--lm-head", type=int, default=0, metavar="VOCAB",
+                    help="end every step with an LM head of this vocabulary and the greedy "
+                         "token (not part of the headline workload, which has no LM head)")
     ap.add_argument("--global-merge", action="store_true",
                     help="fused plan: flat attention grid merged through global memory "
                          "instead of one cluster per KV head")
@@ -366,6 +369,11 @@ def run_ours(args, w, rank, world, local_rank):
                                     persistent=persistent, graph=not args.eager,
                                     pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
                                     cluster_attn=not args.global_merge, three=args.plan == "three")
+    if args.lm_head:
+        nw, Wlm = synth.lm_head(w, args.lm_head)
+        d.load_lm_head(nw, Wlm)
+        tok_out = torch.empty(1, dtype=torch.int32, device=dev)
+        d.set_token_out(tok_out)
     info = d.info()
     H = w.hidden
     xs = torch.from_numpy(workload.step_inputs(w, max(K, W))).to(dev)
@@ -461,6 +469,9 @@ def run_ours(args, w, rank, world, local_rank):
     tok_s = replica_tok_s(world, K, ms)
     tok_s_e2e = replica_tok_s(world, K, ms_e2e)
     bpt = bytes_per_token(w, w.prefill + (K + 1) / 2.0)
+    if args.lm_head:
+        lm_bytes = 2 * args.lm_head * (w.hidden + 1)
+        bpt = {**bpt, "lm_head": lm_bytes, "total": bpt["total"] + lm_bytes}
 
     result = {
         "metric": metric_name(w),
@@ -477,7 +488,8 @@ def run_ours(args, w, rank, world, local_rank):
                                      + (["no L2 look-ahead"] if args.no_l2_ahead else [])
                                      + (["global-merge attention"] if args.global_merge else [])),
                    "kernels_per_layer": info.kernels_per_layer,
-                   "kernels_per_token": info.kernels_per_token,
+                   "kernels_per_token": info.kernels_per_token + (1 if args.lm_head else 0),
+                   "lm_head_vocab": args.lm_head or None,
                    "attn_ctas": info.attn_grid, "attn_cluster": info.attn_cluster,
                    "l2": "no flush: each step streams %.1f GB of weights + KV (> 129 MB L2)"
                          % (bpt["total"] / 1e9)},
@@ -491,7 +503,7 @@ def run_ours(args, w, rank, world, local_rank):
                      "avg_launch_ms": k_ms, "peak_kind": peak_kind},
         "e2e": {"value": tok_s_e2e, "unit": "tok/s", "h2d_bytes_per_step": 4 * H,
                 "d2h_bytes_per_step": 4 * H},
-        "gpu_launches": info.kernels_per_token * K,
+        "gpu_launches": (info.kernels_per_token + (1 if args.lm_head else 0)) * K,
         "clocks": clocks.summary(),
     }
     d.close()

@@ -76,11 +76,18 @@ enum dec_flags {
                                  KV append; attention + o-proj + residual; norm + gate/up +
                                  SwiGLU + down + residual (each of the last two one launch of
                                  two phases separated by a grid barrier) */
-  DEC_DEBUG_GUARDS = 128      /* memory-safety checks that need no sanitizer: every device
+  DEC_DEBUG_GUARDS = 128,     /* memory-safety checks that need no sanitizer: every device
                                  buffer between guard bands of a known pattern, its bytes
                                  poisoned with 0xFF (NaN as fp32 and bf16) until written, KV
                                  rows past the KV length kept poisoned; dec_check_guards
                                  verifies them */
+  DEC_ROPE_INTERLEAVED = 256, /* RoPE rotates dims (2i, 2i+1) of a head as pair i instead of
+                                 (i, i + head_dim/2); same angles pos * theta^(-2i/head_dim) */
+  DEC_PAGED_KV = 512          /* fused plans: each layer's KV cache is a pool of pages, a page
+                                 holding page_rows positions of one KV head (one attention
+                                 chunk: 64 at head_dim 128, 128 at 64), laid out
+                                 [page][n_kv_heads][page_rows][head_dim]; a page table maps
+                                 position chunk c to page pages[c] (dec_set_page_table) */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
@@ -123,6 +130,8 @@ typedef struct dec_info {
   int32_t attn_grid;          /* CTAs of the attention launch (fused plan) */
   int32_t attn_cluster;       /* CTAs per KV head in one thread-block cluster, or 0 for
                                  the flat grid merged through global memory */
+  int32_t page_rows;          /* DEC_PAGED_KV: positions per page (else 0) */
+  int32_t n_pages;            /* DEC_PAGED_KV: pages per layer = entries of the page table */
 } dec_info;
 
 typedef struct dec_handle dec_handle; /* opaque */
@@ -154,6 +163,37 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
  * position, v raw).  Sets that layer's KV length to n_pos.  Blocks until done
  * and waits for all queued work of the device first. */
 int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16, int n_pos);
+
+/* Source: "RDNA4 Decode Kernel Fusion", section "What it does to the token",
+ * Table 1 (the token ends with "LM head + sampling" after the layers).
+ * Loads the LM head: final_norm_bf16, host or device bf16 [hidden], the
+ * final RMSNorm weight, and w_bf16, host or device bf16 [vocab][hidden]
+ * ([out][in], row-major), copied (repacked) into library-owned memory.
+ * vocab must be a positive multiple of 4.  Blocks until done; discards the
+ * captured graph.  Tokens are produced only once dec_set_token_out is given a
+ * destination. */
+int dec_load_lm_head(dec_handle* h, const void* final_norm_bf16, const void* w_bf16, int vocab);
+
+/* Source: as dec_load_lm_head.  token_out: device int32, or NULL to stop
+ * producing tokens.  While set, every dec_step ends with the LM head: the
+ * final RMSNorm (the model's eps) of the step's out_hidden times the final
+ * norm weight, logits = W n in fp32, and the greedy token, the index of the
+ * largest logit (the lowest index among equal ones), written to *token_out.
+ * logits_tap (device fp32 [vocab] or NULL) also receives the logits.  The
+ * choice is the same every run: each CTA's largest logit is combined with an
+ * order-independent maximum.  Needs dec_load_lm_head first (DEC_ERR_STATE);
+ * discards the captured graph. */
+int dec_set_token_out(dec_handle* h, int32_t* token_out, float* logits_tap);
+
+/* Source: "Kernel fusion and block bridging", section "Fusion" (the rotated k
+ * and the v of a token written into their KV pages by the projection launch).
+ * Sets the page table of a DEC_PAGED_KV handle: pages, host or device int32
+ * [n], n = n_pages (dec_get_info), a permutation of 0..n-1; position chunk c
+ * lives in page pages[c] of every layer's pool.  Rows already in the cache
+ * move with their chunks.  Waits for the device; discards nothing (the graph
+ * reads the table from device memory).  DEC_ERR_STATE without DEC_PAGED_KV,
+ * DEC_ERR_ARG for a wrong length, an entry out of range or repeated. */
+int dec_set_page_table(dec_handle* h, const int32_t* pages, int n);
 
 /* Source: none on the pages; an addition the parity check of the KV append
  * forces (the rows the QKV kernel wrote are compared with the reference chain's).

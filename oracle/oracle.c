@@ -16,7 +16,8 @@
  *
  * The pages give no formulas.  Readings taken where they are silent:
  *   RMSNorm      n = x / sqrt(mean(x^2) + eps) * w   (eps inside the root, w direct)
- *   RoPE         rotate-half pairs (i, i + d/2), angle pos * theta^(-2i/d)
+ *   RoPE         rotate-half pairs (i, i + d/2), angle pos * theta^(-2i/d); the
+ *                interleaved form rotates pairs (2i, 2i + 1) by the same angle
  *   KV append    rotated k and raw v stored as bf16 (round to nearest even) at
  *                row pos; the new token then attends to rows 0..pos
  *   attention    softmax(q.K^T / sqrt(d)) V, query head h reads KV head
@@ -54,6 +55,9 @@ enum {
   MUT_Q4_STALE_N1 = 12,     /* gate/up input reuses the int8 codes of n1 */
   MUT_Q4_O_TENSOR_SCALE = 13, /* o quantized with one scale over the whole vector */
   MUT_Q4_A_NO_DX = 14,      /* down projection drops the block scales of a */
+  MUT_ROPE_PAIR_SWAP = 15,  /* interleaved RoPE rotating (2i+1, 2i) instead of (2i, 2i+1) */
+  MUT_ARGMAX_LAST_TIE = 16, /* greedy choice keeps the last of equal logits */
+  MUT_LM_NO_NORM = 17,      /* LM head without the final RMSNorm */
 };
 
 /* ---- storage formats ---------------------------------------------------- */
@@ -163,6 +167,27 @@ void orc_attention_head(const double* q, const uint16_t* K, const uint16_t* V, i
   free(s);
 }
 
+/* RoPE with interleaved pairs: dims (2i, 2i + 1) of each head are rotated by
+ * pos * theta^(-2i/d), the pairing of models whose rotary embedding treats
+ * adjacent dims as one complex number. */
+void orc_rope_interleaved(double* h, int n_heads, int d, int pos, double theta) {
+  for (int hd = 0; hd < n_heads; ++hd) {
+    double* v = h + (size_t)hd * d;
+    for (int i = 0; i < d / 2; ++i) {
+      double phi = pos * pow(theta, -2.0 * i / d);
+      double c = cos(phi), s = sin(phi);
+      int e = 2 * i, o = 2 * i + 1;
+      if (g_mutation == MUT_ROPE_PAIR_SWAP) {
+        e = 2 * i + 1;
+        o = 2 * i;
+      }
+      double a = v[e], b = v[o];
+      v[e] = a * c - b * s;
+      v[o] = a * s + b * c;
+    }
+  }
+}
+
 /* Query head -> KV head (contiguous groups). */
 int orc_kv_head_of(int h, int n_q, int n_kv) {
   if (g_mutation == MUT_ATTN_GQA_MOD) return h % n_kv;
@@ -243,7 +268,7 @@ void orc_gemv_q4(const uint8_t* Wq, const uint16_t* Ws, int N, int K, const int8
 
 typedef struct orc_dims {
   int32_t hidden, n_q_heads, n_kv_heads, head_dim, ffn, max_ctx, q4;
-  int32_t pad_;
+  int32_t rope_interleaved; /* 0: rotate-half pairs, 1: interleaved pairs */
   double rms_eps, rope_theta;
 } orc_dims;
 
@@ -362,8 +387,13 @@ int orc_layer_step(const orc_dims* D, const orc_layer* L, int pos, const double*
   project(D, L, W_K, nkv * d, H, n1, k, qb, db);
   project(D, L, W_V, nkv * d, H, n1, v, qb, db);
   /* RoPE on q and k */
-  orc_rope(q, nq, d, pos, D->rope_theta);
-  orc_rope(k, nkv, d, pos, D->rope_theta);
+  if (D->rope_interleaved) {
+    orc_rope_interleaved(q, nq, d, pos, D->rope_theta);
+    orc_rope_interleaved(k, nkv, d, pos, D->rope_theta);
+  } else {
+    orc_rope(q, nq, d, pos, D->rope_theta);
+    orc_rope(k, nkv, d, pos, D->rope_theta);
+  }
   if (tap && tap->kz) memcpy(tap->kz, k, sizeof(double) * (size_t)nkv * d);
   if (tap && tap->vz) memcpy(tap->vz, v, sizeof(double) * (size_t)nkv * d);
   /* KV append at row pos (storage rounding to bf16 is itself a decision made
@@ -425,4 +455,28 @@ int orc_stack_step(const orc_dims* D, const orc_layer* layers, int n_layers, int
   free(cur);
   free(nxt);
   return 0;
+}
+
+/* ---- after the stack: LM head and greedy choice --------------------------- */
+
+/* The token after the stack's output x[H]: the final RMSNorm and its weight
+ * multiply, the vocabulary projection (W bf16 [V][H]) into logits[V], and the
+ * greedy choice, the index of the largest logit (the lowest index among equal
+ * ones).  "RDNA4 Decode Kernel Fusion", section "What it does to the token",
+ * Table 1 ("LM head + sampling"). */
+int orc_lm_head(const double* x, int H, const uint16_t* norm_w, const uint16_t* W, int V,
+                double eps, double* logits) {
+  double* n = (double*)malloc(sizeof(double) * (size_t)H);
+  if (g_mutation == MUT_LM_NO_NORM) {
+    for (int i = 0; i < H; ++i) n[i] = x[i];
+  } else {
+    orc_rmsnorm(x, norm_w, H, eps, n);
+  }
+  orc_gemv_bf16(W, V, H, n, logits);
+  int best = 0;
+  for (int j = 1; j < V; ++j)
+    if (logits[j] > logits[best] || (g_mutation == MUT_ARGMAX_LAST_TIE && logits[j] == logits[best]))
+      best = j;
+  free(n);
+  return best;
 }

@@ -28,6 +28,7 @@ MUTATIONS = {
     "attn_no_scale": 5, "attn_gqa_mod": 6, "silu_on_up": 7, "no_residual2": 8,
     "gemv_transpose": 9, "q4_no_offset": 10, "attn_skip_last": 11,
     "q4_stale_n1_codes": 12, "q4_o_tensor_scale": 13, "q4_a_no_dx": 14,
+    "rope_pair_swap": 15, "argmax_last_tie": 16, "lm_no_norm": 17,
 }
 
 # Tensor order of the layer struct's matrix slots.
@@ -38,7 +39,7 @@ class Dims(ctypes.Structure):
     _fields_ = [("hidden", ctypes.c_int32), ("n_q_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
                 ("ffn", ctypes.c_int32), ("max_ctx", ctypes.c_int32), ("q4", ctypes.c_int32),
-                ("pad_", ctypes.c_int32), ("rms_eps", ctypes.c_double),
+                ("rope_interleaved", ctypes.c_int32), ("rms_eps", ctypes.c_double),
                 ("rope_theta", ctypes.c_double)]
 
 
@@ -85,6 +86,7 @@ def lib() -> ctypes.CDLL:
                 "orc_rmsnorm": (None, [vp, vp, i32, dbl, vp]),
                 "orc_gemv_bf16": (None, [vp, i32, i32, vp, vp]),
                 "orc_rope": (None, [vp, i32, i32, i32, dbl]),
+                "orc_rope_interleaved": (None, [vp, i32, i32, i32, dbl]),
                 "orc_attention_head": (None, [vp, vp, vp, i32, i32, vp]),
                 "orc_kv_head_of": (i32, [i32, i32, i32]),
                 "orc_silu": (dbl, [dbl]),
@@ -94,6 +96,7 @@ def lib() -> ctypes.CDLL:
                 "orc_gemv_q4": (None, [vp, vp, i32, i32, vp, vp, vp]),
                 "orc_layer_step": (i32, [vp, vp, i32, vp, vp, vp]),
                 "orc_stack_step": (i32, [vp, vp, i32, i32, vp, vp, vp]),
+                "orc_lm_head": (i32, [vp, i32, vp, vp, i32, dbl, vp]),
             }
             for name, (res, args) in sig.items():
                 fn = getattr(L, name)
@@ -158,11 +161,12 @@ def gemv_bf16(W_bits: np.ndarray, x) -> np.ndarray:
     return y
 
 
-def rope(h, pos: int, theta: float) -> np.ndarray:
-    """h: [n_heads, d] -> rotated copy."""
+def rope(h, pos: int, theta: float, interleaved: bool = False) -> np.ndarray:
+    """h: [n_heads, d] -> rotated copy (rotate-half pairs, or interleaved pairs)."""
     h = _f64(h).copy()
     n, d = h.shape
-    lib().orc_rope(_p(h), n, d, pos, theta)
+    fn = lib().orc_rope_interleaved if interleaved else lib().orc_rope
+    fn(_p(h), n, d, pos, theta)
     return h
 
 
@@ -222,6 +226,18 @@ def gemv_q4(packed: np.ndarray, scales: np.ndarray, qx: np.ndarray, dx: np.ndarr
     return y
 
 
+def lm_head(x, norm_w_bits: np.ndarray, W_bits: np.ndarray, eps: float = 1e-6):
+    """Final RMSNorm x weight, logits = W n (W bf16 bits [V][H]), and the greedy
+    token (the lowest index of the largest logit).  Returns (token, logits)."""
+    x = _f64(x)
+    nw = np.ascontiguousarray(norm_w_bits, dtype=np.uint16)
+    W = np.ascontiguousarray(W_bits, dtype=np.uint16)
+    V, H = W.shape
+    logits = np.empty(V, dtype=np.float64)
+    tok = lib().orc_lm_head(_p(x), H, _p(nw), _p(W), V, eps, _p(logits))
+    return int(tok), logits
+
+
 # ---- the stack ----------------------------------------------------------------
 
 class OracleStack:
@@ -233,9 +249,9 @@ class OracleStack:
     """
 
     def __init__(self, *, hidden, n_q_heads, n_kv_heads, head_dim, ffn, max_ctx, layers,
-                 rms_eps=1e-6, rope_theta=1e4, q4=False):
-        self.dims = Dims(hidden, n_q_heads, n_kv_heads, head_dim, ffn, max_ctx, int(q4), 0,
-                         rms_eps, rope_theta)
+                 rms_eps=1e-6, rope_theta=1e4, q4=False, rope_interleaved=False):
+        self.dims = Dims(hidden, n_q_heads, n_kv_heads, head_dim, ffn, max_ctx, int(q4),
+                         int(rope_interleaved), rms_eps, rope_theta)
         self.n_layers = len(layers)
         self.hidden = hidden
         self.kv_len = 0

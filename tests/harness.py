@@ -25,7 +25,8 @@ def oracle_stack(w: synth.Workload, host: dict, max_ctx: int) -> orc.OracleStack
                                q4=[lw.q4[t] for t in order]))
     st = orc.OracleStack(hidden=w.hidden, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
                          head_dim=w.head_dim, ffn=w.ffn, max_ctx=max_ctx, layers=layers,
-                         rms_eps=w.rms_eps, rope_theta=w.rope_theta, q4=w.weight_fmt == "q4")
+                         rms_eps=w.rms_eps, rope_theta=w.rope_theta, q4=w.weight_fmt == "q4",
+                         rope_interleaved=w.rope_interleaved)
     for l, (k, v) in enumerate(host["kv"]):
         if w.prefill:
             st.load_kv(l, k, v)

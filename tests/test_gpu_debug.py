@@ -34,6 +34,7 @@ PLANS = {
     "three": {"three": True},
     "persistent": {"persistent": True},
     "unfused": {"unfused": True},
+    "paged": {"paged_kv": True},
 }
 
 
@@ -48,6 +49,8 @@ def test_debug_build_with_guards(debug_lib, name, plan):
     w = SHAPES[name]
     max_ctx = w.prefill + w.steps + 3
     d = dec.Decoder(workload.shape_of(w, max_ctx), guards=True, lib_path=debug_lib, **PLANS[plan])
+    if plan == "paged":
+        d.set_page_table(np.random.default_rng(3).permutation(d.info().n_pages))
     host = {"layers": [], "kv": []}
     for l in range(w.n_layers):
         lw = synth.layer_weights(w, l)

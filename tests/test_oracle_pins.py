@@ -142,6 +142,43 @@ def pin_rope():
     _close(r, _rope_complex(h, 777, theta), 1e-12, "complex formulation")
 
 
+def pin_rope_interleaved():
+    """Interleaved pairs (2i, 2i+1): the rotate-half rotation conjugated by the
+    permutation that takes dim 2i to i and 2i+1 to i + d/2; a d = 2 head turns
+    by pos radians; identity at pos 0; pair norms kept; and a whole layer with
+    interleaved RoPE equals the rotate-half layer on weights whose q/k rows are
+    permuted the same way (attention is invariant under a shared permutation of
+    q and k dims)."""
+    theta, d = 1e4, 64
+    perm = np.concatenate([np.arange(0, d, 2), np.arange(1, d, 2)])  # new order of old dims
+    h = RNG.normal(0, 1, (3, d))
+    got = orc.rope(h, 321, theta, interleaved=True)
+    via = np.empty_like(h)
+    via[:, perm] = orc.rope(h[:, perm], 321, theta)
+    _close(got, via, 1e-12, "interleaved = conjugated rotate-half")
+    _close(orc.rope(h, 0, theta, interleaved=True), h, 0, "pos 0 identity")
+    pn = lambda v: v[:, 0::2] ** 2 + v[:, 1::2] ** 2
+    _close(pn(got), pn(h), 1e-12, "pair norms")
+    e = np.array([[1.0, 0.0]])
+    _close(orc.rope(e, 3, theta, interleaved=True), np.array([[math.cos(3), math.sin(3)]]), 1e-15,
+           "d = 2 turns by pos radians")
+    # a layer: interleaved pairs on permuted q/k rows == rotate-half on the originals
+    H, nq, nkv, dd, Fd = 32, 2, 1, 8, 48
+    lw = _toy_layer(H, nq, nkv, dd, Fd)
+    pr = np.concatenate([np.arange(0, dd, 2), np.arange(1, dd, 2)])
+    lw_i = dict(lw)
+    lw_i["w"] = list(lw["w"])
+    for t, heads in ((0, nq), (1, nkv)):
+        rows = np.concatenate([hh * dd + np.argsort(pr) for hh in range(heads)])
+        lw_i["w"][t] = lw["w"][t][rows]
+    kw = dict(hidden=H, n_q_heads=nq, n_kv_heads=nkv, head_dim=dd, ffn=Fd, max_ctx=4)
+    a = orc.OracleStack(layers=[lw], **kw)
+    b = orc.OracleStack(layers=[lw_i], rope_interleaved=True, **kw)
+    for pos in range(3):
+        x = RNG.normal(0, 1, H)
+        _close(b.step(x, pos), a.step(x, pos), 1e-12, f"interleaved layer, pos {pos}")
+
+
 # ---- attention -------------------------------------------------------------------
 
 def pin_attention():
@@ -225,6 +262,37 @@ def pin_q4_dots():
     Wd = qw * np.repeat(sc.view(np.float16).astype(np.float64), 32, axis=1)
     xd = qx * np.repeat(dx.astype(np.float64), 32)
     _close(orc.gemv_q4(pk, sc, qx, dx), Wd @ xd, 1e-13, "dequantised matmul")
+
+
+# ---- LM head and greedy choice ------------------------------------------------------
+
+def pin_lm_head():
+    """A one-hot hidden state picks one column of W: the token is the row whose
+    entry in that column is largest (checked against numpy on the column);
+    equal largest logits go to the lowest index; the logits equal torch's
+    float64 rms_norm followed by numpy's matmul."""
+    H, V, eps = 64, 40, 1e-6
+    W = _rand_bf16((V, H), 0.5)
+    nw = _rand_bf16(H, 0.1, 1.0)
+    k = 23
+    x = np.zeros(H)
+    x[k] = 3.0
+    tok, logits = orc.lm_head(x, nw, W, eps)
+    col = _bf16_f64(W)[:, k] * _bf16_f64(nw)[k]
+    assert tok == int(np.argmax(col)), (tok, int(np.argmax(col)))
+    # ties: rows 7 and 19 equal and the largest
+    Wt = W.copy()
+    Wt[19] = Wt[7]
+    top = _bf16_bits_from_f32(np.array([9.0], np.float32))[0]
+    Wt[7, k] = Wt[19, k] = top
+    assert orc.lm_head(x, nw, Wt, eps)[0] == 7
+    # library restatement of the logits
+    xr = RNG.normal(0, 2, H)
+    n = F.rms_norm(torch.from_numpy(xr), (H,), weight=torch.from_numpy(_bf16_f64(nw)), eps=eps)
+    tok, logits = orc.lm_head(xr, nw, W, eps)
+    ref = _bf16_f64(W) @ n.numpy()
+    _close(logits, ref, 1e-13, "LM head logits")
+    assert tok == int(np.argmax(ref))
 
 
 # ---- whole layer -----------------------------------------------------------------
@@ -599,7 +667,8 @@ def pin_q4_layer_restated():
             st.kv_len = pos + 1
 
 
-PINS = [pin_storage_formats, pin_rmsnorm, pin_gemv, pin_rope, pin_attention, pin_swiglu,
+PINS = [pin_storage_formats, pin_rmsnorm, pin_gemv, pin_rope, pin_rope_interleaved,
+        pin_attention, pin_swiglu, pin_lm_head,
         pin_quant, pin_q4_dots, pin_layer, pin_residual_wiring, pin_kv_append_closed_form,
         pin_q4_layer, pin_layer_brute_force, pin_q4_layer_restated]
 

@@ -51,6 +51,13 @@ struct dec_handle {
   bool fused = true, graph = true, pdl = true, persistent = false, l2_ahead = true;
   bool cluster_attn = true;
   bool three = false;  // fused plan: three kernels per layer (else five)
+  bool rope_inter = false;  // RoPE pairs (2i, 2i+1)
+  // paged KV cache: pages of page_rows positions of one KV head; the page table
+  // (host copy and device copy) maps position chunk c to page pages[c]
+  bool paged = false;
+  int page_rows = 0, n_pages = 0;
+  std::vector<int> h_pages;
+  int* d_pages = nullptr;
   // three-kernel plan: barrier counters [n_layers][2 launch sites][2 parities],
   // and the ring / shared memory of the two-phase kernels
   int* d_fbar = nullptr;
@@ -96,6 +103,16 @@ struct dec_handle {
   float* tap = nullptr;
   int8_t* qtap = nullptr;
   float* qstap = nullptr;
+  // LM head after the stack (optional)
+  Tiled lm;
+  uint16_t* lm_norm = nullptr;
+  float* logits = nullptr;             // [vocab], when the caller gives no tap
+  unsigned long long* lm_key = nullptr;  // [2]: running best key, CTA ticket
+  int vocab = 0;
+  bool lm_loaded = false;
+  int32_t* token_out = nullptr;
+  float* logits_tap = nullptr;
+  cudaGraphNode_t lm_node = nullptr;
   // graph
   cudaStream_t cap_stream = nullptr;
   cudaGraph_t graph_g = nullptr;
@@ -216,7 +233,26 @@ void drop_graph(dec_handle* h) {
   if (h->graph_g) cudaGraphDestroy(h->graph_g);
   h->exec = nullptr;
   h->graph_g = nullptr;
-  h->first_node = h->last_node = nullptr;
+  h->first_node = h->last_node = h->lm_node = nullptr;
+}
+
+// Calls fn(element offset, rows, src row offset) for every run of rows
+// [t0, t1) of every KV head that is contiguous in the cache layout (one run a
+// head when contiguous, one a page when paged); the source row offset counts
+// rows of a [nkv][t1 - t0][hd] array.
+template <class Fn>
+int for_kv_runs(const dec_handle* h, int t0, int t1, Fn&& fn) {
+  const dec_model_desc& d = h->d;
+  const int* pages = h->paged ? h->h_pages.data() : nullptr;
+  for (int g = 0; g < d.n_kv_heads; ++g)
+    for (int t = t0; t < t1;) {
+      const int end = h->paged ? std::min(t1, (t / h->page_rows + 1) * h->page_rows) : t1;
+      const int64_t off = kv_row_offset(pages, h->page_rows, d.n_kv_heads, d.max_ctx, d.head_dim, g, t);
+      const int rc = fn(off, end - t, (int64_t)g * (t1 - t0) + (t - t0));
+      if (rc) return rc;
+      t = end;
+    }
+  return DEC_OK;
 }
 
 // ---- the fused plan ------------------------------------------------------------
@@ -236,6 +272,8 @@ GemvParams gemv_base(const dec_handle* h, const Tiled& t) {
   p.max_ctx = h->d.max_ctx;
   p.pos = h->d_pos;
   p.rope = h->rope;
+  p.rope_inter = h->rope_inter ? 1 : 0;
+  p.pages = h->paged ? h->d_pages : nullptr;
   return p;
 }
 
@@ -256,6 +294,7 @@ AttnParams k2_params(const dec_handle* h, int l) {
   AttnParams p{};
   p.kc = L.kc;
   p.vc = L.vc;
+  p.pages = h->paged ? h->d_pages : nullptr;
   p.q = h->q;
   p.o = h->o;
   p.part = h->apart;
@@ -334,6 +373,7 @@ L2Ahead l2_ahead_of(const dec_handle* h, int kernel, int l) {
       a.pos = h->d_pos;
       a.grid = fused_att_grid(h);
       a.cluster = h->att_cluster;
+      a.pages = h->paged ? h->d_pages : nullptr;
       a.cap = kL2AheadBytes;
       break;
     case 1: rows(L.o); break;
@@ -481,7 +521,7 @@ int enqueue_unfused_layer(dec_handle* h, int l, const float* x_in, float* out, b
   TLD_U(proj(0, nq * hd, H, h->n1, h->q));
   TLD_U(proj(1, nkv * hd, H, h->n1, h->k));
   TLD_U(proj(2, nkv * hd, H, h->n1, h->v));
-  TLD_U(unf::rope(h->q, h->k, nq, nkv, hd, h->d_pos, h->rope, s));
+  TLD_U(unf::rope(h->q, h->k, nq, nkv, hd, h->d_pos, h->rope, h->rope_inter ? 1 : 0, s));
   TLD_U(unf::kv_append(h->k, h->v, nkv, hd, d.max_ctx, h->d_pos, L.kc, L.vc, s));
   TLD_U(unf::attention(h->q, L.kc, L.vc, nq, nkv, hd, d.max_ctx, h->d_pos, h->o, s));
   if (q4) TLD_U(quant(h->o, nq * hd, 1));
@@ -537,8 +577,37 @@ TokenParams token_params(const dec_handle* h, const float* emb, float* out) {
   return P;
 }
 
+int enqueue_layers(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing);
+
+LmHeadParams lm_params(const dec_handle* h, const float* out) {
+  LmHeadParams P{};
+  P.g = gemv_base(h, h->lm);
+  P.g.x = out;
+  P.g.norm_w = h->lm_norm;
+  P.g.out = h->logits_tap ? h->logits_tap : h->logits;
+  P.key = h->lm_key;
+  P.token_out = h->token_out;
+  return P;
+}
+
+// The LM head and the greedy token after the stack's last layer (when the
+// caller asked for tokens).
+int enqueue_lm_head(dec_handle* h, const float* out, cudaStream_t s, bool capturing) {
+  if (!h->token_out) return DEC_OK;
+  cudaError_t e = launch_lm_head(lm_params(h, out), h->n_sm, h->lm.smem, s, h->pdl);
+  if (e != cudaSuccess) return cuda_fail(h, e, "LM head launch");
+  if (capturing) h->lm_node = last_captured_node(s);
+  return DEC_OK;
+}
+
 // Queues one whole token.  Records the first and last kernel nodes when capturing.
 int enqueue_step(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing) {
+  const int rc = enqueue_layers(h, emb, out, s, capturing);
+  if (rc) return rc;
+  return enqueue_lm_head(h, out, s, capturing);
+}
+
+int enqueue_layers(dec_handle* h, const float* emb, float* out, cudaStream_t s, bool capturing) {
   const int Lc = h->d.n_layers;
   if (h->persistent) {
     cudaError_t e = launch_persistent(h->d.head_dim, h->G, h->d.weight_fmt == DEC_W_Q4B32,
@@ -583,7 +652,7 @@ int capture(dec_handle* h, const float* emb, float* out) {
   if (e != cudaSuccess) return cuda_fail(h, e, "cudaStreamEndCapture");
   h->graph_g = g;
   TLD_CUDA(h, cudaGraphInstantiate(&h->exec, g, 0));
-  if (h->fused && (!h->first_node || !h->last_node))
+  if ((h->fused && (!h->first_node || !h->last_node)) || (h->token_out && !h->lm_node))
     return fail(h, DEC_ERR_CUDA, "could not locate the captured kernel nodes");
   h->cap_emb = emb;
   h->cap_out = out;
@@ -592,8 +661,27 @@ int capture(dec_handle* h, const float* emb, float* out) {
 
 // The taps a captured launch of kernel k (0 QKV, 4 down) of layer l carries.
 // Points the captured graph at new input / output buffers.
+int patch_io_layers(dec_handle* h, const float* emb, float* out);
+
 int patch_io(dec_handle* h, const float* emb, float* out) {
   if (!h->fused) return capture(h, emb, out);  // the unfused chain is only the ablation
+  const float* old_out = h->cap_out;
+  const int rc = patch_io_layers(h, emb, out);
+  if (rc || !h->lm_node || out == old_out) return rc;
+  // the LM head reads the stack's output
+  LmHeadParams P = lm_params(h, out);
+  void* args[] = {&P};
+  cudaKernelNodeParams kp{};
+  kp.func = const_cast<void*>(lm_head_kernel_ptr());
+  kp.gridDim = dim3(h->n_sm);
+  kp.blockDim = dim3(kThreads);
+  kp.sharedMemBytes = (unsigned)h->lm.smem;
+  kp.kernelParams = args;
+  TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->lm_node, &kp));
+  return DEC_OK;
+}
+
+int patch_io_layers(dec_handle* h, const float* emb, float* out) {
   if (h->persistent) {
     if (emb == h->cap_emb && out == h->cap_out) return DEC_OK;
     TokenParams P = token_params(h, emb, out);
@@ -690,7 +778,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       (d.hidden % 64 || d.ffn % 64 || (d.n_q_heads * d.head_dim) % 64))
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
-                  DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS))
+                  DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS | DEC_ROPE_INTERLEAVED |
+                  DEC_PAGED_KV))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -705,6 +794,14 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   h->three = h->fused && !h->persistent && (d.flags & DEC_PLAN_THREE);
   h->guards = (d.flags & DEC_DEBUG_GUARDS) != 0;
+  h->rope_inter = (d.flags & DEC_ROPE_INTERLEAVED) != 0;
+  h->paged = (d.flags & DEC_PAGED_KV) != 0;
+  if (h->paged && !h->fused) {
+    delete h;
+    return fail(nullptr, DEC_ERR_SHAPE, "the paged KV cache needs a fused plan");
+  }
+  h->page_rows = kAttnStageBytes / 4 / d.head_dim;  // one attention chunk
+  h->n_pages = (d.max_ctx + h->page_rows - 1) / h->page_rows;
   if (h->three) h->cluster_attn = false;  // its attention phase is a flat grid
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -747,8 +844,10 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
         }
       }
     }
-    A(&L.kc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
-    A(&L.vc, 2 * (size_t)nkv * d.max_ctx * hd, &h->kv_bytes);
+    const size_t kv_elems = h->paged ? (size_t)h->n_pages * nkv * h->page_rows * hd
+                                     : (size_t)nkv * d.max_ctx * hd;
+    A(&L.kc, 2 * kv_elems, &h->kv_bytes);
+    A(&L.vc, 2 * kv_elems, &h->kv_bytes);
   }
   const int km = max_k(d);
   A(&h->X, 4 * (size_t)H, &h->ws_bytes);
@@ -771,6 +870,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     A(&h->d_bar, 16, &h->ws_bytes);
   }
   if (h->three) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
+  if (h->paged) A(&h->d_pages, sizeof(int) * (size_t)h->n_pages, &h->ws_bytes);
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
   A(&h->rope, sizeof(float2) * (size_t)d.max_ctx * (hd / 2), &h->ws_bytes);
@@ -794,6 +894,12 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess && h->three) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
+  if (e == cudaSuccess && h->paged) {  // identity page table until the caller sets one
+    h->h_pages.resize(h->n_pages);
+    for (int c = 0; c < h->n_pages; ++c) h->h_pages[c] = c;
+    e = cudaMemcpy(h->d_pages, h->h_pages.data(), sizeof(int) * h->h_pages.size(),
+                   cudaMemcpyHostToDevice);
+  }
   if (e == cudaSuccess && h->persistent) {
     std::vector<PLayer> pl(d.n_layers);
     for (int l = 0; l < d.n_layers; ++l) {
@@ -940,8 +1046,10 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
   uint8_t* dst = nullptr;
   int row0 = 0, kind = 0;
   switch (mt) {
-    case DEC_T_WQ: dst = L.qkv.w; row0 = 0; kind = 1; break;
-    case DEC_T_WK: dst = L.qkv.w; row0 = d.n_q_heads * hd; kind = 1; break;
+    // q/k rows: a RoPE pair's two rows adjacent (pairs (i, i+hd/2) interleaved;
+    // pairs (2i, 2i+1) already are)
+    case DEC_T_WQ: dst = L.qkv.w; row0 = 0; kind = h->rope_inter ? 0 : 1; break;
+    case DEC_T_WK: dst = L.qkv.w; row0 = d.n_q_heads * hd; kind = h->rope_inter ? 0 : 1; break;
     case DEC_T_WV: dst = L.qkv.w; row0 = (d.n_q_heads + d.n_kv_heads) * hd; kind = 0; break;
     case DEC_T_WO: dst = L.o.w; row0 = 0; kind = 0; break;
     case DEC_T_WGATE: dst = L.gu.w; row0 = 0; kind = 2; break;
@@ -972,19 +1080,111 @@ int dec_load_kv(dec_handle* h, int layer, const void* k_bf16, const void* v_bf16
   TLD_CUDA(h, cudaDeviceSynchronize());
   LayerDev& L = h->layers[layer];
   if (n_pos > 0) {
-    const size_t row = 2 * (size_t)n_pos * d.head_dim, pitch = 2 * (size_t)d.max_ctx * d.head_dim;
-    TLD_CUDA(h, cudaMemcpy2D(L.kc, pitch, k_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
-    TLD_CUDA(h, cudaMemcpy2D(L.vc, pitch, v_bf16, row, row, d.n_kv_heads, cudaMemcpyDefault));
+    const int hd = d.head_dim;
+    int rc = for_kv_runs(h, 0, n_pos, [&](int64_t off, int rows, int64_t src_row) -> int {
+      const size_t n = 2 * (size_t)rows * hd;
+      const size_t so = 2 * (size_t)src_row * hd;
+      TLD_CUDA(h, cudaMemcpy(L.kc + off, static_cast<const uint8_t*>(k_bf16) + so, n, cudaMemcpyDefault));
+      TLD_CUDA(h, cudaMemcpy(L.vc + off, static_cast<const uint8_t*>(v_bf16) + so, n, cudaMemcpyDefault));
+      return DEC_OK;
+    });
+    if (rc) return rc;
   }
   if (h->guards && n_pos < d.max_ctx) {  // rows past the new length hold poison again
-    const size_t pitch = 2 * (size_t)d.max_ctx * d.head_dim, row = 2 * (size_t)d.head_dim;
-    for (uint16_t* c : {L.kc, L.vc})
-      TLD_CUDA(h, cudaMemset2D(c + (size_t)n_pos * d.head_dim, pitch, 0xFF,
-                               row * (d.max_ctx - n_pos), d.n_kv_heads));
+    int rc = for_kv_runs(h, n_pos, d.max_ctx, [&](int64_t off, int rows, int64_t) -> int {
+      for (uint16_t* c : {L.kc, L.vc})
+        TLD_CUDA(h, cudaMemset(c + off, 0xFF, 2 * (size_t)rows * d.head_dim));
+      return DEC_OK;
+    });
+    if (rc) return rc;
   }
   L.kv_len = n_pos;
   h->kv_len = n_pos;
   return set_device_pos(h, n_pos);
+}
+
+int dec_load_lm_head(dec_handle* h, const void* final_norm_bf16, const void* w_bf16, int vocab) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!final_norm_bf16 || !w_bf16) return fail(h, DEC_ERR_ARG, "final norm or LM head weights NULL");
+  if (vocab < kTileR || vocab % kTileR)
+    return fail(h, DEC_ERR_SHAPE, "vocab %d: a positive multiple of %d", vocab, kTileR);
+  if (h->lm_loaded && vocab != h->vocab)
+    return fail(h, DEC_ERR_ARG, "vocab %d differs from the loaded %d", vocab, h->vocab);
+  const int H = h->d.hidden;
+  if (!h->lm_loaded) {
+    plan_tiled(h->lm, vocab, H, h->n_sm, false);
+    int rc = dev_alloc(h, &h->lm.w, h->lm.bytes, &h->weight_bytes);
+    if (!rc) rc = dev_alloc(h, &h->lm_norm, 2 * (size_t)H, &h->weight_bytes);
+    if (!rc) rc = dev_alloc(h, &h->logits, 4 * (size_t)vocab, &h->ws_bytes);
+    if (!rc) rc = dev_alloc(h, &h->lm_key, 16, &h->ws_bytes);
+    if (rc) return rc;
+    TLD_CUDA(h, cudaMemset(h->lm_key, 0, 16));
+    h->vocab = vocab;
+  }
+  const size_t want = 2 * (size_t)vocab * H;
+  if (h->staging_bytes < want) {
+    if (h->staging) {
+      uint8_t* user = reinterpret_cast<uint8_t*>(h->staging);
+      void* base = h->guards ? user - kGuardBytes : user;
+      cudaFree(base);
+      for (auto& p : h->allocs)
+        if (p == base) p = nullptr;
+      for (auto& g : h->guard_list)
+        if (g.user == user) g.bytes = 0;
+    }
+    h->staging = nullptr;
+    h->staging_bytes = 0;
+    int rc = dev_alloc(h, &h->staging, want, nullptr);
+    if (rc) return rc;
+    h->staging_bytes = want;
+  }
+  TLD_CUDA(h, cudaMemcpy(h->lm_norm, final_norm_bf16, 2 * (size_t)H, cudaMemcpyDefault));
+  TLD_CUDA(h, cudaMemcpy(h->staging, w_bf16, want, cudaMemcpyDefault));
+  cudaError_t e = launch_repack_bf16(h->staging, vocab, H, h->lm.w, 0, 0, h->d.head_dim, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e, "LM head repack");
+  h->lm_loaded = true;
+  drop_graph(h);
+  return DEC_OK;
+}
+
+int dec_set_token_out(dec_handle* h, int32_t* token_out, float* logits_tap) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (token_out && !h->lm_loaded) return fail(h, DEC_ERR_STATE, "no LM head loaded (dec_load_lm_head)");
+  if (logits_tap && !token_out) return fail(h, DEC_ERR_ARG, "a logits tap needs token_out");
+  h->token_out = token_out;
+  h->logits_tap = logits_tap;
+  drop_graph(h);
+  return DEC_OK;
+}
+
+int dec_set_page_table(dec_handle* h, const int32_t* pages, int n) {
+  if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
+  if (!h->paged) return fail(h, DEC_ERR_STATE, "the handle was created without DEC_PAGED_KV");
+  if (!pages || n != h->n_pages)
+    return fail(h, DEC_ERR_ARG, "the page table has %d entries, expected %d", n, h->n_pages);
+  std::vector<int> t(n), seen(n, 0);
+  TLD_CUDA(h, cudaMemcpy(t.data(), pages, sizeof(int) * (size_t)n, cudaMemcpyDefault));
+  for (int c = 0; c < n; ++c) {
+    if (t[c] < 0 || t[c] >= n || seen[t[c]]++)
+      return fail(h, DEC_ERR_ARG, "page table entry %d (%d) out of range or repeated", c, t[c]);
+  }
+  // the rows already in the cache move with their pages
+  TLD_CUDA(h, cudaDeviceSynchronize());
+  const dec_model_desc& d = h->d;
+  const size_t page_elems = (size_t)d.n_kv_heads * h->page_rows * d.head_dim;
+  const size_t page_bytes = 2 * page_elems;
+  std::vector<uint8_t> tmp(page_bytes * (size_t)n);
+  for (LayerDev& L : h->layers)
+    for (uint16_t* c : {L.kc, L.vc}) {
+      TLD_CUDA(h, cudaMemcpy(tmp.data(), c, tmp.size(), cudaMemcpyDeviceToHost));
+      for (int ch = 0; ch < n; ++ch)
+        TLD_CUDA(h, cudaMemcpy(c + (size_t)t[ch] * page_elems, tmp.data() + (size_t)h->h_pages[ch] * page_bytes,
+                               page_bytes, cudaMemcpyHostToDevice));
+    }
+  h->h_pages = t;
+  TLD_CUDA(h, cudaMemcpy(h->d_pages, t.data(), sizeof(int) * (size_t)n, cudaMemcpyHostToDevice));
+  return DEC_OK;
 }
 
 int dec_read_kv(dec_handle* h, int layer, void* k_bf16, void* v_bf16, int first_pos, int n_pos) {
@@ -998,11 +1198,13 @@ int dec_read_kv(dec_handle* h, int layer, void* k_bf16, void* v_bf16, int first_
   TLD_CUDA(h, cudaDeviceSynchronize());
   if (n_pos == 0) return DEC_OK;
   const LayerDev& L = h->layers[layer];
-  const size_t row = 2 * (size_t)n_pos * d.head_dim, pitch = 2 * (size_t)d.max_ctx * d.head_dim;
-  const size_t off = (size_t)first_pos * d.head_dim;
-  TLD_CUDA(h, cudaMemcpy2D(k_bf16, row, L.kc + off, pitch, row, d.n_kv_heads, cudaMemcpyDefault));
-  TLD_CUDA(h, cudaMemcpy2D(v_bf16, row, L.vc + off, pitch, row, d.n_kv_heads, cudaMemcpyDefault));
-  return DEC_OK;
+  return for_kv_runs(h, first_pos, first_pos + n_pos, [&](int64_t off, int rows, int64_t dst_row) -> int {
+    const size_t n = 2 * (size_t)rows * d.head_dim;
+    const size_t so = 2 * (size_t)dst_row * d.head_dim;
+    TLD_CUDA(h, cudaMemcpy(static_cast<uint8_t*>(k_bf16) + so, L.kc + off, n, cudaMemcpyDefault));
+    TLD_CUDA(h, cudaMemcpy(static_cast<uint8_t*>(v_bf16) + so, L.vc + off, n, cudaMemcpyDefault));
+    return DEC_OK;
+  });
 }
 
 int dec_truncate_kv(dec_handle* h, int n_pos) {
@@ -1014,10 +1216,12 @@ int dec_truncate_kv(dec_handle* h, int n_pos) {
   const dec_model_desc& d = h->d;
   for (LayerDev& L : h->layers) {
     if (h->guards && n_pos < d.max_ctx) {  // rows past the new length hold poison again
-      const size_t pitch = 2 * (size_t)d.max_ctx * d.head_dim, row = 2 * (size_t)d.head_dim;
-      for (uint16_t* c : {L.kc, L.vc})
-        TLD_CUDA(h, cudaMemset2D(c + (size_t)n_pos * d.head_dim, pitch, 0xFF,
-                                 row * (d.max_ctx - n_pos), d.n_kv_heads));
+      int rc = for_kv_runs(h, n_pos, d.max_ctx, [&](int64_t off, int rows, int64_t) -> int {
+        for (uint16_t* c : {L.kc, L.vc})
+          TLD_CUDA(h, cudaMemset(c + off, 0xFF, 2 * (size_t)rows * d.head_dim));
+        return DEC_OK;
+      });
+      if (rc) return rc;
     }
     L.kv_len = n_pos;
   }
@@ -1139,18 +1343,22 @@ int dec_check_guards(dec_handle* h) {
   const size_t row = 2 * (size_t)d.head_dim;
   for (int l = 0; l < d.n_layers; ++l) {
     const LayerDev& L = h->layers[l];
-    const int n = d.max_ctx - L.kv_len;
-    if (n <= 0) continue;
-    buf.resize(row * n);
-    for (const uint16_t* c : {L.kc, L.vc})
-      for (int g = 0; g < d.n_kv_heads; ++g) {
-        TLD_CUDA(h, cudaMemcpy(buf.data(), c + ((size_t)g * d.max_ctx + L.kv_len) * d.head_dim,
-                               row * n, cudaMemcpyDeviceToHost));
+    if (L.kv_len >= d.max_ctx) continue;
+    int rc = for_kv_runs(h, L.kv_len, d.max_ctx, [&](int64_t off, int rows, int64_t src_row) -> int {
+      buf.resize(row * rows);
+      for (const uint16_t* c : {L.kc, L.vc}) {
+        TLD_CUDA(h, cudaMemcpy(buf.data(), c + off, row * rows, cudaMemcpyDeviceToHost));
         for (size_t j = 0; j < buf.size(); ++j)
-          if (buf[j] != 0xFF)
+          if (buf[j] != 0xFF) {
+            const int g = (int)(src_row / (d.max_ctx - L.kv_len));
+            const int t = L.kv_len + (int)(src_row % (d.max_ctx - L.kv_len)) + (int)(j / row);
             return fail(h, DEC_ERR_DEVICE, "layer %d KV head %d: row %d past the KV length %d written",
-                        l, g, L.kv_len + (int)(j / row), L.kv_len);
+                        l, g, t, L.kv_len);
+          }
       }
+      return DEC_OK;
+    });
+    if (rc) return rc;
   }
   return DEC_OK;
 }
@@ -1168,6 +1376,8 @@ int dec_get_info(const dec_handle* h, dec_info* info) {
   info->workspace_bytes = h->ws_bytes;
   info->attn_grid = h->fused && !h->persistent ? fused_att_grid(h) : h->att_grid;
   info->attn_cluster = h->fused && !h->persistent ? h->att_cluster : 0;
+  info->page_rows = h->paged ? h->page_rows : 0;
+  info->n_pages = h->paged ? h->n_pages : 0;
   return DEC_OK;
 }
 

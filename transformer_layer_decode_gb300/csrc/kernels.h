@@ -32,8 +32,19 @@ __host__ __device__ inline int split_owner(int64_t total, int parts, int64_t u) 
 constexpr int kTileR = 4;
 constexpr int kTileK = 256;
 constexpr int kTileKQ4 = 1024;
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // 8 consumer warps + 1 producer warp
+// Consumer warps of the GEMV kernels and of the fused phase kernels: one tile of
+// each 16-tile stage per warp.  Sixteen keep enough warps in flight to hide the
+// latency of the per-stage arithmetic (measured: 8 warps streamed the 7B-shape
+// gate/up matrix at 5.4 TB/s, 16 at 5.9 TB/s, 4 at 4.3 TB/s).
+#ifndef TLD_CONSUMER_WARPS
+#define TLD_CONSUMER_WARPS 16
+#endif
+constexpr int kConsumerWarps = TLD_CONSUMER_WARPS;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // consumer warps + 1 producer warp
+// Consumer warps of the standalone attention kernels, except the cluster
+// kernels of GQA groups up to 2, which run 16 (larger groups need the register
+// budget of 8 warps).
+constexpr int kAttnWarps = 8;
 // Shared memory budget per CTA.  Above half of the SM's 228 KB, so two CTAs of
 // one kernel never share an SM; the next kernel (programmatic dependent launch)
 // then takes each SM as soon as its current CTA leaves and starts streaming.
@@ -51,8 +62,9 @@ constexpr int kMaxSplits = 32;
 constexpr int kCopiesPerStage = TLD_COPIES_PER_STAGE;  // bulk copies a GEMV stage is issued as
 constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
 constexpr int kMaxCluster = 16;            // CTAs per KV head in the cluster attention
-constexpr int kStageTiles = 2 * kConsumerWarps;  // two tiles per consumer warp per stage
+constexpr int kStageTiles = 16;  // a GEMV stage: 16 tiles (32 KB bf16, 36 KB int4)
 constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
+static_assert(kStageTiles % kConsumerWarps == 0, "every consumer warp takes whole tiles of a stage");
 constexpr int kTileBytes = kTileR * kTileK * 2;                          // 2 KB
 constexpr int kTileBytesQ4 = kTileR * (kTileKQ4 / 2 + kTileKQ4 / 16);    // 2304 B
 constexpr int kStageBytes = kStageTiles * kTileBytes;                    // 32 KB
@@ -109,6 +121,19 @@ __host__ __device__ inline int64_t q4_scale_byte(int64_t r, int64_t b, int K) {
          ((b - kt * (kTileKQ4 / 32)) * kTileR + (r % kTileR)) * 2;
 }
 
+// ---- KV cache geometry ---------------------------------------------------------
+// Contiguous: a layer's K (or V) cache is [nkv][max_ctx][hd].  Paged: it is a
+// pool of pages [page][nkv][page_rows][hd] and a page table maps the chunk of
+// positions [c * page_rows, (c + 1) * page_rows) to page pages[c] (the same
+// table for every layer).  A page holds one attention chunk of one KV head, so
+// an attention stage is one contiguous copy either way.
+__host__ __device__ inline int64_t kv_row_offset(const int* pages, int page_rows, int nkv,
+                                                 int max_ctx, int hd, int g, int t) {
+  if (!pages) return ((int64_t)g * max_ctx + t) * hd;
+  const int c = t / page_rows;
+  return (((int64_t)pages[c] * nkv + g) * page_rows + (t - c * page_rows)) * hd;
+}
+
 // The next kernel's share of the bytes of one CTA index, fetched into L2 by
 // that CTA's producer once its own stream is issued: HBM keeps streaming
 // through the tail of a kernel (its last stages, epilogue, merge), when the
@@ -123,10 +148,11 @@ struct L2Ahead {
   int kv, nkv, hd, max_ctx;
   const int* pos;
   int cluster;  // attention next: its cluster size (0: global-merge grid)
+  const int* pages;  // paged KV cache: page table (null: contiguous)
 };
 
 enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
-enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2 };
+enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
 struct GemvParams {
   const uint8_t* w;  // tiled weights
@@ -140,11 +166,13 @@ struct GemvParams {
   int* err;
   // EPI_QKV: rows are q (pair-interleaved per head), k (same), v
   int nq, nkv, hd, max_ctx;
+  int rope_inter;       // RoPE pairs (2i, 2i+1) (rows in ABI order) instead of (i, i+hd/2)
   const int* pos;       // device step position
   const float2* rope;   // [max_ctx][hd/2] (cos, sin)
   float* q_out;         // [nq*hd]
-  uint16_t* kc;         // layer cache [nkv][max_ctx][hd]
+  uint16_t* kc;         // layer cache (kv_row_offset)
   uint16_t* vc;
+  const int* pages;     // paged KV cache: page table (null: contiguous [nkv][max_ctx][hd])
   // EPI_RESID
   const float* resid;
   float* out;
@@ -161,8 +189,9 @@ struct GemvParams {
 };
 
 struct AttnParams {
-  const uint16_t* kc;  // layer cache [nkv][max_ctx][hd]
+  const uint16_t* kc;  // layer cache (kv_row_offset)
   const uint16_t* vc;
+  const int* pages;    // paged KV cache: page table (null: contiguous [nkv][max_ctx][hd])
   const float* q;      // [nq*hd] rotated
   float* o;            // [nq*hd]
   float* part;         // [grid][2][G][hd+4]: (acc, m, l) of split heads
@@ -198,6 +227,16 @@ struct FfnParams {  // norm + gate/up + SwiGLU, then down + residual
   int nstages, slot_bytes;
   uint64_t* tl2;          // timeline row of the down phase or null
 };
+
+// The LM head after the stack: final RMSNorm x weight + vocabulary GEMV
+// (PRO_NORM, EPI_LOGITS: rows to g.out) and the greedy token.
+struct LmHeadParams {
+  GemvParams g;
+  unsigned long long* key;  // [2]: best key of the running launch, CTA ticket (both zero between launches)
+  int* token_out;           // device int32: the chosen row
+};
+cudaError_t launch_lm_head(const LmHeadParams& p, int grid, size_t smem, cudaStream_t s, bool pdl);
+const void* lm_head_kernel_ptr();
 
 size_t attn_oproj_smem_bytes(int hd, int G, int K_o, int max_rb_o, bool q4, int nstages,
                              int slot_bytes);
@@ -272,8 +311,11 @@ int noalloc_sync_status(cudaStream_t stream, int* flag_out);
 
 // Load-time repack of a row-major [rows][K] bf16 block into the tiled layout
 // of a matrix with K columns, source row s going to tiled row map(s):
-//   map = dst_row0 + s                                  (kind 0, plain)
-//   q/k heads: dst_row0 + rope pair interleave          (kind 1)
+//   map = dst_row0 + s                                  (kind 0, plain; also
+//                                                        q/k rows whose RoPE
+//                                                        pairs are (2i, 2i+1))
+//   q/k heads: dst_row0 + rope pair interleave          (kind 1: pairs (i, i+hd/2)
+//                                                        made adjacent)
 //   gate/up:   dst_row0 + 2*s (+1 for up via dst_row0)  (kind 2)
 cudaError_t launch_repack_bf16(const uint16_t* src, int rows, int K, uint8_t* dst_tiled,
                                int dst_row0, int kind, int hd, cudaStream_t s);
@@ -288,7 +330,7 @@ cudaError_t rms_scale(const float* x, int H, float eps, float* n, cudaStream_t s
 cudaError_t mul(float* n, const uint16_t* w, int H, cudaStream_t s);
 cudaError_t gemv(const uint16_t* W, int N, int K, const float* x, float* y, cudaStream_t s);
 cudaError_t rope(float* q, float* k, int nq, int nkv, int hd, const int* pos, const float2* tab,
-                 cudaStream_t s);
+                 int interleaved, cudaStream_t s);
 cudaError_t kv_append(const float* k, const float* v, int nkv, int hd, int max_ctx, const int* pos,
                       uint16_t* kc, uint16_t* vc, cudaStream_t s);
 cudaError_t attention(const float* q, const uint16_t* kc, const uint16_t* vc, int nq, int nkv,

@@ -36,7 +36,7 @@ size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
 
 // Consumer warps of the attention kernel: 16 for the cluster kernels of GQA
 // groups up to 2 (their registers allow 17 warps a CTA), else 8.
-int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 2 ? 16 : kConsumerWarps; }
+int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 2 ? 16 : kAttnWarps; }
 
 size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster) {
   return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages +
@@ -143,6 +143,82 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams
   }
   if (!ok && tid == 0) ring_drain(R, P, p.err);
 }
+
+// ---- the LM head and the greedy token ------------------------------------------
+// Order-preserving key of a logit at row j: the float's bits mapped so that
+// unsigned order is float order, and the row's complement below them, so the
+// largest key is the largest logit at its lowest row.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int j) {
+  const uint32_t u = __float_as_uint(v);
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (uint32_t)~(uint32_t)j;
+}
+
+// Final RMSNorm x weight and the vocabulary GEMV (logits to p.g.out), then the
+// greedy token: each CTA reduces its own rows' logits to one key, takes the
+// maximum with the global key, and the last CTA to finish (a ticket) writes
+// the token and clears the key and the ticket for the next launch.  The
+// maximum does not depend on the order of arrival, so the token is the same
+// every run.
+__global__ void __launch_bounds__(kThreads, 1) lm_head_argmax(const LmHeadParams P) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const GemvParams& p = P.g;
+  const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.geo.stage_bytes),
+               reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * p.geo.stage_bytes) + p.nstages,
+               p.nstages, p.geo.stage_bytes};
+  uint8_t* work = smem + (size_t)p.nstages * p.geo.stage_bytes + 16 * (size_t)p.nstages;
+  const GemvWork W(work, GemvLayout{p.geo.K, p.max_rb_local, false});
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = gridDim.x, b = blockIdx.x;
+  const int rb0 = (int)split_begin(p.n_rb, nb, b), rb1 = (int)split_begin(p.n_rb, nb, b + 1);
+  if (tid == 0) ring_init(R);
+  __syncthreads();
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      RingPos Pp{0, 0, 0};
+      gemv_produce(p, p.w, R, Pp, rb0, rb1, policy_evict_first());
+    }
+    return;
+  }
+  gemv_pre<PRO_NORM>(p, p.norm_w, W, tid);
+  pdl_wait();  // the stack's output comes from the last layer
+  pdl_trigger();
+  RingPos Pp{0, 0, 0};
+  const bool ok = gemv_main<PRO_NORM, EPI_LOGITS, false>(p, gemv_io(p), W, R, Pp, rb0, rb1, tid, b == 0);
+  if (!ok) {
+    if (tid == 0) ring_drain(R, Pp, p.err);
+    return;
+  }
+  named_barrier(1, kNC);  // this CTA's logits are written
+  unsigned long long best = 0;
+  for (int r = rb0 * kTileR + tid; r < rb1 * kTileR; r += kNC) {
+    const unsigned long long k = argmax_key(__ldcg(p.out + r), r);
+    best = k > best ? k : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long k = __shfl_xor_sync(0xffffffffu, best, o);
+    best = k > best ? k : best;
+  }
+  unsigned long long* red = reinterpret_cast<unsigned long long*>(W.part);
+  if (lane == 0) red[warp] = best;
+  named_barrier(1, kNC);
+  if (tid == 0) {
+    for (int w = 1; w < kConsumerWarps; ++w) best = red[w] > best ? red[w] : best;
+    atomicMax(P.key, best);
+    // release this CTA's maximum, acquire the others'
+    unsigned long long t;
+    asm volatile("atom.add.acq_rel.gpu.u64 %0, [%1], 1;" : "=l"(t) : "l"(P.key + 1) : "memory");
+    if (t == (unsigned long long)(nb - 1)) {
+      const unsigned long long k = atomicMax(P.key, 0ull);
+      *P.token_out = (int)~(uint32_t)(k & 0xffffffffu);
+      P.key[0] = 0;
+      P.key[1] = 0;
+    }
+  }
+}
+
+const void* lm_head_kernel_ptr() { return (const void*)lm_head_argmax; }
 
 // ---- two-phase kernels (the three-kernel layer) -------------------------------
 // Shared memory: ring (nstages x slot_bytes) | mbarriers | one work area that
@@ -328,8 +404,8 @@ const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
 const void* attn_kernel_ptr(int hd, int G, bool cluster) {
 #define TLD_ATTN(H_, G_)                                                                       \
   if (hd == H_ && G == G_)                                                                    \
-    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 2 ? 16 : kConsumerWarps)>  \
-                   : (const void*)attn_decode<H_, G_, false, kConsumerWarps>;
+    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 2 ? 16 : kAttnWarps)>  \
+                   : (const void*)attn_decode<H_, G_, false, kAttnWarps>;
   TLD_ATTN(64, 1) TLD_ATTN(64, 2) TLD_ATTN(64, 4) TLD_ATTN(64, 8)
   TLD_ATTN(128, 1) TLD_ATTN(128, 2) TLD_ATTN(128, 4) TLD_ATTN(128, 8)
 #undef TLD_ATTN
@@ -346,6 +422,11 @@ cudaError_t set_smem_limits() {
                       gemv_kernel_ptr(PRO_NORM, EPI_SWIGLU, true)};
   for (const void* k : ks) {
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+    if (e != cudaSuccess) return e;
+  }
+  {
+    cudaError_t e = cudaFuncSetAttribute(lm_head_kernel_ptr(),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
     if (e != cudaSuccess) return e;
   }
   for (bool q4 : {false, true}) {
@@ -416,6 +497,12 @@ cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t sme
   void* args[] = {&copy};
   return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster,
                     (attn_consumer_warps(G, p.cluster > 0) + 1) * 32);
+}
+
+cudaError_t launch_lm_head(const LmHeadParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {
+  LmHeadParams copy = p;
+  void* args[] = {&copy};
+  return launch_pdl((const void*)lm_head_argmax, args, grid, smem, s, pdl);
 }
 
 cudaError_t launch_attn_oproj(int hd, int G, bool q4, const AttnOprojParams& p, int grid,

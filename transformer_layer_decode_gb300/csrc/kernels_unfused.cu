@@ -60,7 +60,8 @@ __global__ void gemv_kernel(const uint16_t* __restrict__ W, int N, int K,
 
 // RoPE on q (nq heads) and k (nkv heads) in place, rotate-half pairs.
 __global__ void rope_kernel(float* __restrict__ q, float* __restrict__ k, int nq, int nkv, int hd,
-                            const int* __restrict__ pos, const float2* __restrict__ tab) {
+                            const int* __restrict__ pos, const float2* __restrict__ tab,
+                            int interleaved) {
   const int half = hd / 2;
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   const int total = (nq + nkv) * half;
@@ -68,9 +69,11 @@ __global__ void rope_kernel(float* __restrict__ q, float* __restrict__ k, int nq
   const int head = idx / half, i = idx % half;
   float* v = head < nq ? q + (size_t)head * hd : k + (size_t)(head - nq) * hd;
   const float2 c = tab[(size_t)(*pos) * half + i];
-  const float a = v[i], b = v[i + half];
-  v[i] = a * c.x - b * c.y;
-  v[i + half] = a * c.y + b * c.x;
+  // pair i: dims (i, i + hd/2), or (2i, 2i + 1) when interleaved
+  const int e = interleaved ? 2 * i : i, o = interleaved ? 2 * i + 1 : i + half;
+  const float a = v[e], b = v[o];
+  v[e] = a * c.x - b * c.y;
+  v[o] = a * c.y + b * c.x;
 }
 
 // KV append: row pos of every KV head <- bf16(k), bf16(v).
@@ -237,8 +240,9 @@ cudaError_t gemv(const uint16_t* W, int N, int K, const float* x, float* y, cuda
   return cudaGetLastError();
 }
 cudaError_t rope(float* q, float* k, int nq, int nkv, int hd, const int* pos, const float2* tab,
+                 int interleaved,
                  cudaStream_t s) {
-  rope_kernel<<<cdiv((nq + nkv) * hd / 2, 256), 256, 0, s>>>(q, k, nq, nkv, hd, pos, tab);
+  rope_kernel<<<cdiv((nq + nkv) * hd / 2, 256), 256, 0, s>>>(q, k, nq, nkv, hd, pos, tab, interleaved);
   return cudaGetLastError();
 }
 cudaError_t kv_append(const float* k, const float* v, int nkv, int hd, int max_ctx, const int* pos,

@@ -128,7 +128,7 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO&
     if (!TLD_IN_BOUNDS(pos >= 0 && pos < p.max_ctx && R0 + kTileR <= qrows + 2 * krows, p.err))
       return;
     if (R0 < qrows + krows) {
-      // rows (2i, 2i+1) of a head hold dims i and i + hd/2: rotate the pair
+      // rows (2i, 2i+1) of a head hold the two dims of RoPE pair i: rotate the pair
       const bool is_q = R0 < qrows;
       const int local = is_q ? R0 : R0 - qrows;
       const int head = local / hd, i0 = (local % hd) / 2;
@@ -140,19 +140,21 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO&
         const float2 c = cs[i];
         const float ra = a * c.x - b * c.y;
         const float rb2 = a * c.y + b * c.x;
+        // pair i holds dims (i, i + hd/2), or (2i, 2i + 1) with interleaved pairs
+        const int e = p.rope_inter ? 2 * i : i, o = p.rope_inter ? 2 * i + 1 : i + half;
         if (is_q) {
-          p.q_out[head * hd + i] = ra;
-          p.q_out[head * hd + i + half] = rb2;
+          p.q_out[head * hd + e] = ra;
+          p.q_out[head * hd + o] = rb2;
         } else {
-          uint16_t* row = io.kc + ((size_t)head * p.max_ctx + pos) * hd;
-          row[i] = f32_to_bf16_bits(ra);
-          row[i + half] = f32_to_bf16_bits(rb2);
+          uint16_t* row = io.kc + kv_row_offset(p.pages, kAttnStageBytes / 4 / hd, p.nkv, p.max_ctx, hd, head, pos);
+          row[e] = f32_to_bf16_bits(ra);
+          row[o] = f32_to_bf16_bits(rb2);
         }
       }
     } else {
       const int local = R0 - qrows - krows;
       const int head = local / hd, j = local % hd;
-      uint16_t* row = io.vc + ((size_t)head * p.max_ctx + pos) * hd;
+      uint16_t* row = io.vc + kv_row_offset(p.pages, kAttnStageBytes / 4 / hd, p.nkv, p.max_ctx, hd, head, pos);
 #pragma unroll
       for (int r = 0; r < kTileR; ++r) row[j + r] = f32_to_bf16_bits(v[r]);
     }
@@ -163,6 +165,9 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO&
       io.out[R0 + r] = y;
       if (io.tap) io.tap[R0 + r] = y;
     }
+  } else if (EPI == EPI_LOGITS) {
+#pragma unroll
+    for (int r = 0; r < kTileR; ++r) io.out[R0 + r] = v[r];
   } else {  // EPI_SWIGLU: tiled rows alternate gate and up of the same output
     const int j = R0 / 2;
 #pragma unroll
@@ -475,6 +480,11 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   float acc[kTileR];
 #pragma unroll
   for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
+#ifdef TLD_F32X2
+  uint64_t acc2[kTileR];
+#pragma unroll
+  for (int r = 0; r < kTileR; ++r) acc2[r] = 0ull;
+#endif
   bool ok = true;
   // cursors: the first tile of the current stage and this warp's two tiles in it
   TileCursor st_cur{rb0, 0};
@@ -527,6 +537,13 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
       if (li >= nloc) continue;
       const int rb = my[j].rb, kt = my[j].kt;
       if (rb != cur_rb) {
+#ifdef TLD_F32X2
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) {
+          acc[r] += unpack_f32x2_sum(acc2[r]);
+          acc2[r] = 0ull;
+        }
+#endif
         if (cur_rb >= 0) {
           const float v = warp_reduce4(acc, lane);
           if ((lane & 7) == 0)
@@ -556,6 +573,18 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
       } else {
         const float4 xa = *reinterpret_cast<const float4*>(xs + kt * kTileK + c);
         const float4 xb = *reinterpret_cast<const float4*>(xs + kt * kTileK + c + 4);
+#ifdef TLD_F32X2
+#pragma unroll
+        for (int r = 0; r < kTileR; ++r) {
+          // even and odd columns in the two halves of a packed fp32 pair
+          uint64_t a2 = acc2[r];
+          a2 = fma_f32x2(bf16pair(wv[j][r].x), pack_f32x2(xa.x, xa.y), a2);
+          a2 = fma_f32x2(bf16pair(wv[j][r].y), pack_f32x2(xa.z, xa.w), a2);
+          a2 = fma_f32x2(bf16pair(wv[j][r].z), pack_f32x2(xb.x, xb.y), a2);
+          a2 = fma_f32x2(bf16pair(wv[j][r].w), pack_f32x2(xb.z, xb.w), a2);
+          acc2[r] = a2;
+        }
+#else
 #pragma unroll
         for (int r = 0; r < kTileR; ++r) {
           float a = acc[r];
@@ -569,6 +598,7 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
           a = fmaf(bf16hi(wv[j][r].w), xb.w, a);
           acc[r] = a;
         }
+#endif
       }
     }
     st_cur.advance(kStageTiles, geo.ktiles);
@@ -576,6 +606,10 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, geo.ktiles);
     P.next(R.n);
   }
+#ifdef TLD_F32X2
+#pragma unroll
+  for (int r = 0; r < kTileR; ++r) acc[r] += unpack_f32x2_sum(acc2[r]);
+#endif
   if (cur_rb >= 0) {
     const float v = warp_reduce4(acc, lane);
     if ((lane & 7) == 0)
@@ -671,6 +705,22 @@ __device__ void l2_ahead_kv(const L2Ahead& a, int b) {
                                 : attn_split<HD>(*a.pos, a.nkv, b, a.grid);
   int left = a.cap;
   int u = S.u0;
+  if (a.pages) {  // one chunk (page) at a time
+    for (; u < S.u1 && left > 0; ++u) {
+      const int g = u / S.cph, c = u - g * S.cph;
+      const int rows = min(CH, S.n - c * CH);
+      int bytes = rows * HD * 2;
+      if (bytes > left / 2) bytes = left / 2;
+      const size_t off = (size_t)kv_row_offset(a.pages, CH, a.nkv, a.max_ctx, HD, g, c * CH) * 2;
+      const uint32_t n = (uint32_t)bytes & ~15u;
+      if (n) {
+        bulk_prefetch_l2(a.base + off, n);
+        bulk_prefetch_l2(a.vbase + off, n);
+      }
+      left -= 2 * bytes;
+    }
+    return;
+  }
   while (u < S.u1 && left > 0) {
     // one head segment: its chunks are contiguous in K and in V
     const int g = u / S.cph, c0 = u - g * S.cph;
@@ -731,7 +781,7 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
       wait_pos();
       waited = true;
     }
-    const size_t off = ((size_t)g * p.max_ctx + (size_t)c * CH) * HD;
+    const size_t off = (size_t)kv_row_offset(p.pages, CH, p.nkv, p.max_ctx, HD, g, c * CH);
     const uint32_t bytes = (uint32_t)rows * HD * 2;
     mbar_arrive_expect_tx(&R.full[P.slot], 2 * bytes);
     uint8_t* dst = R.slot(P.slot);
@@ -1002,28 +1052,18 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     const int e0 = split_begin32(G * HD, C, r), e1 = split_begin32(G * HD, C, r + 1);
     for (int e = e0 + tid; e < e1; e += NC) {
       const int gg = e / HD, j = e - gg * HD;
-      float mv[kMaxCluster], lv[kMaxCluster], av[kMaxCluster];
-#pragma unroll
-      for (int c2 = 0; c2 < kMaxCluster; ++c2) {
-        mv[c2] = -INFINITY;
-        lv[c2] = 0.f;
-        av[c2] = 0.f;
-        if (c2 < C) {
-          const uint32_t a = dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2);
-          mv[c2] = dsmem_ld(a + 4 * HD);
-          lv[c2] = dsmem_ld(a + 4 * (HD + 1));
-          av[c2] = dsmem_ld(a + 4 * j);
-        }
-      }
+      // two passes over the cluster's records in rank order: the largest
+      // running max, then the rescaled sums (no per-record arrays in registers)
       float M = -INFINITY;
-#pragma unroll
-      for (int c2 = 0; c2 < kMaxCluster; ++c2) M = fmaxf(M, mv[c2]);
+      for (int c2 = 0; c2 < C; ++c2)
+        M = fmaxf(M, dsmem_ld(dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2) + 4 * HD));
       float Lsum = 0.f, o = 0.f;
-#pragma unroll
-      for (int c2 = 0; c2 < kMaxCluster; ++c2) {
-        const float w = (mv[c2] == -INFINITY) ? 0.f : expf(mv[c2] - M);
-        Lsum = fmaf(lv[c2], w, Lsum);
-        o = fmaf(av[c2], w, o);
+      for (int c2 = 0; c2 < C; ++c2) {
+        const uint32_t a = dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2);
+        const float mv = dsmem_ld(a + 4 * HD);
+        const float w = (mv == -INFINITY) ? 0.f : expf(mv - M);
+        Lsum = fmaf(dsmem_ld(a + 4 * (HD + 1)), w, Lsum);
+        o = fmaf(dsmem_ld(a + 4 * j), w, o);
       }
       p.o[(size_t)(gh * G + gg) * HD + j] = o / Lsum;
     }
@@ -1077,29 +1117,22 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     if (g < 0) continue;
     const int gg = e / HD, j = e - gg * HD;
     const int* mb = mbase + i * kMaxSplits;
-    float mv[kMaxSplits], lv[kMaxSplits], av[kMaxSplits];
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp) {
-      mv[sp] = -INFINITY;
-      lv[sp] = 0.f;
-      av[sp] = 0.f;
-      const int off = mb[sp];
-      if (off >= 0) {
-        const float* rec = p.part + off + gg * (HD + 4);
-        mv[sp] = __ldcg(rec + HD);
-        lv[sp] = __ldcg(rec + HD + 1);
-        av[sp] = __ldcg(rec + j);
-      }
-    }
+    // two passes over the head's split records in split order: the largest
+    // running max, then the rescaled sums (no per-split arrays in registers)
     float M = -INFINITY;
-#pragma unroll
-    for (int sp = 0; sp < kMaxSplits; ++sp) M = fmaxf(M, mv[sp]);
-    float Lsum = 0.f, o = 0.f;
-#pragma unroll
     for (int sp = 0; sp < kMaxSplits; ++sp) {
-      const float w = (mv[sp] == -INFINITY) ? 0.f : expf(mv[sp] - M);
-      Lsum = fmaf(lv[sp], w, Lsum);
-      o = fmaf(av[sp], w, o);
+      const int off = mb[sp];
+      if (off >= 0) M = fmaxf(M, __ldcg(p.part + off + gg * (HD + 4) + HD));
+    }
+    float Lsum = 0.f, o = 0.f;
+    for (int sp = 0; sp < kMaxSplits; ++sp) {
+      const int off = mb[sp];
+      if (off < 0) continue;
+      const float* rec = p.part + off + gg * (HD + 4);
+      const float mv = __ldcg(rec + HD);
+      const float w = (mv == -INFINITY) ? 0.f : expf(mv - M);
+      Lsum = fmaf(__ldcg(rec + HD + 1), w, Lsum);
+      o = fmaf(__ldcg(rec + j), w, o);
     }
     p.o[(size_t)(g * G + gg) * HD + j] = o / Lsum;
   }

@@ -23,6 +23,7 @@ DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6
 DEC_W_BF16, DEC_W_Q4B32 = 0, 1
 DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL, DEC_PLAN_PERSISTENT = 0, 1, 2, 4, 8
 DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE, DEC_PLAN_THREE, DEC_DEBUG_GUARDS = 16, 32, 64, 128
+DEC_ROPE_INTERLEAVED, DEC_PAGED_KV = 256, 512
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
@@ -33,6 +34,7 @@ KERNEL_NAMES_THREE = ("norm_qkv_rope_append", "attention_oproj_residual",
                       "norm_gateup_swiglu_down_residual")
 
 EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_read_kv", "dec_truncate_kv", "dec_step",
+            "dec_load_lm_head", "dec_set_token_out", "dec_set_page_table",
             "dec_set_tap", "dec_set_dot_tap", "dec_set_timeline", "dec_sync_status",
             "dec_check_guards", "dec_get_info", "dec_launch_kernel",
             "dec_destroy", "dec_last_error", "dec_attention_noalloc")
@@ -58,7 +60,8 @@ class Info(ctypes.Structure):
                 ("n_sm", ctypes.c_int32), ("kv_len", ctypes.c_int32),
                 ("weight_bytes", ctypes.c_int64), ("kv_bytes", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_int64), ("attn_grid", ctypes.c_int32),
-                ("attn_cluster", ctypes.c_int32)]
+                ("attn_cluster", ctypes.c_int32), ("page_rows", ctypes.c_int32),
+                ("n_pages", ctypes.c_int32)]
 
 
 _libs: dict = {}
@@ -79,6 +82,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dec_load_weights": [vp, i32, i32, vp, sz],
         "dec_load_kv": [vp, i32, vp, vp, i32],
         "dec_read_kv": [vp, i32, vp, vp, i32, i32],
+        "dec_load_lm_head": [vp, vp, vp, i32],
+        "dec_set_token_out": [vp, vp, vp],
+        "dec_set_page_table": [vp, vp, i32],
         "dec_truncate_kv": [vp, i32],
         "dec_step": [vp, vp, i32, vp, vp],
         "dec_set_tap": [vp, vp, vp, vp],
@@ -170,6 +176,7 @@ class Decoder:
     def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True,
                  pdl: bool = True, persistent: bool = False, l2_ahead: bool = True,
                  cluster_attn: bool = True, three: bool = False, guards: bool = False,
+                 rope_interleaved: bool = False, paged_kv: bool = False,
                  lib_path: str | None = None):
         self.lib = load_library(lib_path or LIB_PATH)
         self.shape = shape
@@ -177,7 +184,9 @@ class Decoder:
                  | (0 if pdl else DEC_NO_PDL) | (DEC_PLAN_PERSISTENT if persistent else 0)
                  | (0 if l2_ahead else DEC_NO_L2_AHEAD)
                  | (0 if cluster_attn else DEC_ATTN_GLOBAL_MERGE)
-                 | (DEC_PLAN_THREE if three else 0) | (DEC_DEBUG_GUARDS if guards else 0))
+                 | (DEC_PLAN_THREE if three else 0) | (DEC_DEBUG_GUARDS if guards else 0)
+                 | (DEC_ROPE_INTERLEAVED if rope_interleaved else 0)
+                 | (DEC_PAGED_KV if paged_kv else 0))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
                               shape.max_ctx, shape.weight_fmt, flags)
@@ -197,6 +206,17 @@ class Decoder:
     def load_kv(self, layer: int, k, v, n_pos: int | None = None):
         n = k.shape[1] if n_pos is None else n_pos
         self._check(self.lib.dec_load_kv(self.h, layer, _ptr(k), _ptr(v), n))
+
+    def load_lm_head(self, final_norm, w):
+        """final_norm: bf16 bits [hidden]; w: bf16 bits [vocab][hidden] (host or device)."""
+        self._check(self.lib.dec_load_lm_head(self.h, _ptr(final_norm), _ptr(w), w.shape[0]))
+
+    def set_token_out(self, token_out=None, logits=None):
+        self._check(self.lib.dec_set_token_out(self.h, _ptr(token_out), _ptr(logits)))
+
+    def set_page_table(self, pages):
+        pages = np.ascontiguousarray(pages, dtype=np.int32)
+        self._check(self.lib.dec_set_page_table(self.h, _ptr(pages), pages.size))
 
     def read_kv(self, layer: int, first_pos: int, n_pos: int):
         """Rows [first_pos, first_pos + n_pos) of one layer's cache: (K, V) bf16

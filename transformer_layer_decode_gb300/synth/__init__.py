@@ -25,6 +25,7 @@ _SO = os.path.join(_BUILD, "libsynth.so")
 # tensor ids of the generator key (weights use the ABI's [out][in] orientation)
 T_ATTN_NORM, T_WQ, T_WK, T_WV, T_WO, T_FFN_NORM, T_WGATE, T_WUP, T_WDOWN = range(9)
 T_KCACHE, T_VCACHE, T_INPUT = 9, 10, 11
+T_LM_NORM, T_LM_HEAD = 12, 13  # after the stack (generator layer index -1)
 Q4_QUANT_OFFSET, Q4_SCALE_OFFSET = 100, 200
 KV_POS_STRIDE = 1 << 24  # element index of K[g][t][i] = (g*KV_POS_STRIDE + t)*d + i
 
@@ -48,6 +49,7 @@ class Workload:
     weight_fmt: str = "bf16"   # "bf16" or "q4" (int4 per 32 + fp16 scale)
     rms_eps: float = 1e-6
     rope_theta: float = 1e4
+    rope_interleaved: bool = False  # RoPE pairs (2i, 2i+1) instead of (i, i + d/2)
     seed: int = 0
     w_std: float = 0.02
     norm_std: float = 0.1
@@ -185,6 +187,16 @@ def step_input(w: Workload, step: int) -> np.ndarray:
     out = np.empty(w.hidden, dtype=np.float32)
     lib().synth_normal_bf16_as_f32(w.seed, step, T_INPUT, 0, w.hidden, 0.0, 1.0, _ptr(out))
     return out
+
+
+def lm_head(w: Workload, vocab: int) -> tuple[np.ndarray, np.ndarray]:
+    """The LM head after the stack: (final RMSNorm weight bf16 bits [H] ~1 + N(0,
+    norm_std), vocabulary matrix bf16 bits [vocab][H] ~N(0, w_std))."""
+    nw = np.empty(w.hidden, dtype=np.uint16)
+    lib().synth_normal_bf16(w.seed, -1, T_LM_NORM, 0, w.hidden, 1.0, w.norm_std, _ptr(nw))
+    W = np.empty((vocab, w.hidden), dtype=np.uint16)
+    lib().synth_normal_bf16(w.seed, -1, T_LM_HEAD, 0, vocab * w.hidden, 0.0, w.w_std, _ptr(W))
+    return nw, W
 
 
 def bf16_to_f32(bits: np.ndarray) -> np.ndarray:
