@@ -7,7 +7,7 @@ Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--no-cpu-baseline] [--layers L]
-                  [--plan fused|three|persistent|unfused] [--eager]
+                  [--plan fused|four|three|persistent|unfused] [--eager]
                   [--no-pdl] [--no-l2-ahead] [--global-merge]
 
 The last five select the ablations of the default plan (five fused kernels a
@@ -38,8 +38,9 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 # the kernel with the largest stream of the layer, per plan (index within the layer)
-DOMINANT_KERNEL = {"three": 2, "fused": 3}  # gate/up (+ down in the three-kernel plan)
-DOMINANT_NAME = {"three": "norm_gateup_swiglu_down_residual", "fused": "norm_gateup_swiglu"}
+DOMINANT_KERNEL = {"three": 2, "four": 3, "fused": 3}  # gate/up (+ down when fused with it)
+DOMINANT_NAME = {"three": "norm_gateup_swiglu_down_residual",
+                 "four": "norm_gateup_swiglu_down_residual", "fused": "norm_gateup_swiglu"}
 
 
 def parse():
@@ -52,9 +53,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only)")
-    ap.add_argument("--plan", default="fused", choices=["fused", "three", "persistent", "unfused"],
-                    help="fused five-kernel layer, the three-kernel layer, the persistent "
-                         "per-token kernel, or the one-kernel-per-op ablation")
+    ap.add_argument("--plan", default="fused",
+                    choices=["fused", "four", "three", "persistent", "unfused"],
+                    help="fused five-kernel layer, the four- or three-kernel layer, the "
+                         "persistent per-token kernel, or the one-kernel-per-op ablation")
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--no-pdl", action="store_true",
                     help="fused plan: no programmatic dependent launch between kernels")
@@ -109,6 +111,8 @@ def kernel_bytes(w, kernel: int, n_ctx: int, plan: str = "fused") -> int:
     kernel: index within the layer of the five-kernel plan, or of the
     three-kernel plan (0 QKV, 1 attention + o-proj, 2 gate/up + down)."""
     H, F, hd, nq, nkv = w.hidden, w.ffn, w.head_dim, w.n_q_heads, w.n_kv_heads
+    if plan == "four" and kernel == 3:
+        return kernel_bytes(w, 3, n_ctx) + kernel_bytes(w, 4, n_ctx)
     if plan == "three" and kernel > 0:
         parts = (1, 2) if kernel == 1 else (3, 4)
         # the phases' shared vector (o, a) is written once and read once
@@ -368,7 +372,8 @@ def run_ours(args, w, rank, world, local_rank):
     d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=want_cpu, unfused=unfused,
                                     persistent=persistent, graph=not args.eager,
                                     pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
-                                    cluster_attn=not args.global_merge, three=args.plan == "three")
+                                    cluster_attn=not args.global_merge, three=args.plan == "three",
+                                    four=args.plan == "four")
     if args.lm_head:
         nw, Wlm = synth.lm_head(w, args.lm_head)
         d.load_lm_head(nw, Wlm)

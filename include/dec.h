@@ -83,11 +83,14 @@ enum dec_flags {
                                  verifies them */
   DEC_ROPE_INTERLEAVED = 256, /* RoPE rotates dims (2i, 2i+1) of a head as pair i instead of
                                  (i, i + head_dim/2); same angles pos * theta^(-2i/head_dim) */
-  DEC_PAGED_KV = 512          /* fused plans: each layer's KV cache is a pool of pages, a page
+  DEC_PAGED_KV = 512,         /* fused plans: each layer's KV cache is a pool of pages, a page
                                  holding page_rows positions of one KV head (one attention
                                  chunk: 64 at head_dim 128, 128 at 64), laid out
                                  [page][n_kv_heads][page_rows][head_dim]; a page table maps
                                  position chunk c to page pages[c] (dec_set_page_table) */
+  DEC_PLAN_FOUR = 1024        /* fused plan with four kernels per layer: norm + QKV + RoPE + KV
+                                 append; attention; o-proj + residual; norm + gate/up + SwiGLU +
+                                 down + residual (one launch of two phases, grid barrier) */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16
@@ -295,12 +298,14 @@ int dec_get_info(const dec_handle* h, dec_info* info);
 
 /* Source: none on the pages; an addition for timing one fused kernel against
  * its bandwidth roofline.
- * Launches `count` times the fused plan's kernel `kernel` of a layer (three-
- * kernel plan: 0 = norm+QKV+RoPE+append, 1 = attention+o-proj+residual, 2 =
- * norm+gate/up+SwiGLU+down+residual; DEC_PLAN_FIVE: 0 = norm+QKV+RoPE+append,
- * 1 = attention, 2 = o-proj+residual, 3 = norm+gate/up+SwiGLU, 4 =
- * down+residual) for layers first_layer, first_layer+1, ... (mod n_layers),
- * back to back on `stream`, on the activations the last step left.
+ * Launches `count` times the fused plan's kernel `kernel` of a layer (the
+ * five-kernel plan: 0 = norm+QKV+RoPE+append, 1 = attention, 2 =
+ * o-proj+residual, 3 = norm+gate/up+SwiGLU, 4 = down+residual;
+ * DEC_PLAN_FOUR: 0-2 as five, 3 = norm+gate/up+SwiGLU+down+residual;
+ * DEC_PLAN_THREE: 0 = norm+QKV+RoPE+append, 1 = attention+o-proj+residual,
+ * 2 = norm+gate/up+SwiGLU+down+residual) for layers first_layer,
+ * first_layer+1, ... (mod n_layers), back to back on `stream`, on the
+ * activations the last step left.
  * For timing one kernel alone; the KV length does not change and the next
  * dec_step overwrites whatever these launches wrote. */
 int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec_stream_t stream);

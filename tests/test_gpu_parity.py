@@ -14,12 +14,9 @@ if not torch.cuda.is_available():
     pytest.skip("no CUDA device", allow_module_level=True)
 
 
-def _check(w, steps, *, unfused=False, graph=True, persistent=False, cluster_attn=True,
-           three=False, max_ctx=None):
+def _check(w, steps, *, max_ctx=None, **plan):
     max_ctx = max_ctx or w.prefill + steps + 2
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=unfused, graph=graph,
-                                    persistent=persistent, cluster_attn=cluster_attn,
-                                    three=three, keep_host=True)
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, **plan)
     xs = workload.step_inputs(w, steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -53,6 +50,7 @@ MODES = {
     "fused_graph": {},                                   # five kernels, cluster attention
     "fused_eager": {"graph": False},
     "global_merge": {"cluster_attn": False},
+    "four": {"four": True},                              # four kernels per layer
     "three": {"three": True},                            # three kernels per layer
     "three_eager": {"three": True, "graph": False},
     "unfused": {"unfused": True},
@@ -82,7 +80,7 @@ def test_rope_interleaved_pairs(name, mode):
     _check(w, w.steps, **MODES[mode])
 
 
-@pytest.mark.parametrize("mode", ["fused_graph", "three", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "four", "three", "persistent"])
 def test_stack16_h2048_all_steps(mode):
     """16-layer 1B-shape stack, 64 steps from pos 1023, every layer at every step."""
     w = synth.WORKLOADS["stack16_h2048"]
@@ -98,6 +96,7 @@ def test_plans_agree_and_are_deterministic():
                     "no_l2_ahead": {"l2_ahead": False}, "no_pdl": {"pdl": False},
                     "global_merge": {"cluster_attn": False},
                     "three": {"three": True}, "three_eager": {"three": True, "graph": False},
+                    "four": {"four": True},
                     "persistent": {"persistent": True},
                     "persistent_eager": {"persistent": True, "graph": False},
                     "unfused": {"unfused": True}}.items():
@@ -109,6 +108,8 @@ def test_plans_agree_and_are_deterministic():
     assert np.array_equal(outs["graph"], outs["no_l2_ahead"]), "the L2 look-ahead changed results"
     assert np.array_equal(outs["graph"], outs["no_pdl"]), "dependent launch changed results"
     assert np.array_equal(outs["three"], outs["three_eager"])
+    # gate/up + down in one launch: the same split and arithmetic as two launches
+    assert np.array_equal(outs["graph"], outs["four"]), "four vs five kernels differ"
     # the three-kernel plan and the persistent plan run the same split and the
     # same per-phase arithmetic (attention with the GEMV kernels' warp count)
     assert np.array_equal(outs["three"], outs["persistent"]), "persistent differs from three"
@@ -197,7 +198,7 @@ PAGED = {
 
 
 @pytest.mark.parametrize("name", sorted(PAGED))
-@pytest.mark.parametrize("mode", ["fused_graph", "global_merge", "three", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "global_merge", "four", "three", "persistent"])
 def test_paged_kv_matches_contiguous_and_oracle(name, mode):
     """Kernel to parts: the fused QKV kernel writing the rotated k and the v of
     each token into its KV page (a shuffled page table), and attention reading

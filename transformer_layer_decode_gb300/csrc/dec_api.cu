@@ -51,6 +51,7 @@ struct dec_handle {
   bool fused = true, graph = true, pdl = true, persistent = false, l2_ahead = true;
   bool cluster_attn = true;
   bool three = false;  // fused plan: three kernels per layer (else five)
+  bool four = false;   // fused plan: QKV, attention, o-proj, gate/up + down
   bool rope_inter = false;  // RoPE pairs (2i, 2i+1)
   // paged KV cache: pages of page_rows positions of one KV head; the page table
   // (host copy and device copy) maps position chunk c to page pages[c]
@@ -441,6 +442,12 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
   const LayerDev& L = h->layers[l];
   const bool q4 = h->d.weight_fmt == DEC_W_Q4B32;
   cudaError_t e = cudaSuccess;
+  if (h->four && kernel == 3) {
+    e = launch_ffn(q4, ffn_params(h, l, emb, out, in_step), nb, h->ffn_smem, s, h->pdl);
+    if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+    return DEC_OK;
+  }
+  if (h->four && kernel > 3) return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
   if (h->three) {
     switch (kernel) {
       case 0:
@@ -626,7 +633,7 @@ int enqueue_layers(dec_handle* h, const float* emb, float* out, cudaStream_t s, 
     }
     return DEC_OK;
   }
-  const int kpl = h->three ? 3 : 5;
+  const int kpl = h->three ? 3 : h->four ? 4 : 5;
   for (int l = 0; l < Lc; ++l) {
     for (int k = 0; k < kpl; ++k) {
       int rc = enqueue_fused_kernel(h, k, l, emb, out, true, s);
@@ -710,7 +717,7 @@ int patch_io_layers(dec_handle* h, const float* emb, float* out) {
     TLD_CUDA(h, cudaGraphExecKernelNodeSetParams(h->exec, h->first_node, &kp));
     h->cap_emb = emb;
   }
-  if (out != h->cap_out && h->three) {
+  if (out != h->cap_out && (h->three || h->four)) {
     const int l = h->d.n_layers - 1;
     FfnParams p = ffn_params(h, l, emb, out, true);
     void* args[] = {&p};
@@ -779,7 +786,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
                   DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS | DEC_ROPE_INTERLEAVED |
-                  DEC_PAGED_KV))
+                  DEC_PAGED_KV | DEC_PLAN_FOUR))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -793,6 +800,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->cluster_attn = !(d.flags & DEC_ATTN_GLOBAL_MERGE);
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   h->three = h->fused && !h->persistent && (d.flags & DEC_PLAN_THREE);
+  h->four = h->fused && !h->persistent && !h->three && (d.flags & DEC_PLAN_FOUR);
   h->guards = (d.flags & DEC_DEBUG_GUARDS) != 0;
   h->rope_inter = (d.flags & DEC_ROPE_INTERLEAVED) != 0;
   h->paged = (d.flags & DEC_PAGED_KV) != 0;
@@ -869,7 +877,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     A(&h->d_players, sizeof(PLayer) * (size_t)d.n_layers, &h->ws_bytes);
     A(&h->d_bar, 16, &h->ws_bytes);
   }
-  if (h->three) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
+  if (h->three || h->four) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
   if (h->paged) A(&h->d_pages, sizeof(int) * (size_t)h->n_pages, &h->ws_bytes);
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
@@ -893,7 +901,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       }
     e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
-  if (e == cudaSuccess && h->three) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
+  if (e == cudaSuccess && h->d_fbar) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
   if (e == cudaSuccess && h->paged) {  // identity page table until the caller sets one
     h->h_pages.resize(h->n_pages);
     for (int c = 0; c < h->n_pages; ++c) h->h_pages[c] = c;
@@ -921,7 +929,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     h->attn_nstages = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
     h->attn_smem = attn_smem_bytes(hd, G, h->attn_nstages, cl);
   }
-  if (h->three) {
+  if (h->three || h->four) {
     // ring slots hold an attention chunk or a GEMV stage; as many as the budget
     // leaves next to the larger of the two phases' work areas
     const bool q4 = d.weight_fmt == DEC_W_Q4B32;
@@ -1365,7 +1373,7 @@ int dec_check_guards(dec_handle* h) {
 
 int dec_get_info(const dec_handle* h, dec_info* info) {
   if (!h || !info) return DEC_ERR_ARG;
-  info->kernels_per_layer = h->persistent ? 1 : h->three ? 3 : h->fused ? 5
+  info->kernels_per_layer = h->persistent ? 1 : h->three ? 3 : h->four ? 4 : h->fused ? 5
                             : h->d.weight_fmt == DEC_W_Q4B32 ? kUnfusedKernelsPerLayerQ4
                                                              : kUnfusedKernelsPerLayer;
   info->kernels_per_token = h->persistent ? 1 : info->kernels_per_layer * h->d.n_layers;
@@ -1385,7 +1393,7 @@ int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
   if (!h->fused || h->persistent)
     return fail(h, DEC_ERR_STATE, "single-kernel launches need a fused plan of several kernels");
-  if (kernel < 0 || kernel >= (h->three ? 3 : 5) || count < 0 || first_layer < 0 ||
+  if (kernel < 0 || kernel >= (h->three ? 3 : h->four ? 4 : 5) || count < 0 || first_layer < 0 ||
       first_layer >= h->d.n_layers)
     return fail(h, DEC_ERR_ARG, "bad kernel / layer / count");
   const uint32_t need = required_mask(h->d);

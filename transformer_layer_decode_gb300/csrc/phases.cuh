@@ -624,16 +624,23 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   if (W.red[kConsumerWarps] != 0.f) return false;
 
   // ---- finish this CTA's row blocks (sum over warps in warp order) ------------
-  for (int j = tid; j < nrb; j += kNC) {
-    float v[kTileR];
-#pragma unroll
-    for (int r = 0; r < kTileR; ++r) {
-      float sum = 0.f;
+  // one thread per row, four neighbouring lanes per row block; the lane of
+  // row 0 gathers the block's four rows and runs its epilogue
+  static_assert(kTileR == 4, "four rows per row block");
+  const int n4 = nrb * kTileR;
+  for (int base = 0; base < n4; base += kNC) {  // the same trip count in every warp
+    const int t = base + tid;
+    float sum = 0.f;
+    if (t < n4) {
+      const int j = t >> 2, r = t & 3;
 #pragma unroll
       for (int w = 0; w < kConsumerWarps; ++w) sum += W.part[(j * kConsumerWarps + w) * kTileR + r];
-      v[r] = sum * rnorm;
+      sum *= rnorm;
     }
-    gemv_epilogue<EPI>(p, io, rb0 + j, v);
+    float v[kTileR];
+#pragma unroll
+    for (int r = 0; r < kTileR; ++r) v[r] = __shfl_sync(0xffffffffu, sum, (lane & ~3) + r);
+    if (t < n4 && (t & 3) == 0) gemv_epilogue<EPI>(p, io, rb0 + (t >> 2), v);
   }
   return true;
 }
@@ -764,14 +771,25 @@ struct RowSlice {
 // Producer of an attention phase: this CTA's chunks.  wait_pos() is called
 // once before the first chunk that holds the row appended by this step's QKV
 // phase (the other rows were written by earlier steps).
-template <int HD, class WaitPos>
+struct NoHook {
+  __device__ void operator()(int) const {}
+};
+
+template <int HD, class WaitPos, class RingFull = NoHook>
 __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t* kc,
                                              const uint16_t* vc, const Ring& R, RingPos& P,
-                                             const AttnSplit& S, uint64_t pol, WaitPos&& wait_pos) {
+                                             const AttnSplit& S, uint64_t pol, WaitPos&& wait_pos,
+                                             RingFull&& ring_full = RingFull{}) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
-  bool waited = false;
+  bool waited = false, full = false;
   int g = S.u0 / S.cph, c = S.u0 - g * S.cph;
   for (int s = 0; s < S.nu; ++s) {
+    // the ring is full: whatever the producer issues now (the hook) queues
+    // behind this CTA's first stages, ahead of the ones still to come
+    if (!full && P.count >= R.n) {
+      ring_full(s);
+      full = true;
+    }
     if (!ring_reserve(R, P, p.err)) return;
     const int rows = min(CH, S.n - c * CH);
     if (!TLD_IN_BOUNDS(g >= 0 && g < p.nkv && rows > 0 && c * CH + rows <= p.max_ctx &&
@@ -792,6 +810,24 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
       ++g;
     }
     P.next(R.n);
+  }
+  if (!full) ring_full(S.nu);
+}
+
+// L2 prefetch of this CTA's attention chunks from chunk index `from` on (the
+// ones that wait for a ring slot).
+template <int HD>
+__device__ void l2_prefetch_chunks(const AttnParams& p, const AttnSplit& S, int from) {
+  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
+  for (int s = from; s < S.nu; ++s) {
+    const int u = S.u0 + s, g = u / S.cph, c = u - g * S.cph;
+    const int rows = min(CH, S.n - c * CH);
+    const size_t off = (size_t)kv_row_offset(p.pages, CH, p.nkv, p.max_ctx, HD, g, c * CH);
+    const uint32_t bytes = ((uint32_t)rows * HD * 2) & ~15u;
+    if (bytes) {
+      bulk_prefetch_l2(p.kc + off, bytes);
+      bulk_prefetch_l2(p.vc + off, bytes);
+    }
   }
 }
 

@@ -23,7 +23,7 @@ DEC_ERR_POS, DEC_ERR_CTX, DEC_ERR_CUDA, DEC_ERR_OOM, DEC_ERR_DEVICE = -4, -5, -6
 DEC_W_BF16, DEC_W_Q4B32 = 0, 1
 DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL, DEC_PLAN_PERSISTENT = 0, 1, 2, 4, 8
 DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE, DEC_PLAN_THREE, DEC_DEBUG_GUARDS = 16, 32, 64, 128
-DEC_ROPE_INTERLEAVED, DEC_PAGED_KV = 256, 512
+DEC_ROPE_INTERLEAVED, DEC_PAGED_KV, DEC_PLAN_FOUR = 256, 512, 1024
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
@@ -32,6 +32,8 @@ KERNEL_NAMES = ("norm_qkv_rope_append", "attention", "oproj_residual",
                 "norm_gateup_swiglu", "down_residual")
 KERNEL_NAMES_THREE = ("norm_qkv_rope_append", "attention_oproj_residual",
                       "norm_gateup_swiglu_down_residual")
+KERNEL_NAMES_FOUR = ("norm_qkv_rope_append", "attention", "oproj_residual",
+                     "norm_gateup_swiglu_down_residual")
 
 EXPORTED = ("dec_create", "dec_load_weights", "dec_load_kv", "dec_read_kv", "dec_truncate_kv", "dec_step",
             "dec_load_lm_head", "dec_set_token_out", "dec_set_page_table",
@@ -175,7 +177,8 @@ class Decoder:
 
     def __init__(self, shape: Shape, *, unfused: bool = False, graph: bool = True,
                  pdl: bool = True, persistent: bool = False, l2_ahead: bool = True,
-                 cluster_attn: bool = True, three: bool = False, guards: bool = False,
+                 cluster_attn: bool = True, three: bool = False, four: bool = False,
+                 guards: bool = False,
                  rope_interleaved: bool = False, paged_kv: bool = False,
                  lib_path: str | None = None):
         self.lib = load_library(lib_path or LIB_PATH)
@@ -184,7 +187,8 @@ class Decoder:
                  | (0 if pdl else DEC_NO_PDL) | (DEC_PLAN_PERSISTENT if persistent else 0)
                  | (0 if l2_ahead else DEC_NO_L2_AHEAD)
                  | (0 if cluster_attn else DEC_ATTN_GLOBAL_MERGE)
-                 | (DEC_PLAN_THREE if three else 0) | (DEC_DEBUG_GUARDS if guards else 0)
+                 | (DEC_PLAN_THREE if three else 0) | (DEC_PLAN_FOUR if four else 0)
+                 | (DEC_DEBUG_GUARDS if guards else 0)
                  | (DEC_ROPE_INTERLEAVED if rope_interleaved else 0)
                  | (DEC_PAGED_KV if paged_kv else 0))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
