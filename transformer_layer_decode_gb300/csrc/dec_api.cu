@@ -949,6 +949,26 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
                             h->ffn_slot);
     h->ffn_smem = ffn_smem_bytes(H, L0.gu.max_rb_local, F, L0.down.max_rb_local, q4,
                                  h->ffn_nstages, h->ffn_slot);
+    // The in-kernel grid barrier needs every CTA of the grid (one per SM)
+    // resident at once: refuse a plan whose CTA does not fit on an SM.
+    struct {
+      const void* fn;
+      size_t smem;
+    } two_phase[2] = {{ffn_kernel_ptr(q4), h->ffn_smem},
+                      {h->three ? attn_oproj_kernel_ptr(hd, G, q4) : nullptr, h->ao_smem}};
+    for (const auto& k : two_phase) {
+      if (!k.fn) continue;
+      int per_sm = 0;
+      e = cudaFuncSetAttribute(k.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)k.smem);
+      if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k.fn, kThreads, k.smem);
+      if (e != cudaSuccess || per_sm < 1) {
+        g_create_error = std::string("two-phase kernel cannot be resident: ") +
+                         (e != cudaSuccess ? cudaGetErrorString(e) : "no room on an SM");
+        dec_destroy(h);
+        return e != cudaSuccess ? DEC_ERR_CUDA : DEC_ERR_SHAPE;
+      }
+    }
   }
   if (h->fused && !h->persistent && h->cluster_attn) {
     // one cluster per KV head, as many CTAs per head as the SMs allow with every
