@@ -8,12 +8,15 @@ Prints one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload NAME] [--no-cpu-baseline] [--layers L]
                   [--plan fused|four|three|persistent|unfused] [--eager]
-                  [--no-pdl] [--no-l2-ahead] [--global-merge]
+                  [--no-pdl] [--no-l2-ahead] [--global-merge] [--lm-head VOCAB]
+                  [--q4-publish]
 
-The last five select the ablations of the default plan (five fused kernels a
-layer, CUDA graph, programmatic dependent launch, L2 look-ahead, attention as
-one cluster per KV head); --plan three runs three kernels a layer (attention +
-o-proj and gate/up + down each one launch of two phases).
+--plan, --eager, --no-pdl, --no-l2-ahead and --global-merge select the
+ablations of the default plan (five fused kernels a layer, CUDA graph,
+programmatic dependent launch, L2 look-ahead, attention as one cluster per KV
+head); --plan four folds the down GEMV into the gated-FFN kernel, --plan three
+also attention and o-proj (each one launch of two phases).  --q4-publish (int4
+workloads) has each GEMV input's producer publish its int8 codes once.
 
 --impl reference times the fp64 CPU oracle on the host cores on the same
 workload (the slow reference arm).  Under torchrun each rank decodes its own
@@ -68,6 +71,9 @@ def parse():
     ap.add_argument("--global-merge", action="store_true",
                     help="fused plan: flat attention grid merged through global memory "
                          "instead of one cluster per KV head")
+    ap.add_argument("--q4-publish", action="store_true",
+                    help="int4 weights: the kernel that produces each GEMV input publishes its "
+                         "int8 codes once, instead of every GEMV CTA quantizing the vector")
     return ap.parse_args()
 
 
@@ -373,7 +379,7 @@ def run_ours(args, w, rank, world, local_rank):
                                     persistent=persistent, graph=not args.eager,
                                     pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
                                     cluster_attn=not args.global_merge, three=args.plan == "three",
-                                    four=args.plan == "four")
+                                    four=args.plan == "four", q4_publish=args.q4_publish)
     if args.lm_head:
         nw, Wlm = synth.lm_head(w, args.lm_head)
         d.load_lm_head(nw, Wlm)
@@ -491,7 +497,9 @@ def run_ours(args, w, rank, world, local_rank):
                    "plan": ", ".join([args.plan, "eager" if args.eager else "CUDA graph"]
                                      + (["no PDL"] if args.no_pdl else [])
                                      + (["no L2 look-ahead"] if args.no_l2_ahead else [])
-                                     + (["global-merge attention"] if args.global_merge else [])),
+                                     + (["global-merge attention"] if args.global_merge else [])
+                                     + (["int8 inputs published by their producers"]
+                                        if args.q4_publish else [])),
                    "kernels_per_layer": info.kernels_per_layer,
                    "kernels_per_token": info.kernels_per_token + (1 if args.lm_head else 0),
                    "lm_head_vocab": args.lm_head or None,

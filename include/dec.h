@@ -88,9 +88,14 @@ enum dec_flags {
                                  chunk: 64 at head_dim 128, 128 at 64), laid out
                                  [page][n_kv_heads][page_rows][head_dim]; a page table maps
                                  position chunk c to page pages[c] (dec_set_page_table) */
-  DEC_PLAN_FOUR = 1024        /* fused plan with four kernels per layer: norm + QKV + RoPE + KV
+  DEC_PLAN_FOUR = 1024,       /* fused plan with four kernels per layer: norm + QKV + RoPE + KV
                                  append; attention; o-proj + residual; norm + gate/up + SwiGLU +
                                  down + residual (one launch of two phases, grid barrier) */
+  DEC_Q4_PUBLISH = 2048       /* DEC_W_Q4B32, five- and four-kernel plans: the kernel that
+                                 produces each GEMV input publishes its int8 codes once (per
+                                 32-block: codes, scale, sum; RMSNorm inputs also per-CTA sums
+                                 of squares), instead of every CTA of the GEMV quantizing the
+                                 whole vector itself (the default) */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16

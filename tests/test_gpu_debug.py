@@ -35,6 +35,7 @@ PLANS = {
     "persistent": {"persistent": True},
     "unfused": {"unfused": True},
     "paged": {"paged_kv": True},
+    "q4_publish": {"q4_publish": True},  # int4 shapes: inputs published by their producers
 }
 
 

@@ -35,14 +35,28 @@ SMALL = {
 }
 
 
+# fused plans: the int8 GEMV inputs quantized by every CTA of the GEMV
+# (default), or published once by the kernel that produces the vector (publish;
+# five- and four-kernel plans)
+MODES = {
+    "fused_graph": {},
+    "fused_eager": {"graph": False},
+    "four": {"four": True},
+    "publish": {"q4_publish": True},
+    "publish_four": {"q4_publish": True, "four": True},
+    "global_merge": {"cluster_attn": False},
+    "three": {"three": True},
+    "unfused": {"unfused": True},
+    "persistent": {"persistent": True},
+}
+
+
 @pytest.mark.parametrize("name", sorted(SMALL))
-@pytest.mark.parametrize("mode", ["fused_graph", "fused_eager", "unfused", "persistent"])
+@pytest.mark.parametrize("mode", sorted(MODES))
 def test_q4_layers_match_oracle(name, mode):
     w = SMALL[name]
     max_ctx = w.prefill + w.steps + 2
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, unfused=(mode == "unfused"),
-                                    graph=(mode != "fused_eager"),
-                                    persistent=(mode == "persistent"), keep_host=True)
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, **MODES[mode])
     xs = workload.step_inputs(w, w.steps)
     got = run_gpu(d, w, xs)
     d.close()
@@ -52,13 +66,13 @@ def test_q4_layers_match_oracle(name, mode):
             assert_close(got[s, l], ref[s, l], f"{name} {mode} step {s} layer {l}")
 
 
-@pytest.mark.parametrize("persistent", [False, True])
+@pytest.mark.parametrize("mode", ["fused_graph", "publish", "persistent"])
 @pytest.mark.parametrize("kernel", [0, 2, 3, 4])
-def test_q4_integer_block_dots_bit_exact(kernel, persistent):
+def test_q4_integer_block_dots_bit_exact(kernel, mode):
     w = SMALL["q4_gqa4_d64"]
     layer = 1
     max_ctx = w.prefill + 3
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, persistent=persistent)
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, **MODES[mode])
     km = max(w.hidden, w.ffn, w.n_q_heads * w.head_dim)
     qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
     qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")
@@ -84,13 +98,14 @@ def test_q4_integer_block_dots_bit_exact(kernel, persistent):
     assert np.array_equal(gpu, ref), f"{np.count_nonzero(gpu != ref)} block dots differ"
 
 
-def test_q4_int8_activations_match_oracle_quantisation():
+@pytest.mark.parametrize("mode", ["fused_graph", "four", "publish", "publish_four"])
+def test_q4_int8_activations_match_oracle_quantisation(mode):
     """Teacher-forced, slot by slot: the GPU's int8 codes against the oracle's
     own quantizer given the same layer input and the same upstream codes; every
     difference is a one-code flip of a value next to a rounding boundary."""
     w = SMALL["q4_mha_d128"]
     max_ctx = w.prefill + 3
-    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True)
+    d, host = workload.make_decoder(w, max_ctx=max_ctx, keep_host=True, **MODES[mode])
     km = max(w.hidden, w.ffn, w.n_q_heads * w.head_dim)
     qact = torch.zeros(w.n_layers, 4, km, dtype=torch.int8, device="cuda")
     qsc = torch.zeros(w.n_layers, 4, km // 32, dtype=torch.float32, device="cuda")

@@ -64,7 +64,7 @@ def _create(lib, **kw):
     ({"max_ctx": 70000}, dec.DEC_ERR_SHAPE),
     ({"n_layers": 0}, dec.DEC_ERR_ARG),
     ({"weight_fmt": 7}, dec.DEC_ERR_ARG),
-    ({"flags": 2048}, dec.DEC_ERR_ARG),
+    ({"flags": 4096}, dec.DEC_ERR_ARG),
     ({"flags": 1 | 512}, dec.DEC_ERR_SHAPE),   # paged KV cache with the unfused plan
     ({"rope_theta": 0.0}, dec.DEC_ERR_ARG),
 ])

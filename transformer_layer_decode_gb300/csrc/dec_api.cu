@@ -84,6 +84,12 @@ struct dec_handle {
   int* d_bar = nullptr;
   int p_nstages = 0, p_slot = 0;
   size_t p_smem = 0;
+  // int4 weights, five- and four-kernel plans: each GEMV's int8 input is
+  // published once by the kernel that produces the vector (QVec): the inputs
+  // of the QKV (n1), o-proj (o), gate/up (n2) and down (a) projections
+  bool qpub = false;
+  enum { QS_N1 = 0, QS_O = 1, QS_N2 = 2, QS_A = 3 };
+  QVec qs[4] = {};
   float* apart = nullptr;  // attention partial records
   int* acount = nullptr;   // attention arrivals per split head
   int att_grid = 0;
@@ -409,6 +415,30 @@ GemvParams fused_gemv_params(const dec_handle* h, int kernel, int l, const float
     p.qstap = h->qstap + ((size_t)l * 4 + slot) * (km / 32);
   }
   if (in_step && h->dot_tap && h->dot_layer == l && h->dot_kernel == kernel) p.dots = h->dot_tap;
+  if (h->qpub) {  // published int8 inputs (the first layer's QKV quantizes its input itself)
+    const QVec* q = h->qs;
+    switch (kernel) {
+      case 0:
+        if (l > 0) p.qin = q[dec_handle::QS_N1];
+        break;
+      case 2:
+        p.qin = q[dec_handle::QS_O];
+        p.qout = q[dec_handle::QS_N2];
+        p.qout.w = h->layers[l].ffn_norm;
+        break;
+      case 3:
+        p.qin = q[dec_handle::QS_N2];
+        p.qout = q[dec_handle::QS_A];
+        break;
+      default:
+        p.qin = q[dec_handle::QS_A];
+        if (!last) {
+          p.qout = q[dec_handle::QS_N1];
+          p.qout.w = h->layers[l + 1].attn_norm;
+        }
+        break;
+    }
+  }
   return p;
 }
 
@@ -477,6 +507,7 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
       p.tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 1) : nullptr;
       p.ahead = l2_ahead_of(h, 1, l);
       p.cluster = h->att_cluster;
+      if (h->qpub) p.qout = h->qs[dec_handle::QS_O];
       e = launch_attn(h->d.head_dim, h->G, p, fused_att_grid(h), h->attn_smem, s, h->pdl);
       break;
     }
@@ -786,7 +817,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
                   DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS | DEC_ROPE_INTERLEAVED |
-                  DEC_PAGED_KV | DEC_PLAN_FOUR))
+                  DEC_PAGED_KV | DEC_PLAN_FOUR | DEC_Q4_PUBLISH))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -801,6 +832,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   h->three = h->fused && !h->persistent && (d.flags & DEC_PLAN_THREE);
   h->four = h->fused && !h->persistent && !h->three && (d.flags & DEC_PLAN_FOUR);
+  h->qpub = h->fused && !h->persistent && !h->three && d.weight_fmt == DEC_W_Q4B32 &&
+            (d.flags & DEC_Q4_PUBLISH);
   h->guards = (d.flags & DEC_DEBUG_GUARDS) != 0;
   h->rope_inter = (d.flags & DEC_ROPE_INTERLEAVED) != 0;
   h->paged = (d.flags & DEC_PAGED_KV) != 0;
@@ -879,6 +912,24 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   }
   if (h->three || h->four) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
   if (h->paged) A(&h->d_pages, sizeof(int) * (size_t)h->n_pages, &h->ws_bytes);
+  // the GEMV reading a published RMSNorm input stages the producers' per-CTA
+  // sums of squares in its K-float input buffer
+  if (h->qpub && H < h->n_sm) h->qpub = false;
+  if (h->qpub) {
+    const int qk[4] = {H, nq * hd, H, F};
+    for (int i = 0; i < 4; ++i) {
+      QVec& q = h->qs[i];
+      q.K = qk[i];
+      A(&q.codes, (size_t)q.K, &h->ws_bytes);
+      A(&q.scale, 4 * (size_t)(q.K / 32), &h->ws_bytes);
+      A(&q.sum, 4 * (size_t)(q.K / 32), &h->ws_bytes);
+      if (i != dec_handle::QS_O) A(&q.cnt, 4 * (size_t)(q.K / 32), &h->ws_bytes);  // o: whole blocks
+      if (i == dec_handle::QS_N1 || i == dec_handle::QS_N2) {  // RMSNorm inputs
+        q.n_part = h->n_sm;
+        A(&q.part, 4 * (size_t)h->n_sm, &h->ws_bytes);
+      }
+    }
+  }
   A(&h->d_pos, 16, &h->ws_bytes);
   A(&h->d_err, 16, &h->ws_bytes);
   A(&h->rope, sizeof(float2) * (size_t)d.max_ctx * (hd / 2), &h->ws_bytes);
@@ -902,6 +953,8 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     e = cudaMemcpy(h->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   }
   if (e == cudaSuccess && h->d_fbar) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+    if (h->qs[i].cnt) e = cudaMemset(h->qs[i].cnt, 0, 4 * (size_t)(h->qs[i].K / 32));
   if (e == cudaSuccess && h->paged) {  // identity page table until the caller sets one
     h->h_pages.resize(h->n_pages);
     for (int c = 0; c < h->n_pages; ++c) h->h_pages[c] = c;

@@ -151,6 +151,25 @@ struct L2Ahead {
   const int* pages;  // paged KV cache: page table (null: contiguous)
 };
 
+// The int8 input of an int4 GEMV, quantized once by the kernel that produces
+// the vector ("the norm writes the matmul's quantized input") instead of by
+// every CTA of the GEMV.  Per 32-block: the codes in the dp4a arrangement, the
+// block scale amax / 127 (for an RMSNorm input: of x * w, the GEMV applying
+// the 1 / rms), the sum of the codes.  An RMSNorm input also gets one sum of
+// squares per producing CTA, which the GEMV adds in CTA order.  A block cut
+// between CTAs is quantized by the CTA that writes its last element (per-block
+// count of elements written, taken modulo 32; the GEMV that reads the codes
+// clears the counts for the next round).
+struct QVec {
+  uint8_t* codes;      // [K] (null: no published input / output)
+  float* scale;        // [K / 32]
+  int32_t* sum;        // [K / 32]
+  float* part;         // [n_part] sums of squares, or null (not an RMSNorm input)
+  unsigned* cnt;       // [K / 32] element counts, or null (blocks written whole)
+  const uint16_t* w;   // producer side: bf16 RMSNorm weight multiplied in, or null
+  int K, n_part;
+};
+
 enum Prologue : int { PRO_NORM = 0, PRO_PLAIN = 1 };
 enum Epilogue : int { EPI_QKV = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_LOGITS = 3 };
 
@@ -186,6 +205,8 @@ struct GemvParams {
   float* qstap;    // [K/32] block scales, or null
   int32_t* dots;   // [n_rb * kTileR][K/32] integer block dots (tiled row order), or null
   L2Ahead ahead;
+  QVec qin;    // q4: the published int8 input (else this GEMV quantizes x itself)
+  QVec qout;   // q4: publish the int8 quantization of this GEMV's output vector
 };
 
 struct AttnParams {
@@ -203,6 +224,7 @@ struct AttnParams {
   uint64_t* tl;  // optional timeline probe (kTimelineSlots x u64)
   L2Ahead ahead;
   int cluster;   // > 0: grid = nkv clusters of this many CTAs, merged in shared memory
+  QVec qout;     // q4 layer: publish the int8 quantization of o (blocks written whole)
 };
 
 // ---- two-phase kernels of the three-kernel layer ------------------------------

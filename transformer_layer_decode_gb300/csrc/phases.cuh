@@ -115,18 +115,19 @@ struct GemvWork {
         red(reinterpret_cast<float*>(base + L.red_off())) {}
 };
 
-// Epilogue of one finished row block (kTileR tiled rows, values v).
+// Epilogue of one finished row block (kTileR tiled rows, values v).  Returns
+// the sum of squares of the rows written by a residual epilogue (0 otherwise).
 template <int EPI>
-__device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO& io, int rb,
-                                              const float v[kTileR]) {
+__device__ __forceinline__ float gemv_epilogue(const GemvParams& p, const GemvIO& io, int rb,
+                                               const float v[kTileR]) {
   const int R0 = rb * kTileR;
-  if (!TLD_IN_BOUNDS(rb >= 0 && rb < p.n_rb, p.err)) return;
+  if (!TLD_IN_BOUNDS(rb >= 0 && rb < p.n_rb, p.err)) return 0.f;
   if (EPI == EPI_QKV) {
     const int hd = p.hd, half = hd / 2;
     const int qrows = p.nq * hd, krows = p.nkv * hd;
     const int pos = *p.pos;
     if (!TLD_IN_BOUNDS(pos >= 0 && pos < p.max_ctx && R0 + kTileR <= qrows + 2 * krows, p.err))
-      return;
+      return 0.f;
     if (R0 < qrows + krows) {
       // rows (2i, 2i+1) of a head hold the two dims of RoPE pair i: rotate the pair
       const bool is_q = R0 < qrows;
@@ -159,12 +160,15 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO&
       for (int r = 0; r < kTileR; ++r) row[j + r] = f32_to_bf16_bits(v[r]);
     }
   } else if (EPI == EPI_RESID) {
+    float ss = 0.f;
 #pragma unroll
     for (int r = 0; r < kTileR; ++r) {
       const float y = __ldcg(p.resid + R0 + r) + v[r];
       io.out[R0 + r] = y;
       if (io.tap) io.tap[R0 + r] = y;
+      ss = fmaf(y, y, ss);
     }
+    return ss;
   } else if (EPI == EPI_LOGITS) {
 #pragma unroll
     for (int r = 0; r < kTileR; ++r) io.out[R0 + r] = v[r];
@@ -173,6 +177,7 @@ __device__ __forceinline__ void gemv_epilogue(const GemvParams& p, const GemvIO&
 #pragma unroll
     for (int pr = 0; pr < kTileR / 2; ++pr) p.a_out[j + pr] = silu_f(v[2 * pr]) * v[2 * pr + 1];
   }
+  return 0.f;
 }
 
 // A position in the tiled matrix, advanced without divisions.
@@ -311,20 +316,89 @@ __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, floa
   }
 }
 
+// One warp quantizes one 32-block whose element `lane` is u, with the same
+// arithmetic as quantize_blocks: the scale amax / 127, the code round-half-even
+// of u / scale clamped to +-127 (0 when the scale is 0), stored at its place in
+// the dp4a arrangement, and the block's code sum.
+__device__ __forceinline__ void q8_block_warp(float u, int lane, uint8_t* codes, float* scale,
+                                              int32_t* sum) {
+  float amax = fabsf(u);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  float d;
+  int v;
+  if (amax >= 1e-30f) {
+    d = div_rn_from_rcp(amax, 127.0f, 1.0f / 127.0f);
+    v = __float2int_rn(div_rn_from_rcp(u, d, __frcp_rn(d)));
+  } else {
+    d = __fdiv_rn(amax, 127.0f);
+    v = d != 0.0f ? __float2int_rn(__fdiv_rn(u, d)) : 0;
+  }
+  const int q = v > 127 ? 127 : (v < -127 ? -127 : v);
+  int s = q;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  const int j = lane & 7;  // per 8 elements: the even ones, then the odd ones
+  codes[(lane & ~7) + ((j & 1) ? 4 : 0) + (j >> 1)] = (uint8_t)(q & 0xff);
+  if (lane == 0) {
+    *scale = d;
+    *sum = s;
+  }
+}
+
+// Publication of an output vector's int8 quantization (see QVec) after this
+// CTA wrote its elements [e0, e1) of v.  Every writer has passed a CTA barrier
+// after its stores before this call.  One warp per block this CTA touched:
+// lane 0 adds the CTA's element count to the block's counter; the CTA that
+// brings it to a multiple of 32 wrote the block's last element and quantizes
+// the block from L2 (times the norm weight, if any).
+__device__ __forceinline__ void q8_publish(const QVec& q, const float* v, int e0, int e1, int warp,
+                                           int lane, int nwarps, int* err) {
+  const int b0 = e0 >> 5, b1 = (e1 + 31) >> 5;
+  for (int blk = b0 + warp; blk < b1; blk += nwarps) {
+    if (!TLD_IN_BOUNDS(blk >= 0 && blk < q.K / 32, err)) break;
+    int last = 0;
+    if (lane == 0) {
+      __threadfence();  // this CTA's elements before its count
+      const int lo = e0 > (blk << 5) ? e0 : (blk << 5);
+      const int hi = e1 < ((blk + 1) << 5) ? e1 : ((blk + 1) << 5);
+      const unsigned n = (unsigned)(hi - lo);
+      const unsigned old = atomicAdd(q.cnt + blk, n);
+      last = ((old + n) & 31u) == 0u;
+    }
+    if (!__shfl_sync(0xffffffffu, last, 0)) continue;
+    __threadfence();  // the other CTAs' elements, fenced before their counts
+    const int e = (blk << 5) + lane;
+    float u = __ldcg(v + e);
+    if (q.w) u *= __uint_as_float((uint32_t)q.w[e] << 16);
+    q8_block_warp(u, lane, q.codes + (blk << 5), q.scale + blk, q.sum + blk);
+  }
+}
+
+// Four-way byte dot with unsigned bytes in a and signed bytes in b.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // Integer dot of one 32-block: packed nibbles (q + 8) against the arranged
-// int8 activations, minus 8 * (sum of the activations).
+// int8 activations, minus 8 * (sum of the activations).  The low nibbles are
+// masked in place; the high nibbles are masked without a shift, so their bytes
+// hold 16 x the nibble (unsigned) and their dot is 16 x theirs, divided out
+// exactly at the end.
 __device__ __forceinline__ int q4_block_dot(const uint4 w, const uint4 x0, const uint4 x1, int sx) {
   constexpr uint32_t M = 0x0F0F0F0Fu;
-  int d = 0;
-  d = __dp4a((int)(w.x & M), (int)x0.x, d);
-  d = __dp4a((int)((w.x >> 4) & M), (int)x0.y, d);
-  d = __dp4a((int)(w.y & M), (int)x0.z, d);
-  d = __dp4a((int)((w.y >> 4) & M), (int)x0.w, d);
-  d = __dp4a((int)(w.z & M), (int)x1.x, d);
-  d = __dp4a((int)((w.z >> 4) & M), (int)x1.y, d);
-  d = __dp4a((int)(w.w & M), (int)x1.z, d);
-  d = __dp4a((int)((w.w >> 4) & M), (int)x1.w, d);
-  return d - 8 * sx;
+  int lo = 0, hi = 0;
+  lo = __dp4a((int)(w.x & M), (int)x0.x, lo);
+  hi = dp4a_us(w.x & ~M, x0.y, hi);
+  lo = __dp4a((int)(w.y & M), (int)x0.z, lo);
+  hi = dp4a_us(w.y & ~M, x0.w, hi);
+  lo = __dp4a((int)(w.z & M), (int)x1.x, lo);
+  hi = dp4a_us(w.z & ~M, x1.y, hi);
+  lo = __dp4a((int)(w.w & M), (int)x1.z, lo);
+  hi = dp4a_us(w.w & ~M, x1.w, hi);
+  return lo + (hi >> 4) - 8 * sx;
 }
 
 // One stage as kCopiesPerStage bulk copies of about equal size on the same
@@ -420,7 +494,9 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   const int nloc = nrb * geo.ktiles;
   const int nst = (nloc + kStageTiles - 1) / kStageTiles;
   float* xs = W.xs;
-  {
+  // q4 with a published input: the codes, not the vector, are read below
+  const bool qin = Q4 && p.qin.codes != nullptr;
+  if (!qin) {
     // the input vector was written by another phase: read it from L2
     const float4* x4 = reinterpret_cast<const float4*>(io.x);
     float ss = 0.f;
@@ -456,19 +532,51 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     for (int k = tid; k < K; k += kNC) io.x_copy[k] = __ldcg(io.x + k);
   }
   if (p.pos_advance && first_cta && tid == 0) atomicAdd(p.pos_advance, 1);
+  if (qin) {
+    // The producer has finished (griddepcontrol.wait): clear its per-block
+    // counts for the next round, take the 1/rms from its per-CTA sums of
+    // squares (added in CTA order, the same in every CTA), and copy the codes,
+    // scales (times 1/rms) and sums into shared memory.
+    if (first_cta && p.qin.cnt)
+      for (int i = tid; i < K / 32; i += kNC) p.qin.cnt[i] = 0u;
+    // everything in one round trip: codes and sums to shared memory, the scales
+    // and the producers' sums of squares (into xs, unused here) to be scaled
+    const uint4* c4 = reinterpret_cast<const uint4*>(p.qin.codes);
+    for (int i = tid; i < K / 16; i += kNC) reinterpret_cast<uint4*>(W.qx)[i] = __ldcg(c4 + i);
+    for (int i = tid; i < K / 32; i += kNC) {
+      W.dx[i] = __ldcg(p.qin.scale + i);
+      W.sx[i] = __ldcg(p.qin.sum + i);
+    }
+    const int np = PRO == PRO_NORM ? p.qin.n_part : 0;
+    for (int c = tid; c < np; c += kNC) xs[c] = __ldcg(p.qin.part + c);
+    named_barrier(1, kNC);
+    if (PRO == PRO_NORM) {
+      float s = 0.f;
+      for (int c = lane; c < np; c += 32) s += xs[c];
+      s = warp_sum(s);  // the same order, so the same value, in every warp and CTA
+      const float rn = 1.0f / sqrtf(s / (float)K + p.eps);
+      for (int i = tid; i < K / 32; i += kNC) W.dx[i] *= rn;
+    }
+    if (first_cta && io.qstap)
+      for (int i = tid; i < K / 32; i += kNC) io.qstap[i] = W.dx[i];
+  }
   named_barrier(1, kNC);
+  if (qin && first_cta && io.qtap) {
+    for (int e = tid; e < K; e += kNC)
+      io.qtap[e] = (int8_t)W.qx[(e & ~7) + ((e & 1) ? 4 : 0) + ((e & 7) >> 1)];
+  }
 
   // RMSNorm is a per-vector scale 1/sqrt(mean(x^2)+eps).  bf16 weights: the
   // projection runs on x*w and the scale multiplies the finished rows.  q4
   // weights: the normalised vector itself is quantised, so it is scaled first.
   float rnorm = 1.f;
-  if (PRO == PRO_NORM) {
+  if (PRO == PRO_NORM && !qin) {
     float tot = 0.f;
 #pragma unroll
     for (int w = 0; w < kConsumerWarps; ++w) tot += W.red[w];
     rnorm = 1.0f / sqrtf(tot / (float)K + p.eps);
   }
-  if (Q4) {
+  if (Q4 && !qin) {
     // the normalised vector itself is quantised: the codes carry the RMS scale
     quantize_blocks(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid, kNC,
                     rnorm);
@@ -628,6 +736,7 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   // row 0 gathers the block's four rows and runs its epilogue
   static_assert(kTileR == 4, "four rows per row block");
   const int n4 = nrb * kTileR;
+  float ssq = 0.f;  // sum of squares of the residual rows this thread wrote
   for (int base = 0; base < n4; base += kNC) {  // the same trip count in every warp
     const int t = base + tid;
     float sum = 0.f;
@@ -640,7 +749,26 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     float v[kTileR];
 #pragma unroll
     for (int r = 0; r < kTileR; ++r) v[r] = __shfl_sync(0xffffffffu, sum, (lane & ~3) + r);
-    if (t < n4 && (t & 3) == 0) gemv_epilogue<EPI>(p, io, rb0 + (t >> 2), v);
+    if (t < n4 && (t & 3) == 0) ssq += gemv_epilogue<EPI>(p, io, rb0 + (t >> 2), v);
+  }
+  if (Q4 && (EPI == EPI_RESID || EPI == EPI_SWIGLU) && p.qout.codes) {
+    // publish the int8 quantization of this GEMV's output for the next GEMV
+    // (the CTA barrier below orders every thread's stores before the fence that
+    // precedes each block count)
+    if (p.qout.part) {
+      ssq = warp_sum(ssq);
+      if (lane == 0) W.red[warp] = ssq;
+    }
+    named_barrier(1, kNC);
+    if (p.qout.part && tid == 0) {
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kConsumerWarps; ++w) tot += W.red[w];
+      p.qout.part[blockIdx.x] = tot;
+    }
+    const int per = EPI == EPI_SWIGLU ? kTileR / 2 : kTileR;  // outputs per row block
+    q8_publish(p.qout, EPI == EPI_SWIGLU ? p.a_out : io.out, rb0 * per, rb1 * per, warp, lane,
+               kConsumerWarps, p.err);
   }
   return true;
 }
@@ -915,7 +1043,11 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
           cr[HD + 1] = Ls;
         }
       } else if (whole) {
-        p.o[(size_t)(g * G + gg) * HD + j] = A / Ls;
+        const size_t oi = (size_t)(g * G + gg) * HD + j;
+        p.o[oi] = A / Ls;
+        if (p.qout.codes)  // the int8 input of the o-proj, one block per warp
+          q8_block_warp(A / Ls, tid & 31, p.qout.codes + (oi & ~(size_t)31),
+                        p.qout.scale + (oi >> 5), p.qout.sum + (oi >> 5));
       } else {
         rec[gg * (HD + 4) + j] = A;
         if (j == 0) {
@@ -1085,7 +1217,8 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
     // ---- the cluster merges its head: CTA r finishes a slice of the G x HD outputs
     cluster_sync_all();  // every CTA's record is in its shared memory
     const int C = p.cluster, r = (int)cluster_rank(), gh = b / C;
-    const int e0 = split_begin32(G * HD, C, r), e1 = split_begin32(G * HD, C, r + 1);
+    // whole 32-element blocks per CTA (a warp finishes one block at a time)
+    const int e0 = 32 * split_begin32(G * HD / 32, C, r), e1 = 32 * split_begin32(G * HD / 32, C, r + 1);
     for (int e = e0 + tid; e < e1; e += NC) {
       const int gg = e / HD, j = e - gg * HD;
       // two passes over the cluster's records in rank order: the largest
@@ -1101,7 +1234,11 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         Lsum = fmaf(dsmem_ld(a + 4 * (HD + 1)), w, Lsum);
         o = fmaf(dsmem_ld(a + 4 * j), w, o);
       }
-      p.o[(size_t)(gh * G + gg) * HD + j] = o / Lsum;
+      const size_t oi = (size_t)(gh * G + gg) * HD + j;
+      p.o[oi] = o / Lsum;
+      if (p.qout.codes)  // the int8 input of the o-proj, one block per warp
+        q8_block_warp(o / Lsum, tid & 31, p.qout.codes + (oi & ~(size_t)31),
+                      p.qout.scale + (oi >> 5), p.qout.sum + (oi >> 5));
     }
     cluster_sync_all();  // the records stay until every CTA of the cluster has read them
     return ok;
@@ -1170,7 +1307,11 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       Lsum = fmaf(__ldcg(rec + HD + 1), w, Lsum);
       o = fmaf(__ldcg(rec + j), w, o);
     }
-    p.o[(size_t)(g * G + gg) * HD + j] = o / Lsum;
+    const size_t oi = (size_t)(g * G + gg) * HD + j;
+    p.o[oi] = o / Lsum;
+    if (p.qout.codes)  // the int8 input of the o-proj, one block per warp
+      q8_block_warp(o / Lsum, tid & 31, p.qout.codes + (oi & ~(size_t)31), p.qout.scale + (oi >> 5),
+                    p.qout.sum + (oi >> 5));
   }
   if (tid < 2 && todo[tid] >= 0) p.counters[todo[tid]] = 0;
   named_barrier(1, NC);
