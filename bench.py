@@ -41,9 +41,12 @@ sys.path.insert(0, ROOT)
 
 FALLBACK_HBM_GBS = 6800.0
 # the kernel with the largest stream of the layer, per plan (index within the layer)
-DOMINANT_KERNEL = {"three": 2, "four": 3, "fused": 3}  # gate/up (+ down when fused with it)
+DOMINANT_KERNEL = {"three": 2, "four": 3, "fused": 3,  # gate/up (+ down when fused with it)
+                   "headproj": 2, "headproj3": 2}
 DOMINANT_NAME = {"three": "norm_gateup_swiglu_down_residual",
-                 "four": "norm_gateup_swiglu_down_residual", "fused": "norm_gateup_swiglu"}
+                 "four": "norm_gateup_swiglu_down_residual", "fused": "norm_gateup_swiglu",
+                 "headproj": "norm_gateup_swiglu",
+                 "headproj3": "norm_gateup_swiglu_down_residual"}
 
 
 def parse():
@@ -57,9 +60,12 @@ def parse():
     ap.add_argument("--layers", type=int, default=0,
                     help="override the layer count (small profiling cases only)")
     ap.add_argument("--plan", default="fused",
-                    choices=["fused", "four", "three", "persistent", "unfused"],
-                    help="fused five-kernel layer, the four- or three-kernel layer, the "
-                         "persistent per-token kernel, or the one-kernel-per-op ablation")
+                    choices=["fused", "headproj", "headproj3", "four", "three", "persistent",
+                             "unfused"],
+                    help="fused five-kernel layer; attention + o-projection in one cluster "
+                         "launch (headproj: four kernels, headproj3: with the two-phase FFN, "
+                         "three); the four- or three-kernel layers with grid barriers; the "
+                         "persistent per-token kernel; or the one-kernel-per-op ablation")
     ap.add_argument("--eager", action="store_true", help="launch eagerly instead of a CUDA graph")
     ap.add_argument("--no-pdl", action="store_true",
                     help="fused plan: no programmatic dependent launch between kernels")
@@ -117,6 +123,11 @@ def kernel_bytes(w, kernel: int, n_ctx: int, plan: str = "fused") -> int:
     kernel: index within the layer of the five-kernel plan, or of the
     three-kernel plan (0 QKV, 1 attention + o-proj, 2 gate/up + down)."""
     H, F, hd, nq, nkv = w.hidden, w.ffn, w.head_dim, w.n_q_heads, w.n_kv_heads
+    if plan in ("headproj", "headproj3") and kernel > 0:
+        # 1: attention + o-projection; 2: gate/up (+ down); 3: down
+        if kernel == 1:
+            return kernel_bytes(w, 1, n_ctx) + kernel_bytes(w, 2, n_ctx)
+        return kernel_bytes(w, kernel + 1, n_ctx, "four" if plan == "headproj3" else "fused")
     if plan == "four" and kernel == 3:
         return kernel_bytes(w, 3, n_ctx) + kernel_bytes(w, 4, n_ctx)
     if plan == "three" and kernel > 0:
@@ -379,7 +390,9 @@ def run_ours(args, w, rank, world, local_rank):
                                     persistent=persistent, graph=not args.eager,
                                     pdl=not args.no_pdl, l2_ahead=not args.no_l2_ahead,
                                     cluster_attn=not args.global_merge, three=args.plan == "three",
-                                    four=args.plan == "four", q4_publish=args.q4_publish)
+                                    four=args.plan in ("four", "headproj3"),
+                                    attn_oproj=args.plan in ("headproj", "headproj3"),
+                                    q4_publish=args.q4_publish)
     if args.lm_head:
         nw, Wlm = synth.lm_head(w, args.lm_head)
         d.load_lm_head(nw, Wlm)

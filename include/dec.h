@@ -91,11 +91,17 @@ enum dec_flags {
   DEC_PLAN_FOUR = 1024,       /* fused plan with four kernels per layer: norm + QKV + RoPE + KV
                                  append; attention; o-proj + residual; norm + gate/up + SwiGLU +
                                  down + residual (one launch of two phases, grid barrier) */
-  DEC_Q4_PUBLISH = 2048       /* DEC_W_Q4B32, five- and four-kernel plans: the kernel that
+  DEC_Q4_PUBLISH = 2048,      /* DEC_W_Q4B32, five- and four-kernel plans: the kernel that
                                  produces each GEMV input publishes its int8 codes once (per
                                  32-block: codes, scale, sum; RMSNorm inputs also per-CTA sums
                                  of squares), instead of every CTA of the GEMV quantizing the
                                  whole vector itself (the default) */
+  DEC_FUSE_ATTN_OPROJ = 4096  /* fused plans with the cluster attention: attention and the
+                                 o-projection + residual in one cluster launch; each KV head's
+                                 cluster multiplies its merged output by its own columns of Wo
+                                 (stored per KV-head group) and the last cluster to finish a
+                                 row range adds the groups' partial vectors in group order.
+                                 Four kernels per layer (three with DEC_PLAN_FOUR) */
 };
 
 /* Tensor ids for dec_load_weights.  bf16 models load the norm vectors (bf16

@@ -36,6 +36,8 @@ PLANS = {
     "unfused": {"unfused": True},
     "paged": {"paged_kv": True},
     "q4_publish": {"q4_publish": True},  # int4 shapes: inputs published by their producers
+    "headproj": {"attn_oproj": True},
+    "headproj3": {"attn_oproj": True, "four": True},
 }
 
 

@@ -55,6 +55,10 @@ MODES = {
     "three_eager": {"three": True, "graph": False},
     "unfused": {"unfused": True},
     "persistent": {"persistent": True},
+    # attention + o-projection by KV-head group in one cluster launch
+    "headproj": {"attn_oproj": True},
+    "headproj_eager": {"attn_oproj": True, "graph": False},
+    "headproj3": {"attn_oproj": True, "four": True},
 }
 
 
@@ -73,14 +77,14 @@ INTERLEAVED = {
 
 
 @pytest.mark.parametrize("name", sorted(INTERLEAVED))
-@pytest.mark.parametrize("mode", ["fused_graph", "three", "unfused", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "headproj", "three", "unfused", "persistent"])
 def test_rope_interleaved_pairs(name, mode):
     """RoPE on pairs (2i, 2i+1): every plan against the oracle's interleaved chain."""
     w = INTERLEAVED[name]
     _check(w, w.steps, **MODES[mode])
 
 
-@pytest.mark.parametrize("mode", ["fused_graph", "four", "three", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "headproj", "four", "three", "persistent"])
 def test_stack16_h2048_all_steps(mode):
     """16-layer 1B-shape stack, 64 steps from pos 1023, every layer at every step."""
     w = synth.WORKLOADS["stack16_h2048"]
@@ -97,6 +101,10 @@ def test_plans_agree_and_are_deterministic():
                     "global_merge": {"cluster_attn": False},
                     "three": {"three": True}, "three_eager": {"three": True, "graph": False},
                     "four": {"four": True},
+                    "headproj": {"attn_oproj": True},
+                    "headproj_eager": {"attn_oproj": True, "graph": False},
+                    "headproj_no_pdl": {"attn_oproj": True, "pdl": False},
+                    "headproj3": {"attn_oproj": True, "four": True},
                     "persistent": {"persistent": True},
                     "persistent_eager": {"persistent": True, "graph": False},
                     "unfused": {"unfused": True}}.items():
@@ -114,6 +122,13 @@ def test_plans_agree_and_are_deterministic():
     # same per-phase arithmetic (attention with the GEMV kernels' warp count)
     assert np.array_equal(outs["three"], outs["persistent"]), "persistent differs from three"
     assert np.array_equal(outs["persistent"], outs["persistent_eager"])
+    # attention + o-projection in one launch: deterministic group order
+    assert np.array_equal(outs["headproj"], outs["headproj_eager"])
+    assert np.array_equal(outs["headproj"], outs["headproj_no_pdl"])
+    assert np.array_equal(outs["headproj"], outs["headproj3"]), "two-phase FFN changed results"
+    for s in range(3):
+        for l in range(w.n_layers):
+            assert_close(outs["graph"][s, l], outs["headproj"][s, l], f"five vs headproj {s},{l}")
     for s in range(3):
         for l in range(w.n_layers):
             assert_close(outs["graph"][s, l], outs["three"][s, l], f"five vs three {s},{l}")
@@ -142,7 +157,7 @@ def test_residual_wiring_zero_projections():
             assert np.array_equal(got[s, l], xs[s])
 
 
-@pytest.mark.parametrize("mode", ["fused_graph", "three", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "headproj", "headproj3", "three", "persistent"])
 def test_io_pointers_can_change_between_steps(mode):
     """The captured graph is re-pointed when the caller passes new buffers."""
     w = SMALL["ragged_g2_empty"]
@@ -198,7 +213,8 @@ PAGED = {
 
 
 @pytest.mark.parametrize("name", sorted(PAGED))
-@pytest.mark.parametrize("mode", ["fused_graph", "global_merge", "four", "three", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "global_merge", "headproj", "four", "three",
+                                  "persistent"])
 def test_paged_kv_matches_contiguous_and_oracle(name, mode):
     """Kernel to parts: the fused QKV kernel writing the rotated k and the v of
     each token into its KV page (a shuffled page table), and attention reading

@@ -45,6 +45,8 @@ MODES = {
     "publish": {"q4_publish": True},
     "publish_four": {"q4_publish": True, "four": True},
     "global_merge": {"cluster_attn": False},
+    "headproj": {"attn_oproj": True},
+    "headproj3": {"attn_oproj": True, "four": True},
     "three": {"three": True},
     "unfused": {"unfused": True},
     "persistent": {"persistent": True},
@@ -66,7 +68,7 @@ def test_q4_layers_match_oracle(name, mode):
             assert_close(got[s, l], ref[s, l], f"{name} {mode} step {s} layer {l}")
 
 
-@pytest.mark.parametrize("mode", ["fused_graph", "publish", "persistent"])
+@pytest.mark.parametrize("mode", ["fused_graph", "publish", "headproj", "persistent"])
 @pytest.mark.parametrize("kernel", [0, 2, 3, 4])
 def test_q4_integer_block_dots_bit_exact(kernel, mode):
     w = SMALL["q4_gqa4_d64"]
@@ -98,7 +100,7 @@ def test_q4_integer_block_dots_bit_exact(kernel, mode):
     assert np.array_equal(gpu, ref), f"{np.count_nonzero(gpu != ref)} block dots differ"
 
 
-@pytest.mark.parametrize("mode", ["fused_graph", "four", "publish", "publish_four"])
+@pytest.mark.parametrize("mode", ["fused_graph", "four", "publish", "publish_four", "headproj"])
 def test_q4_int8_activations_match_oracle_quantisation(mode):
     """Teacher-forced, slot by slot: the GPU's int8 codes against the oracle's
     own quantizer given the same layer input and the same upstream codes; every

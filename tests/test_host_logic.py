@@ -64,8 +64,9 @@ def _create(lib, **kw):
     ({"max_ctx": 70000}, dec.DEC_ERR_SHAPE),
     ({"n_layers": 0}, dec.DEC_ERR_ARG),
     ({"weight_fmt": 7}, dec.DEC_ERR_ARG),
-    ({"flags": 4096}, dec.DEC_ERR_ARG),
+    ({"flags": 8192}, dec.DEC_ERR_ARG),
     ({"flags": 1 | 512}, dec.DEC_ERR_SHAPE),   # paged KV cache with the unfused plan
+    ({"flags": 4096 | 32}, dec.DEC_ERR_SHAPE),  # attention + o-proj without the cluster attention
     ({"rope_theta": 0.0}, dec.DEC_ERR_ARG),
 ])
 def test_create_rejects_bad_descs_on_the_host(lib, kw, code):

@@ -21,7 +21,8 @@ enum ErrBits : int {
   ERR_DRAIN = 4,
   ERR_SPLITS = 8,
   ERR_GRID_WAIT = 16,
-  ERR_BOUNDS = 32  // debug builds: an index check failed; err[1] holds the source line
+  ERR_BOUNDS = 32,  // debug builds: an index check failed; err[1] holds the source line
+  ERR_CLUSTER_WAIT = 64
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -180,6 +181,45 @@ __device__ __forceinline__ float dsmem_ld(uint32_t a) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
+}
+
+__device__ __forceinline__ void dsmem_st(uint32_t a, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier of a CTA of the cluster (address from dsmem_addr),
+// releasing this thread's prior writes (and those ordered before it by a CTA
+// barrier) at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire: the writes released by the other
+// CTAs' arrivals are visible after it.  Bounded like mbar_wait.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  const int* abort = nullptr) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1; i < kWaitLimit; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+      if (abort && *reinterpret_cast<const volatile int*>(abort)) return false;
+    }
+  }
+  return false;
 }
 
 // Two bf16 packed in a 32-bit word -> two fp32 (exact).

@@ -88,6 +88,16 @@ struct dec_handle {
   // published once by the kernel that produces the vector (QVec): the inputs
   // of the QKV (n1), o-proj (o), gate/up (n2) and down (a) projections
   bool qpub = false;
+  // attention + o-projection by KV-head group in one cluster launch
+  // (DEC_FUSE_ATTN_OPROJ): Wo stored per group, the groups' partial vectors,
+  // arrival counters per row range
+  bool headproj = false;
+  TileGeom hp_geo{};
+  int64_t hp_group_bytes = 0;
+  int hp_nstages = 0;
+  size_t hp_smem = 0;
+  float* hp_part = nullptr;
+  int* hp_cnt = nullptr;
   enum { QS_N1 = 0, QS_O = 1, QS_N2 = 2, QS_A = 3 };
   QVec qs[4] = {};
   float* apart = nullptr;  // attention partial records
@@ -263,6 +273,12 @@ int for_kv_runs(const dec_handle* h, int t0, int t1, Fn&& fn) {
 }
 
 // ---- the fused plan ------------------------------------------------------------
+
+// Launches per layer of a fused (non-persistent) plan.
+int kernels_per_layer(const dec_handle* h) {
+  if (h->three) return 3;
+  return 5 - (h->four ? 1 : 0) - (h->headproj ? 1 : 0);
+}
 
 GemvParams gemv_base(const dec_handle* h, const Tiled& t) {
   GemvParams p{};
@@ -442,6 +458,33 @@ GemvParams fused_gemv_params(const dec_handle* h, int kernel, int l, const float
   return p;
 }
 
+AttnHeadProjParams hp_params(const dec_handle* h, int l, bool in_step) {
+  const LayerDev& L = h->layers[l];
+  AttnHeadProjParams p{};
+  p.attn = k2_params(h, l);
+  p.attn.tl = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 1) : nullptr;
+  p.attn.cluster = h->att_cluster;
+  p.wo = L.o.w;
+  p.group_bytes = h->hp_group_bytes;
+  p.geo = h->hp_geo;
+  p.n_rb = h->d.hidden / kTileR;
+  p.resid = h->X;
+  p.out = h->h1;
+  p.part = h->hp_part;
+  p.cnt = h->hp_cnt;
+  p.nstages = h->hp_nstages;
+  p.slot_bytes = kAttnStageBytes;
+  p.tl2 = (in_step && h->timeline) ? h->timeline + kTimelineSlots * (size_t)(l * 5 + 2) : nullptr;
+  p.ahead = l2_ahead_of(h, 2, l);  // the gate/up weights
+  if (in_step && h->qtap) {  // the o-projection's int8 input (slot 1 of the layer's taps)
+    const int km = max_k(h->d);
+    p.qtap = h->qtap + ((size_t)l * 4 + 1) * km;
+    p.qstap = h->qstap + ((size_t)l * 4 + 1) * (km / 32);
+  }
+  if (in_step && h->dot_tap && h->dot_layer == l && h->dot_kernel == 2) p.dots = h->dot_tap;
+  return p;
+}
+
 AttnOprojParams ao_params(const dec_handle* h, int l, const float* emb, float* out, bool in_step) {
   AttnOprojParams p{};
   p.attn = k2_params(h, l);
@@ -472,6 +515,17 @@ int enqueue_fused_kernel(dec_handle* h, int kernel, int l, const float* emb, flo
   const LayerDev& L = h->layers[l];
   const bool q4 = h->d.weight_fmt == DEC_W_Q4B32;
   cudaError_t e = cudaSuccess;
+  if (h->headproj) {
+    // QKV; attention + o-projection; then gate/up and down, or the two-phase FFN
+    if (kernel == 1) {
+      e = launch_attn_headproj(h->d.head_dim, h->G, q4, hp_params(h, l, in_step), fused_att_grid(h),
+                               h->hp_smem, s, h->pdl);
+      if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
+      return DEC_OK;
+    }
+    if (kernel >= kernels_per_layer(h)) return fail(h, DEC_ERR_ARG, "kernel id %d out of range", kernel);
+    if (kernel >= 2) kernel = h->four ? 3 : kernel + 1;  // the five-kernel plan's ids
+  }
   if (h->four && kernel == 3) {
     e = launch_ffn(q4, ffn_params(h, l, emb, out, in_step), nb, h->ffn_smem, s, h->pdl);
     if (e != cudaSuccess) return cuda_fail(h, e, "kernel launch");
@@ -664,7 +718,7 @@ int enqueue_layers(dec_handle* h, const float* emb, float* out, cudaStream_t s, 
     }
     return DEC_OK;
   }
-  const int kpl = h->three ? 3 : h->four ? 4 : 5;
+  const int kpl = kernels_per_layer(h);
   for (int l = 0; l < Lc; ++l) {
     for (int k = 0; k < kpl; ++k) {
       int rc = enqueue_fused_kernel(h, k, l, emb, out, true, s);
@@ -817,7 +871,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     return fail(nullptr, DEC_ERR_SHAPE, "int4 weights need hidden, ffn and heads*head_dim multiples of 64");
   if (d.flags & ~(DEC_PLAN_UNFUSED | DEC_NO_GRAPH | DEC_NO_PDL | DEC_PLAN_PERSISTENT | DEC_NO_L2_AHEAD |
                   DEC_ATTN_GLOBAL_MERGE | DEC_PLAN_THREE | DEC_DEBUG_GUARDS | DEC_ROPE_INTERLEAVED |
-                  DEC_PAGED_KV | DEC_PLAN_FOUR | DEC_Q4_PUBLISH))
+                  DEC_PAGED_KV | DEC_PLAN_FOUR | DEC_Q4_PUBLISH | DEC_FUSE_ATTN_OPROJ))
     return fail(nullptr, DEC_ERR_ARG, "unknown flags 0x%x", d.flags);
 
   dec_handle* h = new (std::nothrow) dec_handle();
@@ -832,8 +886,9 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->persistent = h->fused && (d.flags & DEC_PLAN_PERSISTENT);
   h->three = h->fused && !h->persistent && (d.flags & DEC_PLAN_THREE);
   h->four = h->fused && !h->persistent && !h->three && (d.flags & DEC_PLAN_FOUR);
-  h->qpub = h->fused && !h->persistent && !h->three && d.weight_fmt == DEC_W_Q4B32 &&
-            (d.flags & DEC_Q4_PUBLISH);
+  h->headproj = h->fused && !h->persistent && !h->three && (d.flags & DEC_FUSE_ATTN_OPROJ);
+  h->qpub = h->fused && !h->persistent && !h->three && !h->headproj &&
+            d.weight_fmt == DEC_W_Q4B32 && (d.flags & DEC_Q4_PUBLISH);
   h->guards = (d.flags & DEC_DEBUG_GUARDS) != 0;
   h->rope_inter = (d.flags & DEC_ROPE_INTERLEAVED) != 0;
   h->paged = (d.flags & DEC_PAGED_KV) != 0;
@@ -844,6 +899,10 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   h->page_rows = kAttnStageBytes / 4 / d.head_dim;  // one attention chunk
   h->n_pages = (d.max_ctx + h->page_rows - 1) / h->page_rows;
   if (h->three) h->cluster_attn = false;  // its attention phase is a flat grid
+  if (h->headproj && !h->cluster_attn) {
+    delete h;
+    return fail(nullptr, DEC_ERR_SHAPE, "the fused attention + o-projection needs the cluster attention");
+  }
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, dev);
@@ -912,6 +971,13 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   }
   if (h->three || h->four) A(&h->d_fbar, 4 * sizeof(int) * (size_t)d.n_layers, &h->ws_bytes);
   if (h->paged) A(&h->d_pages, sizeof(int) * (size_t)h->n_pages, &h->ws_bytes);
+  if (h->headproj) {
+    A(&h->hp_part, 4 * (size_t)nkv * H, &h->ws_bytes);
+    A(&h->hp_cnt, sizeof(int) * (size_t)kMaxCluster, &h->ws_bytes);
+    const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+    h->hp_geo = tile_geom(G * hd, q4);
+    h->hp_group_bytes = (int64_t)(H / kTileR) * h->hp_geo.rb_bytes;
+  }
   // the GEMV reading a published RMSNorm input stages the producers' per-CTA
   // sums of squares in its K-float input buffer
   if (h->qpub && H < h->n_sm) h->qpub = false;
@@ -955,6 +1021,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
   if (e == cudaSuccess && h->d_fbar) e = cudaMemset(h->d_fbar, 0, 4 * sizeof(int) * (size_t)d.n_layers);
   for (int i = 0; i < 4 && e == cudaSuccess; ++i)
     if (h->qs[i].cnt) e = cudaMemset(h->qs[i].cnt, 0, 4 * (size_t)(h->qs[i].K / 32));
+  if (e == cudaSuccess && h->hp_cnt) e = cudaMemset(h->hp_cnt, 0, sizeof(int) * (size_t)kMaxCluster);
   if (e == cudaSuccess && h->paged) {  // identity page table until the caller sets one
     h->h_pages.resize(h->n_pages);
     for (int c = 0; c < h->n_pages; ++c) h->h_pages[c] = c;
@@ -1029,12 +1096,22 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
     int C = h->n_sm / nkv;
     if (C > kMaxCluster) C = kMaxCluster;
     if (C < 1) C = 1;
-    const void* fn = attn_kernel_ptr(hd, G, true);
+    const bool q4 = d.weight_fmt == DEC_W_Q4B32;
+    const void* fn = h->headproj ? attn_headproj_kernel_ptr(hd, G, q4) : attn_kernel_ptr(hd, G, true);
+    auto hp_size = [&](int c) {  // ring stages and shared memory of the fused kernel at cluster size c
+      const int quads = (H / kTileR + c - 1) / c;
+      const size_t fixed = attn_headproj_smem_bytes(hd, G, q4, 0, quads, nkv);
+      int ns = (int)(((size_t)kSmemBudget > fixed ? kSmemBudget - fixed : 0) / (kAttnStageBytes + 16));
+      ns = ns < 2 ? 2 : (ns > 6 ? 6 : ns);
+      h->hp_nstages = ns;
+      h->hp_smem = attn_headproj_smem_bytes(hd, G, q4, ns, quads, nkv);
+    };
     for (; C > 1; --C) {
+      if (h->headproj) hp_size(C);
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(nkv * C);
-      cfg.blockDim = dim3((attn_consumer_warps(G, true) + 1) * 32);
-      cfg.dynamicSmemBytes = h->attn_smem;
+      cfg.blockDim = dim3(h->headproj ? kThreads : (attn_consumer_warps(G, true) + 1) * 32);
+      cfg.dynamicSmemBytes = h->headproj ? h->hp_smem : h->attn_smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;
       attr[0].val.clusterDim.x = C;
@@ -1046,6 +1123,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       if (cudaOccupancyMaxActiveClusters(&active, fn, &cfg) == cudaSuccess && active >= nkv) break;
       cudaGetLastError();  // a size the device refuses is not an error of the handle
     }
+    if (h->headproj) hp_size(C);
     h->att_cluster = C;
   }
   if (h->persistent) {
@@ -1138,7 +1216,9 @@ int dec_load_weights(dec_handle* h, int layer, int tensor, const void* src, size
     default: dst = L.down.w; row0 = 0; kind = 0; break;
   }
   cudaError_t e;
-  if (!q4)
+  if (mt == DEC_T_WO && h->headproj)  // stored per KV-head group (columns of G heads)
+    e = launch_repack_groups(h->staging, scales, q4, N, K, h->G * hd, dst, h->hp_group_bytes, 0);
+  else if (!q4)
     e = launch_repack_bf16(h->staging, N, K, dst, row0, kind, hd, 0);
   else if (scales)
     e = launch_repack_q4(nullptr, h->staging, N, K, dst, row0, kind, hd, 0);
@@ -1446,7 +1526,7 @@ int dec_check_guards(dec_handle* h) {
 
 int dec_get_info(const dec_handle* h, dec_info* info) {
   if (!h || !info) return DEC_ERR_ARG;
-  info->kernels_per_layer = h->persistent ? 1 : h->three ? 3 : h->four ? 4 : h->fused ? 5
+  info->kernels_per_layer = h->persistent ? 1 : h->fused ? kernels_per_layer(h)
                             : h->d.weight_fmt == DEC_W_Q4B32 ? kUnfusedKernelsPerLayerQ4
                                                              : kUnfusedKernelsPerLayer;
   info->kernels_per_token = h->persistent ? 1 : info->kernels_per_layer * h->d.n_layers;
@@ -1466,7 +1546,7 @@ int dec_launch_kernel(dec_handle* h, int kernel, int first_layer, int count, dec
   if (!h) return fail(nullptr, DEC_ERR_ARG, "handle is NULL");
   if (!h->fused || h->persistent)
     return fail(h, DEC_ERR_STATE, "single-kernel launches need a fused plan of several kernels");
-  if (kernel < 0 || kernel >= (h->three ? 3 : h->four ? 4 : 5) || count < 0 || first_layer < 0 ||
+  if (kernel < 0 || kernel >= kernels_per_layer(h) || count < 0 || first_layer < 0 ||
       first_layer >= h->d.n_layers)
     return fail(h, DEC_ERR_ARG, "bad kernel / layer / count");
   const uint32_t need = required_mask(h->d);

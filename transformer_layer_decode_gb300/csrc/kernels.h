@@ -250,6 +250,40 @@ struct FfnParams {  // norm + gate/up + SwiGLU, then down + residual
   uint64_t* tl2;          // timeline row of the down phase or null
 };
 
+// Attention with the o-projection split by KV-head group, in one cluster
+// launch: cluster g (C CTAs) attends for the query heads of KV head g, merges
+// them in distributed shared memory, and every CTA of the cluster receives the
+// group's whole output o_g (G * hd values).  CTA rank r then multiplies o_g by
+// rows [rb0, rb1) of Wo_g = Wo[:, g*G*hd : (g+1)*G*hd] (the columns of the
+// group, stored per group in the tiled layout of K = G*hd), streamed right
+// behind its K/V chunks, into part[g][rows].  The CTA of rank r that finishes
+// last among the nkv clusters adds the nkv partial vectors of its rows in
+// group order to the residual: out = resid + sum_g Wo_g o_g.
+struct AttnHeadProjParams {
+  AttnParams attn;        // cluster attention (attn.cluster = C CTAs per KV head)
+  const uint8_t* wo;      // group g's tiled Wo_g at wo + g * group_bytes
+  int64_t group_bytes;
+  TileGeom geo;           // of K = G * hd
+  int n_rb;               // hidden / 4 row blocks per group
+  const float* resid;     // [hidden]
+  float* out;             // [hidden]
+  float* tap;             // optional copy of out
+  float* part;            // [nkv][hidden] per-group partial projections
+  int* cnt;               // [C] arrivals per row range (zero between launches)
+  int nstages, slot_bytes;
+  uint64_t* tl2;          // timeline row of the projection phase or null
+  L2Ahead ahead;          // the next kernel's bytes
+  int8_t* qtap;           // q4: the int8 o (natural order) and its block scales, or null
+  float* qstap;
+  int32_t* dots;          // q4: [hidden][G*hd*nkv/32] integer block dots, or null
+};
+size_t attn_headproj_smem_bytes(int hd, int G, bool q4, int nstages, int quads, int nkv);
+const void* attn_headproj_kernel_ptr(int hd, int G, bool q4);
+cudaError_t launch_attn_headproj(int hd, int G, bool q4, const AttnHeadProjParams& p, int grid,
+                                 size_t smem, cudaStream_t s, bool pdl);
+cudaError_t launch_repack_groups(const void* src, bool q4_scales, bool q4, int rows, int K, int Kg,
+                                 uint8_t* dst, int64_t group_bytes, cudaStream_t s);
+
 // The LM head after the stack: final RMSNorm x weight + vocabulary GEMV
 // (PRO_NORM, EPI_LOGITS: rows to g.out) and the greedy token.
 struct LmHeadParams {

@@ -35,8 +35,9 @@ size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
 }
 
 // Consumer warps of the attention kernel: 16 for the cluster kernels of GQA
-// groups up to 2 (their registers allow 17 warps a CTA), else 8.
-int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 2 ? 16 : kAttnWarps; }
+// groups up to 4 (their registers allow 17 warps a CTA, and at head_dim 64 a
+// group of 4 then keeps the one-butterfly form), else 8.
+int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 4 ? 16 : kAttnWarps; }
 
 size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster) {
   return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages +
@@ -398,6 +399,117 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_fused(const FfnParams p) {
   if (!ok && tid == 0) ring_drain(R, P, p.gu.err);
 }
 
+// ---- attention + o-projection by KV-head group (one cluster launch) -------------
+size_t attn_headproj_smem_bytes(int hd, int G, bool q4, int nstages, int quads, int nkv) {
+  const HeadProjLayout L{hd, G, quads, (nkv + 15) / 16, q4};
+  return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages + L.total();
+}
+
+template <int HD, int G, bool Q4>
+__global__ void __launch_bounds__(kThreads, 1) attn_headproj(const AttnHeadProjParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Ring R{smem, reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * kAttnStageBytes),
+               reinterpret_cast<uint64_t*>(smem + (size_t)p.nstages * kAttnStageBytes) + p.nstages,
+               p.nstages, kAttnStageBytes};
+  uint8_t* work = smem + (size_t)p.nstages * kAttnStageBytes + 16 * (size_t)p.nstages;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nb = gridDim.x, b = blockIdx.x;
+  const int C = p.attn.cluster, r = (int)cluster_rank(), gh = b / C, nkv = p.attn.nkv;
+  constexpr int Kg = G * HD;
+  const int quads_max = (p.n_rb + C - 1) / C;
+  const HeadProjLayout L{HD, G, quads_max, (nkv + 15) / 16, Q4};
+  float* og = reinterpret_cast<float*>(work + L.og_off());
+  uint64_t* bars = reinterpret_cast<uint64_t*>(work + L.bar_off());
+  int* last_flag = reinterpret_cast<int*>(bars + 3);
+  if (tid == 0) tl_mark_min(p.attn.tl, 0);
+  const int pos = *p.attn.pos;  // see attn_decode
+  const AttnSplit S = attn_split_cluster<HD>(pos, nkv, b, C);
+  // this CTA's rows of the group's projection (the same split in every cluster)
+  const int rb0 = (int)split_begin(p.n_rb, C, r), rb1 = (int)split_begin(p.n_rb, C, r + 1);
+  if (tid == 0) {
+    ring_init(R);
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], (uint32_t)C);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  cluster_sync_all();  // every CTA's exchange barriers exist before any remote arrival
+
+  if (warp == kConsumerWarps) {
+    if (lane == 0) {
+      RingPos P{0, 0, 0};
+      const uint64_t pol = policy_evict_first();
+      attn_produce<HD>(p.attn, p.attn.kc, p.attn.vc, R, P, S, pol, [] { pdl_wait(); });
+      rows_produce(p.wo + (int64_t)gh * p.group_bytes, p.geo, rb0, rb1, R, P, pol, p.attn.err);
+      l2_ahead(p.ahead, b);
+    }
+    return;
+  }
+  pdl_wait();  // q comes from the QKV kernel
+  pdl_trigger();
+  if (tid == 0) {
+    tl_mark_min(p.attn.tl, 2);
+    tl_mark_max(p.attn.tl, 3);
+  }
+  RingPos P{0, 0, 0};
+  const ClusterXchg xg{og, bars};
+  bool ok = attn_main<HD, G, true, kConsumerWarps, true>(p.attn, work, R, P, S, b, nb, tid, &xg);
+  if (tid == 0) {
+    tl_mark_max(p.attn.tl, 1);
+    tl_mark_min(p.attn.tl, 7);
+    tl_mark_min(p.tl2, 0);
+    tl_mark_min(p.tl2, 2);
+    tl_mark_max(p.tl2, 3);
+  }
+  // o_g is complete in this CTA: its int8 codes (q4), then rows [rb0, rb1) of
+  // Wo_g o_g into the group's partial vector
+  uint8_t* qx = work + L.qx_off();
+  float* dx = reinterpret_cast<float*>(work + L.dx_off());
+  int* sx = reinterpret_cast<int*>(work + L.sx_off());
+  if (Q4) {
+    quantize_blocks(og, Kg, qx, dx, sx, (r == 0 && p.qtap) ? p.qtap + (size_t)gh * Kg : nullptr,
+                    (r == 0 && p.qstap) ? p.qstap + (size_t)gh * (Kg / 32) : nullptr, tid, kNC,
+                    1.0f);
+    named_barrier(1, kNC);
+  }
+  float* part = p.part + (size_t)gh * p.n_rb * kTileR;
+  ok &= rows_main<Q4>(p.geo, og, qx, dx, sx, R, P, rb0, rb1, tid, p.attn.err,
+                      p.dots ? p.dots + (size_t)gh * (Kg / 32) : nullptr, nkv * (Kg / 32),
+                      [&](int row, float v) { part[row] = v; });
+  if (tid == 0) tl_mark_max(p.tl2, 6);
+  // the CTA of rank r that finishes last over the groups adds up their rows
+  named_barrier(1, kNC);
+  if (tid == 0) {
+    const int last = atomic_add_acq_rel(&p.cnt[r], 1) == nkv - 1;
+    if (last) p.cnt[r] = 0;  // every group has arrived: ready for the next launch
+    *last_flag = last;
+  }
+  named_barrier(1, kNC);
+  if (*last_flag)
+    headproj_sum(p.part, nkv, p.n_rb * kTileR, p.resid, p.out, p.tap, rb0 * kTileR, rb1 * kTileR,
+                 reinterpret_cast<float4*>(work + L.red_off()), tid, kNC);
+  // the other CTAs of the cluster have read this CTA's attention record
+  if (!mbar_wait_cluster(&bars[2], 0, p.attn.err)) {
+    raise_error(p.attn.err, ERR_CLUSTER_WAIT);
+    ok = false;
+  }
+  if (tid == 0) {
+    tl_mark_max(p.tl2, 1);
+    tl_mark_min(p.tl2, 7);
+  }
+  if (!ok && tid == 0) ring_drain(R, P, p.attn.err);
+}
+
+const void* attn_headproj_kernel_ptr(int hd, int G, bool q4) {
+#define TLD_HP(H_, G_)                                                    \
+  if (hd == H_ && G == G_)                                                \
+    return q4 ? (const void*)attn_headproj<H_, G_, true>                  \
+              : (const void*)attn_headproj<H_, G_, false>;
+  TLD_HP(64, 1) TLD_HP(64, 2) TLD_HP(64, 4) TLD_HP(64, 8)
+  TLD_HP(128, 1) TLD_HP(128, 2) TLD_HP(128, 4) TLD_HP(128, 8)
+#undef TLD_HP
+  return nullptr;
+}
+
 const void* attn_oproj_kernel_ptr(int hd, int G, bool q4) {
 #define TLD_AO(H_, G_)                                                    \
   if (hd == H_ && G == G_)                                                \
@@ -427,7 +539,7 @@ const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
 const void* attn_kernel_ptr(int hd, int G, bool cluster) {
 #define TLD_ATTN(H_, G_)                                                                       \
   if (hd == H_ && G == G_)                                                                    \
-    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 2 ? 16 : kAttnWarps)>  \
+    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 4 ? 16 : kAttnWarps)>  \
                    : (const void*)attn_decode<H_, G_, false, kAttnWarps>;
   TLD_ATTN(64, 1) TLD_ATTN(64, 2) TLD_ATTN(64, 4) TLD_ATTN(64, 8)
   TLD_ATTN(128, 1) TLD_ATTN(128, 2) TLD_ATTN(128, 4) TLD_ATTN(128, 8)
@@ -470,6 +582,14 @@ cudaError_t set_smem_limits() {
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
         if (e == cudaSuccess && cl)
           e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+      }
+  for (int hd : {64, 128})
+    for (int G : {1, 2, 4, 8})
+      for (bool q4 : {false, true}) {
+        const void* k = attn_headproj_kernel_ptr(hd, G, q4);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
+        if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
       }
   return cudaSuccess;
@@ -537,6 +657,16 @@ cudaError_t launch_attn_oproj(int hd, int G, bool q4, const AttnOprojParams& p, 
   return launch_pdl(fn, args, grid, smem, s, pdl);
 }
 
+cudaError_t launch_attn_headproj(int hd, int G, bool q4, const AttnHeadProjParams& p, int grid,
+                                 size_t smem, cudaStream_t s, bool pdl) {
+  const void* fn = attn_headproj_kernel_ptr(hd, G, q4);
+  if (!fn || p.attn.cluster < 1 || p.attn.cluster > kMaxCluster || grid != p.attn.nkv * p.attn.cluster)
+    return cudaErrorInvalidValue;
+  AttnHeadProjParams copy = p;
+  void* args[] = {&copy};
+  return launch_pdl(fn, args, grid, smem, s, pdl, p.attn.cluster);
+}
+
 cudaError_t launch_ffn(bool q4, const FfnParams& p, int grid, size_t smem, cudaStream_t s,
                        bool pdl) {
   FfnParams copy = p;
@@ -595,6 +725,41 @@ __global__ void repack_q4_kernel(const uint8_t* __restrict__ nib, const uint16_t
         *reinterpret_cast<uint16_t*>(dst + q4_scale_byte(r, bb, K)) = in[bb];
     }
   }
+}
+
+// Wo split by KV-head group: columns [g*Kg, (g+1)*Kg) of each row go to group
+// g's tiled matrix of K = Kg at dst + g * group_bytes.
+__global__ void repack_groups_kernel(const uint8_t* __restrict__ src, int mode, int rows, int K,
+                                     int Kg, uint8_t* __restrict__ dst, int64_t group_bytes) {
+  for (int s = blockIdx.x; s < rows; s += gridDim.x) {
+    if (mode == 0) {  // bf16 elements
+      const uint16_t* in = reinterpret_cast<const uint16_t*>(src) + (size_t)s * K;
+      for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const int g = k / Kg, kk = k - g * Kg;
+        reinterpret_cast<uint16_t*>(dst + g * group_bytes)[tiled_elem_offset(s, kk, Kg)] = in[k];
+      }
+    } else if (mode == 1) {  // q4 nibble pairs
+      const uint8_t* in = src + (size_t)s * (K / 2);
+      for (int c2 = threadIdx.x; c2 < K / 2; c2 += blockDim.x) {
+        const int g = (2 * c2) / Kg, cc = c2 - g * (Kg / 2);
+        dst[g * group_bytes + q4_nibble_byte(s, cc, Kg)] = in[c2];
+      }
+    } else {  // q4 block scales
+      const uint16_t* in = reinterpret_cast<const uint16_t*>(src) + (size_t)s * (K / 32);
+      for (int bb = threadIdx.x; bb < K / 32; bb += blockDim.x) {
+        const int g = (32 * bb) / Kg, bg = bb - g * (Kg / 32);
+        *reinterpret_cast<uint16_t*>(dst + g * group_bytes + q4_scale_byte(s, bg, Kg)) = in[bb];
+      }
+    }
+  }
+}
+
+cudaError_t launch_repack_groups(const void* src, bool q4_scales, bool q4, int rows, int K, int Kg,
+                                 uint8_t* dst, int64_t group_bytes, cudaStream_t s) {
+  const int grid = rows < 4096 ? rows : 4096;
+  repack_groups_kernel<<<grid, 256, 0, s>>>(reinterpret_cast<const uint8_t*>(src),
+                                            !q4 ? 0 : q4_scales ? 2 : 1, rows, K, Kg, dst, group_bytes);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_repack_q4(const uint8_t* nibbles, const uint16_t* scales, int rows, int K,

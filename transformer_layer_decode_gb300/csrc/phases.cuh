@@ -959,11 +959,22 @@ __device__ void l2_prefetch_chunks(const AttnParams& p, const AttnSplit& S, int 
   }
 }
 
+// The cluster merge of the attention + head-projection kernel: instead of two
+// cluster-wide barriers (which the producer, still streaming the projection's
+// weights, cannot join), three mbarriers per CTA that the consumers of every
+// CTA arrive on remotely: records ready, o_g pushed, records read.  og is this
+// CTA's copy of the group's merged output, filled by every CTA of the cluster.
+struct ClusterXchg {
+  float* og;       // [G * HD]
+  uint64_t* bars;  // [3]: records ready, og complete, records read (C arrivals each)
+};
+
 // Consumer part of an attention phase (q must be ready).  Returns false if a
 // wait ran out.
-template <int HD, int G, bool CL = false, int NW = kConsumerWarps>
+template <int HD, int G, bool CL = false, int NW = kConsumerWarps, bool XG = false>
 __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, const Ring& R, RingPos& P,
-                          const AttnSplit& S, int b, int nb, int tid) {
+                          const AttnSplit& S, int b, int nb, int tid,
+                          const ClusterXchg* xg = nullptr) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);  // positions per chunk (16 KB of K)
   constexpr int NC = NW * 32;                          // consumer threads
   constexpr int PW = CH / NW;                          // positions per warp per chunk
@@ -1215,8 +1226,18 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
 
   if (CL) {
     // ---- the cluster merges its head: CTA r finishes a slice of the G x HD outputs
-    cluster_sync_all();  // every CTA's record is in its shared memory
     const int C = p.cluster, r = (int)cluster_rank(), gh = b / C;
+    if (XG) {
+      named_barrier(1, NC);  // this CTA's record (or its empty record) is written
+      if (tid == 0)
+        for (int c2 = 0; c2 < C; ++c2) mbar_arrive_cluster(dsmem_addr(&xg->bars[0], (uint32_t)c2));
+      if (!mbar_wait_cluster(&xg->bars[0], 0, p.err)) {
+        raise_error(p.err, ERR_CLUSTER_WAIT);
+        ok = false;
+      }
+    } else {
+      cluster_sync_all();  // every CTA's record is in its shared memory
+    }
     // whole 32-element blocks per CTA (a warp finishes one block at a time)
     const int e0 = 32 * split_begin32(G * HD / 32, C, r), e1 = 32 * split_begin32(G * HD / 32, C, r + 1);
     for (int e = e0 + tid; e < e1; e += NC) {
@@ -1235,10 +1256,29 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         o = fmaf(dsmem_ld(a + 4 * j), w, o);
       }
       const size_t oi = (size_t)(gh * G + gg) * HD + j;
+      if (XG) {  // into every CTA's copy of o_g
+        for (int c2 = 0; c2 < C; ++c2) dsmem_st(dsmem_addr(xg->og + e, (uint32_t)c2), o / Lsum);
+        continue;
+      }
       p.o[oi] = o / Lsum;
       if (p.qout.codes)  // the int8 input of the o-proj, one block per warp
         q8_block_warp(o / Lsum, tid & 31, p.qout.codes + (oi & ~(size_t)31),
                       p.qout.scale + (oi >> 5), p.qout.sum + (oi >> 5));
+    }
+    if (XG) {
+      // this CTA's pushes are done and it has read every record; o_g is complete
+      // once every CTA has pushed (the records are released at the kernel's end)
+      named_barrier(1, NC);
+      if (tid == 0)
+        for (int c2 = 0; c2 < C; ++c2) {
+          mbar_arrive_cluster(dsmem_addr(&xg->bars[1], (uint32_t)c2));
+          mbar_arrive_cluster(dsmem_addr(&xg->bars[2], (uint32_t)c2));
+        }
+      if (!mbar_wait_cluster(&xg->bars[1], 0, p.err)) {
+        raise_error(p.err, ERR_CLUSTER_WAIT);
+        ok = false;
+      }
+      return ok;
     }
     cluster_sync_all();  // the records stay until every CTA of the cluster has read them
     return ok;
@@ -1316,6 +1356,157 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   if (tid < 2 && todo[tid] >= 0) p.counters[todo[tid]] = 0;
   named_barrier(1, NC);
   return ok;
+}
+
+// ---- o-projection by KV-head group (the attention + head-projection kernel) ----
+// Work area after the attention's: the group's merged output o_g, its int8
+// codes (q4), the scratch of the final sum over groups, the three exchange
+// mbarriers and the last-arrival flag.
+struct HeadProjLayout {
+  int hd, G, quads, nh;  // quads: row quads per CTA at most; nh: 16-group chunks of the sum
+  bool q4;
+  __host__ __device__ size_t attn_bytes() const { return (AttnLayout{hd, G, kConsumerWarps}.total() + 15) & ~(size_t)15; }
+  __host__ __device__ size_t og_off() const { return attn_bytes(); }
+  __host__ __device__ size_t qx_off() const { return og_off() + 4 * (size_t)G * hd; }
+  __host__ __device__ size_t dx_off() const { return qx_off() + (q4 ? (size_t)G * hd : 0); }
+  __host__ __device__ size_t sx_off() const { return dx_off() + (q4 ? 4 * (size_t)G * hd / 32 : 0); }
+  __host__ __device__ size_t red_off() const { return (sx_off() + (q4 ? 4 * (size_t)G * hd / 32 : 0) + 15) & ~(size_t)15; }
+  __host__ __device__ size_t bar_off() const { return red_off() + 16 * (size_t)quads * nh; }
+  __host__ __device__ size_t total() const { return bar_off() + 3 * 8 + 8; }
+};
+
+// Producer: rows [rb0, rb1) of a group's tiled matrix, as many whole row
+// blocks per stage as a ring slot holds.
+__device__ __forceinline__ void rows_produce(const uint8_t* w, const TileGeom& geo, int rb0, int rb1,
+                                             const Ring& R, RingPos& P, uint64_t pol, int* err) {
+  const int rps = (int)(R.slot_bytes / geo.rb_bytes);
+  if (!TLD_IN_BOUNDS(rps >= 1 && (geo.rb_bytes & 15) == 0, err)) return;
+  for (int rb = rb0; rb < rb1; rb += rps) {
+    const int n = rb1 - rb < rps ? rb1 - rb : rps;
+    if (!ring_reserve(R, P, err)) return;
+    const uint32_t bytes = (uint32_t)(n * geo.rb_bytes);
+    mbar_arrive_expect_tx(&R.full[P.slot], bytes);
+    bulk_g2s_split(R.slot(P.slot), w + (int64_t)rb * geo.rb_bytes, bytes, &R.full[P.slot], pol);
+    P.next(R.n);
+  }
+}
+
+// Consumers: x (fp32 [K], or its int8 codes qx / dx / sx for q4 weights) times
+// rows [rb0, rb1) of the tiled matrix streamed by rows_produce.  A warp takes
+// whole row blocks (every k-tile of them), so each row is finished inside one
+// warp: emit(row, value) is called by lane 8r of the warp for row r of the
+// block.  dots (q4, optional): the integer block dots, row-major with ld
+// blocks per row.  Returns false if a wait ran out.
+template <bool Q4, class Emit>
+__device__ __forceinline__ bool rows_main(const TileGeom& geo, const float* x, const uint8_t* qx,
+                                          const float* dx, const int* sx, const Ring& R, RingPos& P,
+                                          int rb0, int rb1, int tid, int* err, int32_t* dots,
+                                          int dots_ld, Emit&& emit) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int rps = (int)(R.slot_bytes / geo.rb_bytes);
+  bool ok = rps >= 1;
+  for (int rbs = rb0; rbs < rb1 && rps >= 1; rbs += rps) {
+    const int n = rb1 - rbs < rps ? rb1 - rbs : rps;
+    if (ok && !mbar_wait(&R.full[P.slot], P.phase, err)) {
+      raise_error(err, ERR_FULL_WAIT);
+      ok = false;
+    }
+    const uint8_t* st = R.slot(P.slot);
+    for (int i = warp; ok && i < n; i += kConsumerWarps) {
+      const int rb = rbs + i;
+      float acc[kTileR] = {0.f, 0.f, 0.f, 0.f};
+      for (int kt = 0; kt < geo.ktiles; ++kt) {
+        const int kw = (kt == geo.ktiles - 1) ? geo.kw_last : geo.tile_k;
+        const uint8_t* tp = st + (int64_t)i * geo.rb_bytes + (int64_t)kt * geo.tile_bytes;
+        if (Q4) {
+          if (lane * 32 >= kw) continue;
+          const int blk = kt * (kTileKQ4 / 32) + lane;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(qx + blk * 32);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(qx + blk * 32 + 16);
+          const uint2 sc = *reinterpret_cast<const uint2*>(tp + (size_t)kTileR * (kw / 2) + lane * 8);
+          const uint32_t sc2[2] = {sc.x, sc.y};
+#pragma unroll
+          for (int r = 0; r < kTileR; ++r) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(tp + (size_t)r * (kw / 2) + lane * 16);
+            const int idot = q4_block_dot(wv, x0, x1, sx[blk]);
+            const uint16_t hb = (uint16_t)(r & 1 ? sc2[r >> 1] >> 16 : sc2[r >> 1] & 0xffff);
+            acc[r] = fmaf(__half2float(__ushort_as_half(hb)) * dx[blk], (float)idot, acc[r]);
+            if (dots) dots[(size_t)(rb * kTileR + r) * dots_ld + blk] = idot;
+          }
+        } else {
+          const int c = lane * 8;
+          if (c >= kw) continue;
+          const float4 xa = *reinterpret_cast<const float4*>(x + kt * kTileK + c);
+          const float4 xb = *reinterpret_cast<const float4*>(x + kt * kTileK + c + 4);
+#pragma unroll
+          for (int r = 0; r < kTileR; ++r) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(tp + ((size_t)r * kw + c) * 2);
+            float a = acc[r];
+            a = fmaf(bf16lo(wv.x), xa.x, a);
+            a = fmaf(bf16hi(wv.x), xa.y, a);
+            a = fmaf(bf16lo(wv.y), xa.z, a);
+            a = fmaf(bf16hi(wv.y), xa.w, a);
+            a = fmaf(bf16lo(wv.z), xb.x, a);
+            a = fmaf(bf16hi(wv.z), xb.y, a);
+            a = fmaf(bf16lo(wv.w), xb.z, a);
+            a = fmaf(bf16hi(wv.w), xb.w, a);
+            acc[r] = a;
+          }
+        }
+      }
+      const float v = warp_reduce4(acc, lane);
+      if ((lane & 7) == 0) emit(rb * kTileR + (lane >> 3), v);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[P.slot]);
+    P.next(R.n);
+  }
+  return ok;
+}
+
+// The last of the nkv CTAs that cover rows [r0, r1) (one per KV-head group)
+// adds their partial projections in group order to the residual:
+// out = resid + sum_g part[g].  Sixteen groups' float4 loads in flight per
+// thread; the chunks of sixteen groups are added in chunk order.
+__device__ __forceinline__ void headproj_sum(const float* part, int nkv, int H, const float* resid,
+                                             float* out, float* tap, int r0, int r1, float4* red,
+                                             int tid, int NC) {
+  const int quads = (r1 - r0) / 4, nh = (nkv + 15) / 16;
+  for (int t = tid; t < quads * nh; t += NC) {
+    const int q = t % quads, h = t / quads;
+    const int row = r0 + 4 * q;
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (16 * h + i < nkv)
+        v[i] = __ldcg(reinterpret_cast<const float4*>(part + (size_t)(16 * h + i) * H + row));
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if (16 * h + i < nkv) {
+        a.x += v[i].x;
+        a.y += v[i].y;
+        a.z += v[i].z;
+        a.w += v[i].w;
+      }
+    red[h * quads + q] = a;
+  }
+  named_barrier(1, NC);
+  for (int q = tid; q < quads; q += NC) {
+    const int row = r0 + 4 * q;
+    float4 a = red[q];
+    for (int h = 1; h < nh; ++h) {
+      const float4 b = red[h * quads + q];
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
+    }
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(resid + row));
+    const float4 y = make_float4(x.x + a.x, x.y + a.y, x.z + a.z, x.w + a.w);
+    *reinterpret_cast<float4*>(out + row) = y;
+    if (tap) *reinterpret_cast<float4*>(tap + row) = y;
+  }
 }
 
 }  // namespace tld

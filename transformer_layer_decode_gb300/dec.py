@@ -24,6 +24,7 @@ DEC_W_BF16, DEC_W_Q4B32 = 0, 1
 DEC_PLAN_FUSED, DEC_PLAN_UNFUSED, DEC_NO_GRAPH, DEC_NO_PDL, DEC_PLAN_PERSISTENT = 0, 1, 2, 4, 8
 DEC_NO_L2_AHEAD, DEC_ATTN_GLOBAL_MERGE, DEC_PLAN_THREE, DEC_DEBUG_GUARDS = 16, 32, 64, 128
 DEC_ROPE_INTERLEAVED, DEC_PAGED_KV, DEC_PLAN_FOUR, DEC_Q4_PUBLISH = 256, 512, 1024, 2048
+DEC_FUSE_ATTN_OPROJ = 4096
 DEC_T_ATTN_NORM, DEC_T_WQ, DEC_T_WK, DEC_T_WV, DEC_T_WO = 0, 1, 2, 3, 4
 DEC_T_FFN_NORM, DEC_T_WGATE, DEC_T_WUP, DEC_T_WDOWN, DEC_T_SCALES = 5, 6, 7, 8, 16
 
@@ -180,7 +181,8 @@ class Decoder:
                  cluster_attn: bool = True, three: bool = False, four: bool = False,
                  guards: bool = False,
                  rope_interleaved: bool = False, paged_kv: bool = False,
-                 q4_publish: bool = False, lib_path: str | None = None):
+                 q4_publish: bool = False, attn_oproj: bool = False,
+                 lib_path: str | None = None):
         self.lib = load_library(lib_path or LIB_PATH)
         self.shape = shape
         flags = ((DEC_PLAN_UNFUSED if unfused else 0) | (0 if graph else DEC_NO_GRAPH)
@@ -191,7 +193,8 @@ class Decoder:
                  | (DEC_DEBUG_GUARDS if guards else 0)
                  | (DEC_ROPE_INTERLEAVED if rope_interleaved else 0)
                  | (DEC_PAGED_KV if paged_kv else 0)
-                 | (DEC_Q4_PUBLISH if q4_publish else 0))
+                 | (DEC_Q4_PUBLISH if q4_publish else 0)
+                 | (DEC_FUSE_ATTN_OPROJ if attn_oproj else 0))
         self.desc = ModelDesc(shape.n_layers, shape.hidden, shape.n_q_heads, shape.n_kv_heads,
                               shape.head_dim, shape.ffn, shape.rms_eps, shape.rope_theta,
                               shape.max_ctx, shape.weight_fmt, flags)

@@ -41,7 +41,8 @@ def make_decoder(w: synth.Workload, *, max_ctx: int | None = None, unfused: bool
                  graph: bool = True, pdl: bool = True, persistent: bool = False,
                  cluster_attn: bool = True, l2_ahead: bool = True, three: bool = False,
                  four: bool = False, paged_kv: bool = False, page_table=None,
-                 q4_publish: bool = False, keep_host: bool = False):
+                 q4_publish: bool = False, attn_oproj: bool = False,
+                 keep_host: bool = False):
     """Create a decoder with every layer's weights and KV prefill loaded.
 
     Returns (decoder, host) where host is None or, with keep_host, a dict with
@@ -49,7 +50,8 @@ def make_decoder(w: synth.Workload, *, max_ctx: int | None = None, unfused: bool
     d = dec.Decoder(shape_of(w, max_ctx), unfused=unfused, graph=graph, pdl=pdl,
                     persistent=persistent, cluster_attn=cluster_attn, l2_ahead=l2_ahead,
                     three=three, four=four, rope_interleaved=w.rope_interleaved,
-                    paged_kv=paged_kv, q4_publish=q4_publish)
+                    paged_kv=paged_kv, q4_publish=q4_publish,
+                    attn_oproj=attn_oproj)
     if page_table is not None:
         d.set_page_table(page_table)
     host = {"layers": [], "kv": []} if keep_host else None
