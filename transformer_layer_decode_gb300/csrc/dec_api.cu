@@ -1110,7 +1110,7 @@ int dec_create(const dec_model_desc* desc, dec_handle** out) {
       if (h->headproj) hp_size(C);
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(nkv * C);
-      cfg.blockDim = dim3(h->headproj ? kThreads : (attn_consumer_warps(G, true) + 1) * 32);
+      cfg.blockDim = dim3(h->headproj ? kThreads : (attn_consumer_warps(hd, G, true) + 1) * 32);
       cfg.dynamicSmemBytes = h->headproj ? h->hp_smem : h->attn_smem;
       cudaLaunchAttribute attr[1];
       attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -350,7 +350,7 @@ cudaError_t launch_persistent(int hd, int G, bool q4, const TokenParams& P, int 
 // Shared memory the fused kernels need.
 size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local);
 size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster = false);
-int attn_consumer_warps(int G, bool cluster);
+int attn_consumer_warps(int hd, int G, bool cluster);
 
 // Launch with programmatic stream serialization (the kernel may start while
 // the previous one on the stream finishes; it waits before reading its inputs).

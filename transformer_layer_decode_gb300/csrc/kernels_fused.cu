@@ -35,13 +35,18 @@ size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
 }
 
 // Consumer warps of the attention kernel: 16 for the cluster kernels of GQA
-// groups up to 4 (their registers allow 17 warps a CTA, and at head_dim 64 a
-// group of 4 then keeps the one-butterfly form), else 8.
-int attn_consumer_warps(int G, bool cluster) { return cluster && G <= 4 ? 16 : kAttnWarps; }
+// groups up to 2 and of group 4 at head_dim 64 (their registers allow 17
+// warps a CTA; at head_dim 64 a group of 4 needs 16 warps to keep the
+// one-butterfly form), else 8 (measured: 16 warps slow group 4 at head_dim 128,
+// whose larger per-warp states leave the ring a stage fewer).
+constexpr int attn_warps(int hd, int G, bool cluster) {
+  return cluster && (G <= 2 || (G == 4 && hd == 64)) ? 16 : kAttnWarps;
+}
+int attn_consumer_warps(int hd, int G, bool cluster) { return attn_warps(hd, G, cluster); }
 
 size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster) {
   return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages +
-         AttnLayout{hd, G, attn_consumer_warps(G, cluster)}.total();
+         AttnLayout{hd, G, attn_consumer_warps(hd, G, cluster)}.total();
 }
 
 template <int PRO, int EPI, bool Q4>
@@ -113,6 +118,10 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams
                          : attn_split<HD>(pos, p.nkv, b, nb);
   if (tid == 0) ring_init(R, NW);
   __syncthreads();
+  // cluster: the CTAs push their records into each other's shared memory at
+  // the end; this first cluster barrier phase (waited for before the first
+  // push) makes sure every CTA of the cluster is running by then
+  if (CL) cluster_arrive_relaxed();
 
   if (warp == NW) {
     if (lane == 0) {
@@ -130,9 +139,9 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams
       l2_ahead(p.ahead, b);
 #endif
     }
-    if (CL) {  // the producer warp takes part in the consumers' two cluster barriers
+    if (CL) {  // the producer warp takes part in the consumers' two cluster barrier phases
       __syncwarp();
-      cluster_sync_all();
+      cluster_wait();
       cluster_sync_all();
     }
     return;
@@ -539,7 +548,7 @@ const void* gemv_kernel_ptr(int pro, int epi, bool q4) {
 const void* attn_kernel_ptr(int hd, int G, bool cluster) {
 #define TLD_ATTN(H_, G_)                                                                       \
   if (hd == H_ && G == G_)                                                                    \
-    return cluster ? (const void*)attn_decode<H_, G_, true, (G_ <= 4 ? 16 : kAttnWarps)>  \
+    return cluster ? (const void*)attn_decode<H_, G_, true, attn_warps(H_, G_, true)>     \
                    : (const void*)attn_decode<H_, G_, false, kAttnWarps>;
   TLD_ATTN(64, 1) TLD_ATTN(64, 2) TLD_ATTN(64, 4) TLD_ATTN(64, 8)
   TLD_ATTN(128, 1) TLD_ATTN(128, 2) TLD_ATTN(128, 4) TLD_ATTN(128, 8)
@@ -639,7 +648,7 @@ cudaError_t launch_attn(int hd, int G, const AttnParams& p, int grid, size_t sme
   AttnParams copy = p;
   void* args[] = {&copy};
   return launch_pdl(fn, args, grid, smem, s, pdl, p.cluster,
-                    (attn_consumer_warps(G, p.cluster > 0) + 1) * 32);
+                    (attn_consumer_warps(hd, G, p.cluster > 0) + 1) * 32);
 }
 
 cudaError_t launch_lm_head(const LmHeadParams& p, int grid, size_t smem, cudaStream_t s, bool pdl) {

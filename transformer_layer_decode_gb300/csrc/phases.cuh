@@ -796,7 +796,13 @@ struct AttnLayout {
   __host__ __device__ size_t rec_off() const { return 4 * (size_t)nw * G * (hd + 2); }
   __host__ __device__ size_t merge_off() const { return rec_off() + 4 * (size_t)G * (hd + 2); }
   // the record offsets of the splits of two heads, then the heads to merge
-  __host__ __device__ size_t total() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
+  __host__ __device__ size_t push_off() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
+  // cluster merge: the slice of every CTA's record this CTA merges, pushed by
+  // the other CTAs: [C][slice] values, then [C][G] (max, sum); at most
+  // G*hd + C*(32 + 2G) floats for any cluster size C
+  __host__ __device__ size_t total() const {
+    return push_off() + 4 * ((size_t)G * hd + (size_t)kMaxCluster * (32 + 2 * G));
+  }
 };
 
 // This CTA's share of the attention units at KV length n.
@@ -1012,6 +1018,28 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   // covered whole is normalised into o, a split head leaves a partial record
   // (acc, m, l), merged after the loop by the last CTA of the head to finish.
   int split_heads[2] = {-1, -1};
+  // Cluster merge by pushing (no XG): element e of the group's G*HD outputs is
+  // merged by the CTA owning its 32-block (rank order of whole blocks); each
+  // CTA writes its (acc) for e into that CTA's slot of the pushed slices, and
+  // its (max, sum) of every head into every CTA.
+  const int cC = CL ? p.cluster : 1, cr_rank = CL ? (int)cluster_rank() : 0;
+  constexpr int NBLK = G * HD / 32;
+  const int MS = 32 * ((NBLK + cC - 1) / cC);  // largest slice
+  float* pv = reinterpret_cast<float*>(work + AttnLayout{HD, G, NW}.push_off());  // [C][MS]
+  float* pml = pv + (size_t)cC * MS;                                               // [C][G][2]
+  auto push_record = [&](int gg, int j, float A, float M, float Ls) {
+    const int e = gg * HD + j, rr = split_owner32(NBLK, cC, e >> 5);
+    const int k = e - 32 * split_begin32(NBLK, cC, rr);
+    if (!TLD_IN_BOUNDS(rr >= 0 && rr < cC && k >= 0 && k < MS, p.err)) return;
+    dsmem_st(dsmem_addr(pv + (size_t)cr_rank * MS + k, (uint32_t)rr), A);
+    if (j == 0)
+      for (int c2 = 0; c2 < cC; ++c2) {
+        const float* ml = pml + ((size_t)cr_rank * G + gg) * 2;
+        dsmem_st(dsmem_addr(ml, (uint32_t)c2), M);
+        dsmem_st(dsmem_addr(ml + 1, (uint32_t)c2), Ls);
+      }
+  };
+  if (CL && !XG) cluster_wait();  // every CTA of the cluster is running before the first push
   auto end_segment = [&](int g) {
     if (FAST) {
 #pragma unroll
@@ -1046,7 +1074,9 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         A += wr[j] * e;
         Ls += wr[HD + 1] * e;
       }
-      if (CL) {  // this CTA's record, in its own shared memory
+      if (CL && !XG) {  // into the shared memory of the CTA that merges element (gg, j)
+        push_record(gg, j, A, M, Ls);
+      } else if (CL) {  // this CTA's record, in its own shared memory
         float* cr = crec + gg * (HD + 2);
         cr[j] = A;
         if (j == 0) {
@@ -1075,7 +1105,11 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
 
   reset();
   if (CL && nu == 0) {  // no chunk of the head: an empty record
-    for (int i = tid; i < G * (HD + 2); i += NC) crec[i] = (i % (HD + 2) == HD) ? -INFINITY : 0.f;
+    if (XG) {
+      for (int i = tid; i < G * (HD + 2); i += NC) crec[i] = (i % (HD + 2) == HD) ? -INFINITY : 0.f;
+    } else {
+      for (int i = tid; i < G * HD; i += NC) push_record(i / HD, i % HD, 0.f, -INFINITY, 0.f);
+    }
   }
   bool ok = true;
   int g = u0 / cph, c = u0 - g * cph;
@@ -1236,7 +1270,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         ok = false;
       }
     } else {
-      cluster_sync_all();  // every CTA's record is in its shared memory
+      cluster_sync_all();  // every CTA's pushes are in this CTA's shared memory
     }
     // whole 32-element blocks per CTA (a warp finishes one block at a time)
     const int e0 = 32 * split_begin32(G * HD / 32, C, r), e1 = 32 * split_begin32(G * HD / 32, C, r + 1);
@@ -1244,16 +1278,25 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       const int gg = e / HD, j = e - gg * HD;
       // two passes over the cluster's records in rank order: the largest
       // running max, then the rescaled sums (no per-record arrays in registers)
-      float M = -INFINITY;
-      for (int c2 = 0; c2 < C; ++c2)
-        M = fmaxf(M, dsmem_ld(dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2) + 4 * HD));
-      float Lsum = 0.f, o = 0.f;
-      for (int c2 = 0; c2 < C; ++c2) {
-        const uint32_t a = dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2);
-        const float mv = dsmem_ld(a + 4 * HD);
-        const float w = (mv == -INFINITY) ? 0.f : expf(mv - M);
-        Lsum = fmaf(dsmem_ld(a + 4 * (HD + 1)), w, Lsum);
-        o = fmaf(dsmem_ld(a + 4 * j), w, o);
+      float M = -INFINITY, Lsum = 0.f, o = 0.f;
+      if (XG) {  // pulled from the other CTAs' records
+        for (int c2 = 0; c2 < C; ++c2)
+          M = fmaxf(M, dsmem_ld(dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2) + 4 * HD));
+        for (int c2 = 0; c2 < C; ++c2) {
+          const uint32_t a = dsmem_addr(crec + gg * (HD + 2), (uint32_t)c2);
+          const float mv = dsmem_ld(a + 4 * HD);
+          const float w = (mv == -INFINITY) ? 0.f : expf(mv - M);
+          Lsum = fmaf(dsmem_ld(a + 4 * (HD + 1)), w, Lsum);
+          o = fmaf(dsmem_ld(a + 4 * j), w, o);
+        }
+      } else {  // pushed into this CTA's shared memory
+        for (int c2 = 0; c2 < C; ++c2) M = fmaxf(M, pml[((size_t)c2 * G + gg) * 2]);
+        for (int c2 = 0; c2 < C; ++c2) {
+          const float mv = pml[((size_t)c2 * G + gg) * 2];
+          const float w = (mv == -INFINITY) ? 0.f : expf(mv - M);
+          Lsum = fmaf(pml[((size_t)c2 * G + gg) * 2 + 1], w, Lsum);
+          o = fmaf(pv[(size_t)c2 * MS + (e - e0)], w, o);
+        }
       }
       const size_t oi = (size_t)(gh * G + gg) * HD + j;
       if (XG) {  // into every CTA's copy of o_g
@@ -1280,8 +1323,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
       }
       return ok;
     }
-    cluster_sync_all();  // the records stay until every CTA of the cluster has read them
-    return ok;
+    return ok;  // nothing is read from another CTA after the barrier
   }
 
   // ---- heads split over CTAs: the last CTA to finish merges them --------------
