@@ -4,7 +4,9 @@
 // the same way from RN(1/127).  This checks, in IEEE fp32 on the host (no
 // contraction but the explicit fused multiply-adds), that scale and codes equal
 // those of the IEEE division for random inputs and for quotients placed next to
-// the rounding boundaries k + 1/2.
+// the rounding boundaries k + 1/2; and that no code of an element |z| <= amax,
+// the block's absmax itself included, leaves [-127, 127] before clamping (the
+// kernels skip the clamp on that path).
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -31,7 +33,7 @@ static double uni() {  // SplitMix64 -> [0, 1)
 }
 
 int main() {
-  long bad_d = 0, bad_q = 0, bad_div = 0, n = 0;
+  long bad_d = 0, bad_q = 0, bad_div = 0, n = 0, beyond = 0;
   const float r127 = 1.0f / 127.0f;
   for (int t = 0; t < 2000000; ++t) {
     const float amax = (float)std::exp(std::log(1e-30) + uni() * (std::log(1e6) - std::log(1e-30)));
@@ -47,16 +49,18 @@ int main() {
     bits += (int)(uni() * 9.0) - 4;
     std::memcpy(&zb, &bits, 4);
     if (uni() < 0.5) zb = -zb;
-    for (float x : {z, zb}) {
+    for (float x : {z, zb, amax, -amax}) {
       if (std::fabs(x) > amax) continue;
       ++n;
       const float qm = div_rn_from_rcp(x, d, rd), qi = x / d;
       if (qm != qi) ++bad_div;
       if (code_of(qm) != code_of(qi)) ++bad_q;
+      if (std::fabs(std::nearbyintf(qm)) > 127.0f) ++beyond;
     }
   }
-  std::printf("scales differing %ld; quotients differing %ld, codes differing %ld of %ld\n",
-              bad_d, bad_div, bad_q, n);
-  std::printf(bad_d || bad_q || bad_div ? "FAILED\n" : "OK\n");
-  return bad_d || bad_q || bad_div ? 1 : 0;
+  std::printf("scales differing %ld; quotients differing %ld, codes differing %ld, "
+              "unclamped codes beyond +-127 %ld of %ld\n", bad_d, bad_div, bad_q, beyond, n);
+  const bool bad = bad_d || bad_q || bad_div || beyond;
+  std::printf(bad ? "FAILED\n" : "OK\n");
+  return bad ? 1 : 0;
 }

@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_headproj(const AttnHeadProjP
   float* dx = reinterpret_cast<float*>(work + L.dx_off());
   int* sx = reinterpret_cast<int*>(work + L.sx_off());
   if (Q4) {
-    quantize_blocks(og, Kg, qx, dx, sx, (r == 0 && p.qtap) ? p.qtap + (size_t)gh * Kg : nullptr,
+    quantize_blocks<false>(og, Kg, qx, dx, sx, (r == 0 && p.qtap) ? p.qtap + (size_t)gh * Kg : nullptr,
                     (r == 0 && p.qstap) ? p.qstap + (size_t)gh * (Kg / 32) : nullptr, tid, kNC,
                     1.0f);
     named_barrier(1, kNC);

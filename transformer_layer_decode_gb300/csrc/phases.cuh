@@ -234,9 +234,15 @@ __device__ __forceinline__ float div_rn_from_rcp(float a, float b, float rb) {
 // fp32 quotient z / d, clamped to +-127, formed from the block's reciprocal as
 // above (three operations instead of a division).  Eight lanes a block, four
 // elements a lane; each lane group takes kQuantBlocks blocks at once so that
-// their shuffle and arithmetic chains overlap.
-constexpr int kQuantBlocks = 4;
+// their shuffle and arithmetic chains overlap (measured on the int4 7B-shape
+// stack: two blocks beat one, three and four, by 3.4 us per layer, as a
+// 4096-element vector then keeps all sixteen warps busy).
+#ifndef TLD_QUANT_BLOCKS
+#define TLD_QUANT_BLOCKS 2
+#endif
+constexpr int kQuantBlocks = TLD_QUANT_BLOCKS;
 
+template <bool SCALED = true>
 __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, float* dx, int* sx,
                                        int8_t* qtap, float* qstap, int tid, int NC, float scale) {
   const int lane = tid & 31, sub = lane & 7, warp = tid >> 5;
@@ -252,10 +258,12 @@ __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, floa
       const int blk = base + r * 4 + (lane >> 3);
       z[r] = blk < nblk ? *reinterpret_cast<const float4*>(xs + blk * 32 + sub * 4)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
-      z[r].x *= scale;
-      z[r].y *= scale;
-      z[r].z *= scale;
-      z[r].w *= scale;
+      if (SCALED) {
+        z[r].x *= scale;
+        z[r].y *= scale;
+        z[r].z *= scale;
+        z[r].w *= scale;
+      }
       amax[r] = fmaxf(fmaxf(fabsf(z[r].x), fabsf(z[r].y)), fmaxf(fabsf(z[r].z), fabsf(z[r].w)));
     }
 #pragma unroll
@@ -271,11 +279,11 @@ __device__ inline void quantize_blocks(const float* xs, int K, uint8_t* qx, floa
       if (amax[r] >= 1e-30f) {
         d = div_rn_from_rcp(amax[r], 127.0f, r127);  // amax / 127
         const float rd = __frcp_rn(d);
+        // no clamp needed: |z| <= amax and d >= (amax / 127)(1 - 2^-24), so
+        // |z / d| <= 127 (1 + 2^-23) and its rounded fp32 quotient rounds to
+        // at most 127
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int v = __float2int_rn(div_rn_from_rcp(zz[i], d, rd));
-          q[r][i] = v > 127 ? 127 : (v < -127 ? -127 : v);
-        }
+        for (int i = 0; i < 4; ++i) q[r][i] = __float2int_rn(div_rn_from_rcp(zz[i], d, rd));
       } else {  // a block so small that 1/d would overflow (or all zero): IEEE divisions
         d = __fdiv_rn(amax[r], 127.0f);
 #pragma unroll
@@ -578,8 +586,12 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   }
   if (Q4 && !qin) {
     // the normalised vector itself is quantised: the codes carry the RMS scale
-    quantize_blocks(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid, kNC,
-                    rnorm);
+    if (PRO == PRO_NORM)
+      quantize_blocks<true>(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid,
+                            kNC, rnorm);
+    else  // the plain input: no scale
+      quantize_blocks<false>(xs, K, W.qx, W.dx, W.sx, first_cta ? io.qtap : nullptr, io.qstap, tid,
+                             kNC, 1.f);
     rnorm = 1.f;
     named_barrier(1, kNC);
   }
