@@ -62,7 +62,10 @@ constexpr int kMaxSplits = 32;
 constexpr int kCopiesPerStage = TLD_COPIES_PER_STAGE;  // bulk copies a GEMV stage is issued as
 constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
 constexpr int kMaxCluster = 16;            // CTAs per KV head in the cluster attention
-constexpr int kStageTiles = 16;  // a GEMV stage: 16 tiles (32 KB bf16, 36 KB int4)
+#ifndef TLD_STAGE_TILES
+#define TLD_STAGE_TILES 16
+#endif
+constexpr int kStageTiles = TLD_STAGE_TILES;  // a GEMV stage: 16 tiles (32 KB bf16, 36 KB int4)
 constexpr int kTilesPerWarp = kStageTiles / kConsumerWarps;
 static_assert(kStageTiles % kConsumerWarps == 0, "every consumer warp takes whole tiles of a stage");
 constexpr int kTileBytes = kTileR * kTileK * 2;                          // 2 KB
