@@ -638,17 +638,10 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
                             my[j].offset(geo) - st_off + geo.tile_bytes <= R.slot_bytes, p.err)) {
         const uint8_t* tp = R.slot(P.slot) + (my[j].offset(geo) - st_off);
         if (Q4) {
-#ifdef TLD_LDS_ASM
-          const uint32_t ta = smem_u32(tp);
-#pragma unroll
-          for (int r = 0; r < kTileR; ++r) wv[j][r] = lds_u4(ta + (uint32_t)(r * (kw / 2) + lane * 16));
-          scl[j] = lds_u2(ta + (uint32_t)(kTileR * (kw / 2) + lane * 8));
-#else
 #pragma unroll
           for (int r = 0; r < kTileR; ++r)
             wv[j][r] = *reinterpret_cast<const uint4*>(tp + (size_t)r * (kw / 2) + lane * 16);
           scl[j] = *reinterpret_cast<const uint2*>(tp + (size_t)kTileR * (kw / 2) + lane * 8);
-#endif
         } else {
 #pragma unroll
           for (int r = 0; r < kTileR; ++r)
@@ -684,13 +677,8 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
       if (c >= kw) continue;
       if (Q4) {
         const int blk = kt * (kTileKQ4 / 32) + lane;
-#ifdef TLD_LDS_ASM
-        const uint32_t xa = smem_u32(W.qx + blk * 32);
-        const uint4 x0 = lds_u4(xa), x1 = lds_u4(xa + 16);
-#else
         const uint4 x0 = *reinterpret_cast<const uint4*>(W.qx + blk * 32);
         const uint4 x1 = *reinterpret_cast<const uint4*>(W.qx + blk * 32 + 16);
-#endif
         const float dxb = W.dx[blk];
         const int sxb = W.sx[blk];
         const uint32_t sc2[2] = {scl[j].x, scl[j].y};
