@@ -305,6 +305,10 @@ __device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
 }
 
 // Makes generic-proxy writes visible to later bulk copies (async proxy) of this thread.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }

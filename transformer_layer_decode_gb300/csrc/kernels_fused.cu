@@ -37,8 +37,8 @@ size_t gemv_smem_bytes(int K, bool q4, int nstages, int max_rb_local) {
 // Consumer warps of the attention kernel: 16 for the cluster kernels of GQA
 // groups up to 2 and of group 4 at head_dim 64 (their registers allow 17
 // warps a CTA; at head_dim 64 a group of 4 needs 16 warps to keep the
-// one-butterfly form), else 8 (measured: 16 warps slow group 4 at head_dim 128,
-// whose larger per-warp states leave the ring a stage fewer).
+// one-butterfly form), else 8 (measured: 16 warps slow group 4 at head_dim 128
+// by 2 %, with or without a ring stage fewer).
 constexpr int attn_warps(int hd, int G, bool cluster) {
   return cluster && (G <= 2 || (G == 4 && hd == 64)) ? 16 : kAttnWarps;
 }
@@ -46,7 +46,7 @@ int attn_consumer_warps(int hd, int G, bool cluster) { return attn_warps(hd, G, 
 
 size_t attn_smem_bytes(int hd, int G, int nstages, bool cluster) {
   return (size_t)nstages * kAttnStageBytes + 16 * (size_t)nstages +
-         AttnLayout{hd, G, attn_consumer_warps(hd, G, cluster)}.total();
+         AttnLayout{hd, G, attn_consumer_warps(hd, G, cluster), cluster}.total();
 }
 
 template <int PRO, int EPI, bool Q4>

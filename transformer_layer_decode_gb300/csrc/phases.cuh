@@ -805,7 +805,8 @@ constexpr int ilog2(int v) { return v <= 1 ? 0 : 1 + ilog2(v / 2); }
 // (cluster merge) | merge scratch (global merge).
 struct AttnLayout {
   int hd, G, nw = kConsumerWarps;  // nw: consumer warps of the kernel
-  __host__ __device__ size_t rec_off() const { return 4 * (size_t)nw * G * (hd + 2); }
+  bool ring_ws = false;            // per-warp states in the drained ring (cluster kernel)
+  __host__ __device__ size_t rec_off() const { return ring_ws ? 0 : 4 * (size_t)nw * G * (hd + 2); }
   __host__ __device__ size_t merge_off() const { return rec_off() + 4 * (size_t)G * (hd + 2); }
   // the record offsets of the splits of two heads, then the heads to merge
   __host__ __device__ size_t push_off() const { return merge_off() + 4 * (size_t)2 * kMaxSplits + 16; }
@@ -1007,8 +1008,13 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   constexpr bool FAST = V <= 32;
   constexpr int LV = FAST ? ilog2(V) : 0, LPW = ilog2(PW), SH = 5 - LV;
   const int warp = tid >> 5, lane = tid & 31;
-  float* ws = reinterpret_cast<float*>(work);  // [warp][G][HD+2]
-  float* crec = reinterpret_cast<float*>(work + AttnLayout{HD, G, NW}.rec_off());  // [G][HD+2]
+  // The cluster kernel (no XG) ends its only head segment after its last
+  // stage: its per-warp states go into the drained ring, so the work area need
+  // not hold them and the ring keeps its stages.
+  constexpr bool RING_WS = CL && !XG;
+  const AttnLayout AL{HD, G, NW, RING_WS};
+  float* ws = reinterpret_cast<float*>(RING_WS ? R.stages : work);  // [warp][G][HD+2]
+  float* crec = reinterpret_cast<float*>(work + AL.rec_off());  // [G][HD+2]
   const int n = S.n, cph = S.cph, U = S.U, u0 = S.u0, u1 = S.u1, nu = S.nu;
   float m[G], l[G], acc[G][DL];
   float m_mine = -INFINITY, l_mine = 0.f;  // fast form: this lane's head
@@ -1037,7 +1043,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   const int cC = CL ? p.cluster : 1, cr_rank = CL ? (int)cluster_rank() : 0;
   constexpr int NBLK = G * HD / 32;
   const int MS = 32 * ((NBLK + cC - 1) / cC);  // largest slice
-  float* pv = reinterpret_cast<float*>(work + AttnLayout{HD, G, NW}.push_off());  // [C][MS]
+  float* pv = reinterpret_cast<float*>(work + AL.push_off());  // [C][MS]
   float* pml = pv + (size_t)cC * MS;                                               // [C][G][2]
   auto push_record = [&](int gg, int j, float A, float M, float Ls) {
     const int e = gg * HD + j, rr = split_owner32(NBLK, cC, e >> 5);
@@ -1059,6 +1065,13 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
         m[gg] = __shfl_sync(0xffffffffu, m_mine, (gg * PW) << SH);
         l[gg] = __shfl_sync(0xffffffffu, l_mine, (gg * PW) << SH);
       }
+    }
+    if (RING_WS) {
+      // every warp is past its last stage (the bulk copies into the ring are
+      // complete and read) before the ring is written as plain shared memory
+      named_barrier(1, NC);
+      fence_proxy_async_shared();
+      if (!TLD_IN_BOUNDS((size_t)NW * G * (HD + 2) * 4 <= (size_t)R.n * R.slot_bytes, p.err)) return;
     }
 #pragma unroll
     for (int gg = 0; gg < G; ++gg) {
@@ -1341,7 +1354,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   // ---- heads split over CTAs: the last CTA to finish merges them --------------
   // (tickets are taken after this CTA's whole loop, so merging never stalls it;
   // the split arithmetic is 32-bit: units * grid stays far below 2^31)
-  int* mbase = reinterpret_cast<int*>(work + AttnLayout{HD, G, NW}.merge_off());  // [2][kMaxSplits]
+  int* mbase = reinterpret_cast<int*>(work + AL.merge_off());  // [2][kMaxSplits]
   int* todo = mbase + 2 * kMaxSplits;                                         // [2]: head, splits
   const int U32 = U;
   auto part_begin = [&](int c) { return split_begin32(U32, nb, c); };
