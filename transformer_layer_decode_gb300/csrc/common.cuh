@@ -236,24 +236,6 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// Packed fp32 pairs (sm_100 and later): two lanes of fp32 in one 64-bit register.
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  return (uint64_t)__float_as_uint(lo) | ((uint64_t)__float_as_uint(hi) << 32);
-}
-// The two bf16 of a 32-bit word as an fp32 pair (element 0 low, element 1 high).
-__device__ __forceinline__ uint64_t bf16pair(uint32_t w) {
-  return (uint64_t)(w << 16) | ((uint64_t)(w & 0xffff0000u) << 32);
-}
-// d = a * b + c on both halves, each rounded as one fp32 fma.
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ float unpack_f32x2_sum(uint64_t v) {
-  return __uint_as_float((uint32_t)v) + __uint_as_float((uint32_t)(v >> 32));
-}
-
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }

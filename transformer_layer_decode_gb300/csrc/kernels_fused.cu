@@ -19,11 +19,12 @@
 // contiguous run of whole 4-row blocks of the tiled weight matrix, i.e. one
 // contiguous slab of bytes, and streams it through a ring of 32 KB
 // shared-memory stages filled by 1-D bulk copies (TMA) issued by one producer
-// thread.  Eight consumer warps each take two 4-row x 256-column tiles per
-// stage, copy them to registers, hand the stage back, and accumulate against
-// the input vector held in shared memory in fp32.  Because CTAs own whole rows,
-// no partial sums cross CTAs.  Weights do not depend on the previous kernel:
-// the producer starts streaming at launch, before griddepcontrol.wait.
+// thread.  Sixteen consumer warps each take one 4-row tile per stage (256
+// columns bf16, 1024 int4), copy it to registers, hand the stage back, and
+// accumulate against the input vector held in shared memory in fp32.  Because
+// CTAs own whole rows, no partial sums cross CTAs.  Weights do not depend on
+// the previous kernel: the producer starts streaming at launch, before
+// griddepcontrol.wait.
 #include "phases.cuh"
 
 namespace tld {
@@ -126,18 +127,8 @@ __global__ void __launch_bounds__((NW + 1) * 32, 1) attn_decode(const AttnParams
   if (warp == NW) {
     if (lane == 0) {
       RingPos P{0, 0, 0};
-#ifdef TLD_ATTN_EARLY_AHEAD
-      // once the ring is full: the chunks still to come into L2, then the next
-      // kernel's share, both behind this CTA's first stages
-      attn_produce<HD>(p, p.kc, p.vc, R, P, S, policy_evict_first(), [] { pdl_wait(); },
-                       [&](int from) {
-                         l2_prefetch_chunks<HD>(p, S, from);
-                         l2_ahead(p.ahead, b);
-                       });
-#else
       attn_produce<HD>(p, p.kc, p.vc, R, P, S, policy_evict_first(), [] { pdl_wait(); });
       l2_ahead(p.ahead, b);
-#endif
     }
     if (CL) {  // the producer warp takes part in the consumers' two cluster barrier phases
       __syncwarp();
@@ -289,20 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_oproj_fused(const AttnOprojP
     if (lane == 0) {
       RingPos P{0, 0, 0};
       const uint64_t pol = policy_evict_first();
-#ifdef TLD_ATTN_EARLY_AHEAD
-      // once the ring is full: the chunks still to come and this CTA's Wo slab
-      // into L2, behind the first stages, so the o-proj phase reads L2
-      attn_produce<HD>(p.attn, p.attn.kc, p.attn.vc, R, P, S, pol, [] { pdl_wait(); },
-                       [&](int from) {
-                         l2_prefetch_chunks<HD>(p.attn, S, from);
-                         const int64_t o0 = (int64_t)rb0 * p.o.geo.rb_bytes;
-                         const int64_t n = (int64_t)(rb1 - rb0) * p.o.geo.rb_bytes;
-                         for (int64_t q = 0; q < n; q += kStageBytes)
-                           bulk_prefetch_l2(p.o.w + o0 + q, (uint32_t)min((int64_t)kStageBytes, n - q) & ~15u);
-                       });
-#else
       attn_produce<HD>(p.attn, p.attn.kc, p.attn.vc, R, P, S, pol, [] { pdl_wait(); });
-#endif
       gemv_produce(p.o, p.o.w, R, P, rb0, rb1, pol);
       l2_ahead(p.o.ahead, b);
     }

@@ -600,11 +600,6 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
   float acc[kTileR];
 #pragma unroll
   for (int r = 0; r < kTileR; ++r) acc[r] = 0.f;
-#ifdef TLD_F32X2
-  uint64_t acc2[kTileR];
-#pragma unroll
-  for (int r = 0; r < kTileR; ++r) acc2[r] = 0ull;
-#endif
   bool ok = true;
   // cursors: the first tile of the current stage and this warp's two tiles in it
   TileCursor st_cur{rb0, 0};
@@ -657,13 +652,6 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
       if (li >= nloc) continue;
       const int rb = my[j].rb, kt = my[j].kt;
       if (rb != cur_rb) {
-#ifdef TLD_F32X2
-#pragma unroll
-        for (int r = 0; r < kTileR; ++r) {
-          acc[r] += unpack_f32x2_sum(acc2[r]);
-          acc2[r] = 0ull;
-        }
-#endif
         if (cur_rb >= 0) {
           const float v = warp_reduce4(acc, lane);
           if ((lane & 7) == 0)
@@ -693,18 +681,6 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
       } else {
         const float4 xa = *reinterpret_cast<const float4*>(xs + kt * kTileK + c);
         const float4 xb = *reinterpret_cast<const float4*>(xs + kt * kTileK + c + 4);
-#ifdef TLD_F32X2
-#pragma unroll
-        for (int r = 0; r < kTileR; ++r) {
-          // even and odd columns in the two halves of a packed fp32 pair
-          uint64_t a2 = acc2[r];
-          a2 = fma_f32x2(bf16pair(wv[j][r].x), pack_f32x2(xa.x, xa.y), a2);
-          a2 = fma_f32x2(bf16pair(wv[j][r].y), pack_f32x2(xa.z, xa.w), a2);
-          a2 = fma_f32x2(bf16pair(wv[j][r].z), pack_f32x2(xb.x, xb.y), a2);
-          a2 = fma_f32x2(bf16pair(wv[j][r].w), pack_f32x2(xb.z, xb.w), a2);
-          acc2[r] = a2;
-        }
-#else
 #pragma unroll
         for (int r = 0; r < kTileR; ++r) {
           float a = acc[r];
@@ -718,7 +694,6 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
           a = fmaf(bf16hi(wv[j][r].w), xb.w, a);
           acc[r] = a;
         }
-#endif
       }
     }
     st_cur.advance(kStageTiles, geo.ktiles);
@@ -726,10 +701,6 @@ __device__ __forceinline__ bool gemv_main(const GemvParams& p, const GemvIO& io,
     for (int j = 0; j < kTilesPerWarp; ++j) my[j].advance(kStageTiles, geo.ktiles);
     P.next(R.n);
   }
-#ifdef TLD_F32X2
-#pragma unroll
-  for (int r = 0; r < kTileR; ++r) acc[r] += unpack_f32x2_sum(acc2[r]);
-#endif
   if (cur_rb >= 0) {
     const float v = warp_reduce4(acc, lane);
     if ((lane & 7) == 0)
@@ -918,25 +889,14 @@ struct RowSlice {
 // Producer of an attention phase: this CTA's chunks.  wait_pos() is called
 // once before the first chunk that holds the row appended by this step's QKV
 // phase (the other rows were written by earlier steps).
-struct NoHook {
-  __device__ void operator()(int) const {}
-};
-
-template <int HD, class WaitPos, class RingFull = NoHook>
+template <int HD, class WaitPos>
 __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t* kc,
                                              const uint16_t* vc, const Ring& R, RingPos& P,
-                                             const AttnSplit& S, uint64_t pol, WaitPos&& wait_pos,
-                                             RingFull&& ring_full = RingFull{}) {
+                                             const AttnSplit& S, uint64_t pol, WaitPos&& wait_pos) {
   constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
-  bool waited = false, full = false;
+  bool waited = false;
   int g = S.u0 / S.cph, c = S.u0 - g * S.cph;
   for (int s = 0; s < S.nu; ++s) {
-    // the ring is full: whatever the producer issues now (the hook) queues
-    // behind this CTA's first stages, ahead of the ones still to come
-    if (!full && P.count >= R.n) {
-      ring_full(s);
-      full = true;
-    }
     if (!ring_reserve(R, P, p.err)) return;
     const int rows = min(CH, S.n - c * CH);
     if (!TLD_IN_BOUNDS(g >= 0 && g < p.nkv && rows > 0 && c * CH + rows <= p.max_ctx &&
@@ -957,24 +917,6 @@ __device__ __forceinline__ void attn_produce(const AttnParams& p, const uint16_t
       ++g;
     }
     P.next(R.n);
-  }
-  if (!full) ring_full(S.nu);
-}
-
-// L2 prefetch of this CTA's attention chunks from chunk index `from` on (the
-// ones that wait for a ring slot).
-template <int HD>
-__device__ void l2_prefetch_chunks(const AttnParams& p, const AttnSplit& S, int from) {
-  constexpr int CH = kAttnStageBytes / 2 / (HD * 2);
-  for (int s = from; s < S.nu; ++s) {
-    const int u = S.u0 + s, g = u / S.cph, c = u - g * S.cph;
-    const int rows = min(CH, S.n - c * CH);
-    const size_t off = (size_t)kv_row_offset(p.pages, CH, p.nkv, p.max_ctx, HD, g, c * CH);
-    const uint32_t bytes = ((uint32_t)rows * HD * 2) & ~15u;
-    if (bytes) {
-      bulk_prefetch_l2(p.kc + off, bytes);
-      bulk_prefetch_l2(p.vc + off, bytes);
-    }
   }
 }
 
