@@ -59,7 +59,12 @@ constexpr int kMaxSplits = 32;
 #ifndef TLD_COPIES_PER_STAGE
 #define TLD_COPIES_PER_STAGE 4
 #endif
-constexpr int kCopiesPerStage = TLD_COPIES_PER_STAGE;  // bulk copies a GEMV stage is issued as
+#ifndef TLD_COPIES_PER_STAGE_Q4
+#define TLD_COPIES_PER_STAGE_Q4 8
+#endif
+// bulk copies a GEMV stage is issued as (bf16, int4)
+constexpr int kCopiesPerStage = TLD_COPIES_PER_STAGE;
+constexpr int kCopiesPerStageQ4 = TLD_COPIES_PER_STAGE_Q4;
 constexpr int kL2AheadBytes = 256 * 1024;  // L2 look-ahead per CTA and kernel
 constexpr int kMaxCluster = 16;            // CTAs per KV head in the cluster attention
 #ifndef TLD_STAGE_TILES
@@ -78,6 +83,7 @@ struct TileGeom {
   int K, tile_k, ktiles, kw_last;
   int64_t rb_bytes, tile_bytes;
   int stage_bytes;
+  int copies;  // bulk copies a stage is issued as
 };
 
 __host__ __device__ inline TileGeom tile_geom(int K, bool q4) {
@@ -89,6 +95,7 @@ __host__ __device__ inline TileGeom tile_geom(int K, bool q4) {
   g.rb_bytes = q4 ? (int64_t)kTileR * (K / 2 + K / 16) : (int64_t)kTileR * K * 2;
   g.tile_bytes = q4 ? kTileBytesQ4 : kTileBytes;
   g.stage_bytes = q4 ? kStageBytesQ4 : kStageBytes;
+  g.copies = q4 ? kCopiesPerStageQ4 : kCopiesPerStage;
   return g;
 }
 
