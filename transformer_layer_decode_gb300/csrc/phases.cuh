@@ -413,13 +413,22 @@ __device__ __forceinline__ int q4_block_dot(const uint4 w, const uint4 x0, const
 // several copies in flight move a stage into shared memory faster than one
 // large copy (measured on the 7B-shape stacks: four for bf16 stages, +1.7 %
 // over one; eight for int4 stages, +2.7 % over four, where eight slow bf16).
-__device__ __forceinline__ void bulk_g2s_split(uint8_t* dst, const uint8_t* src, uint32_t bytes,
-                                               uint64_t* bar, uint64_t pol, int copies) {
-  const uint32_t part = (bytes / (uint32_t)copies) & ~15u;
+template <int COPIES>
+__device__ __forceinline__ void bulk_g2s_split_n(uint8_t* dst, const uint8_t* src, uint32_t bytes,
+                                                 uint64_t* bar, uint64_t pol) {
+  const uint32_t part = (bytes / COPIES) & ~15u;
   uint32_t o = 0;
   if (part > 0)
-    for (int k = 0; k < copies - 1; ++k, o += part) bulk_g2s_hint(dst + o, src + o, part, bar, pol);
+#pragma unroll
+    for (int k = 0; k < COPIES - 1; ++k, o += part) bulk_g2s_hint(dst + o, src + o, part, bar, pol);
   bulk_g2s_hint(dst + o, src + o, bytes - o, bar, pol);
+}
+__device__ __forceinline__ void bulk_g2s_split(uint8_t* dst, const uint8_t* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t pol, int copies) {
+  if (copies == kCopiesPerStageQ4)
+    bulk_g2s_split_n<kCopiesPerStageQ4>(dst, src, bytes, bar, pol);
+  else
+    bulk_g2s_split_n<kCopiesPerStage>(dst, src, bytes, bar, pol);
 }
 
 // Producer of a GEMV phase: this CTA's slab, whole row blocks [rb0, rb1).
