@@ -25,3 +25,47 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == "layer_h512"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def _traffic_records():
+    prof = os.path.join(ROOT, "profiles")
+    return sorted(os.path.join(prof, f) for f in os.listdir(prof)
+                  if f.startswith("traffic_") and f.endswith(".json"))
+
+
+def test_traffic_records_are_whole_and_consistent():
+    """Each committed DRAM-traffic record names its kernel, workload, the ncu
+    command (clocks left alone, committed files only), the source hash it was
+    taken on, and bytes that add up: read + write = per launch, and at least
+    the kernel's algorithmic bytes (the stream is read once; the excess is the
+    look-ahead of the next kernel's bytes)."""
+    recs = _traffic_records()
+    assert recs
+    for p in recs:
+        d = json.load(open(p))
+        for key in ("kernel", "workload", "dram_bytes_per_launch", "dram_bytes_read",
+                    "dram_bytes_write", "algorithmic_bytes_per_launch", "kernel_source_sha",
+                    "command"):
+            assert key in d, (p, key)
+        name = os.path.basename(p)[len("traffic_"):-len(".json")]
+        assert name.endswith(d["workload"].split()[0]), (p, d["workload"])
+        tot = d["dram_bytes_read"] + d["dram_bytes_write"]
+        assert abs(d["dram_bytes_per_launch"] - tot) <= 1e5 + 1e-6 * tot, p
+        assert d["dram_bytes_per_launch"] >= d["algorithmic_bytes_per_launch"], p
+        cmd = d["command"]
+        assert "--clock-control none" in cmd and "python bench.py" in cmd, p
+        assert "/root" not in cmd and "_work" not in cmd, p
+        assert len(d["kernel_source_sha"]) == 16, p
+
+
+def test_bench_reports_traffic_only_for_matching_sources(monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    p = _traffic_records()[0]
+    d = json.load(open(p))
+    kernel, workload = os.path.basename(p)[len("traffic_"):-len(".json")].rsplit("_stack", 1)
+    workload = "stack" + workload
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda: d["kernel_source_sha"])
+    assert bench.profiled_traffic(workload, kernel) == d["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_sha", lambda: "0" * 16)
+    assert bench.profiled_traffic(workload, kernel) is None
