@@ -53,6 +53,9 @@ constexpr int kAttnWarps = 8;
 #endif
 constexpr int kSmemBudget = TLD_SMEM_BUDGET_KB * 1024;
 constexpr int kAttnStageBytes = 32768;  // K chunk + V chunk, 16 KB each
+// Online softmax: a head's reference max moves only when a score exceeds it by
+// more than this (natural-log units: the weights stay below e^8 ~ 3e3).
+constexpr float kAttnRescaleSlack = 8.f;
 constexpr int kTimelineSlots = 8;       // u64 per launch of the timeline probe
 // Most attention CTAs one KV head may be split over (bounds the merge).
 constexpr int kMaxSplits = 32;

@@ -953,8 +953,10 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   // Fast form (PW * G <= 32 partial dots per lane): one reduce-scatter
   // butterfly sums all of a chunk's dots, leaving lane l the total of dot
   // number (l >> SH) & (V - 1), dot v = (head gg, position i) at v = gg*PW + i;
-  // each lane then runs the online softmax for its own (position, head), and
-  // the running max / sum of head gg live in the lanes of that head.
+  // each lane then runs the online softmax for its own (position, head): the
+  // reference max of head gg is shared by the lanes of that head, the sum of
+  // the weights is kept per (position, head) and summed over the positions
+  // when the segment ends.
   constexpr int V = PW * G;
   constexpr bool FAST = V <= 32;
   constexpr int LV = FAST ? ilog2(V) : 0, LPW = ilog2(PW), SH = 5 - LV;
@@ -968,7 +970,7 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   float* crec = reinterpret_cast<float*>(work + AL.rec_off());  // [G][HD+2]
   const int n = S.n, cph = S.cph, U = S.U, u0 = S.u0, u1 = S.u1, nu = S.nu;
   float m[G], l[G], acc[G][DL];
-  float m_mine = -INFINITY, l_mine = 0.f;  // fast form: this lane's head
+  float m_mine = -INFINITY, l_mine = 0.f;  // fast form: head's reference max, slot's sum
   const int my_v = (lane >> SH) & (V - 1), my_i = my_v % PW;
   int cur_g = -1, seg_idx = 0;
   auto reset = [&]() {
@@ -1011,10 +1013,13 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
   if (CL && !XG) cluster_wait();  // every CTA of the cluster is running before the first push
   auto end_segment = [&](int g) {
     if (FAST) {
+      float lsum = l_mine;  // over the positions of this lane's head
+#pragma unroll
+      for (int bt = 0; bt < LPW; ++bt) lsum += __shfl_xor_sync(0xffffffffu, lsum, 1 << (SH + bt));
 #pragma unroll
       for (int gg = 0; gg < G; ++gg) {
         m[gg] = __shfl_sync(0xffffffffu, m_mine, (gg * PW) << SH);
-        l[gg] = __shfl_sync(0xffffffffu, l_mine, (gg * PW) << SH);
+        l[gg] = __shfl_sync(0xffffffffu, lsum, (gg * PW) << SH);
       }
     }
     if (RING_WS) {
@@ -1150,23 +1155,28 @@ __device__ __forceinline__ bool attn_main(const AttnParams& p, uint8_t* work, co
 #pragma unroll
       for (int o = 16 >> LV; o > 0; o >>= 1) x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
       const float sc = (warp + my_i * NW < rows) ? x[0] : -INFINITY;
-      float mx = sc;
+      // Lazy rescaling: a head's reference max m_mine moves only when one of
+      // its scores exceeds it by more than kAttnRescaleSlack, so most chunks
+      // need no max, no rescale and no cross-lane sum.  The weights
+      // exp(s - m_mine) stay below e^slack, and acc / l is the same ratio
+      // whichever reference both carry.
+      if (__any_sync(0xffffffffu, sc > m_mine + kAttnRescaleSlack)) {  // warp-uniform
+        float mx = sc;
 #pragma unroll
-      for (int bt = 0; bt < LPW; ++bt) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1 << (SH + bt)));
-      const float m_new = fmaxf(m_mine, mx);
-      const float pr = (sc == -INFINITY) ? 0.f : expf(sc - m_new);
-      const float alpha = (m_mine == -INFINITY) ? 0.f : expf(m_mine - m_new);
-      float ps = pr;
+        for (int bt = 0; bt < LPW; ++bt) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1 << (SH + bt)));
+        const float m_new = fmaxf(m_mine, mx);
+        const float alpha = (m_mine == -INFINITY) ? 0.f : expf(m_mine - m_new);
+        l_mine *= alpha;
+        m_mine = m_new;
 #pragma unroll
-      for (int bt = 0; bt < LPW; ++bt) ps += __shfl_xor_sync(0xffffffffu, ps, 1 << (SH + bt));
-      l_mine = l_mine * alpha + ps;
-      m_mine = m_new;
+        for (int gg = 0; gg < G; ++gg) {
+          const float a = __shfl_sync(0xffffffffu, alpha, (gg * PW) << SH);
 #pragma unroll
-      for (int gg = 0; gg < G; ++gg) {
-        const float a = __shfl_sync(0xffffffffu, alpha, (gg * PW) << SH);
-#pragma unroll
-        for (int j = 0; j < DL; ++j) acc[gg][j] *= a;
+          for (int j = 0; j < DL; ++j) acc[gg][j] *= a;
+        }
       }
+      const float pr = (sc == -INFINITY) ? 0.f : expf(sc - m_mine);
+      l_mine += pr;  // this lane's (head, position) slot; the positions are summed at the segment's end
 #pragma unroll
       for (int i = 0; i < PW; ++i) {
         if (warp + i * NW >= rows) break;  // warp-uniform
