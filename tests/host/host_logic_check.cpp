@@ -98,6 +98,10 @@ static void check_tiled_q4(int N, int K) {
 int main() {
   for (int64_t total : {1, 2, 3, 7, 151, 152, 153, 384, 1000, 49152, 22016 * 43})
     for (int parts : {1, 5, 148, 152, 160}) check_split(total, parts);
+  // the attention cluster's shares: a head's chunks (fewer than the CTAs too)
+  // and the merge's 32-element blocks over the cluster sizes in use
+  for (int64_t total : {1, 4, 8, 16, 32, 33, 35, 64, 65})
+    for (int parts : {2, 3, 4, 8, 12, 16}) check_split(total, parts);
   for (int K : {8, 264, 512, 1000, 1408, 2048, 4096}) check_tiled(16, K);
   check_tiled(64, 11008);
   for (int K : {64, 512, 1408, 2048, 4096, 11008}) check_tiled_q4(8, K);
