@@ -149,3 +149,46 @@ def test_noalloc_refuses_records_beyond_its_array():
     torch.cuda.synchronize()
     assert torch.all(o == 7.0)                 # nothing ran
     dec.noalloc_sync_status()
+
+
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 2, 2), (64, 4, 2)])
+def test_noalloc_attention_rising_scores_against_oracle(hd, nq, nkv):
+    """Scores that climb by 20 per attention chunk over a period of 8 chunks
+    (far past the online softmax's slack of 8) move the running max at almost
+    every chunk a CTA streams, so the rescaling path runs again and again (a
+    CTA streams ~8 chunks of the 40 000-row context); the other KV head's keys
+    are random (one rescale, at its first chunk).  Compared head by head with
+    the oracle's attention."""
+    rng = np.random.default_rng(hd + nq)
+    n = 40000
+    ctx = n + 8
+    ch = 16384 // (2 * hd)  # rows of one 16 KB K chunk
+    q = rng.normal(0, 1, (nq, hd)).astype(np.float32)
+    scale = 1.0 / np.sqrt(hd)
+    t = np.arange(ctx)
+    target = 20.0 * (t % (8 * ch)) / ch  # scores wanted for query head 0
+    kc = np.empty((nkv, ctx, hd), np.float32)
+    g0 = orc.kv_head_of(0, nq, nkv)
+    qh = q[0].astype(np.float64)
+    kc[g0] = (target / scale)[:, None] * (qh / (qh @ qh))[None, :]
+    for g in range(nkv):
+        if g != g0:
+            kc[g] = rng.normal(0, 1, (ctx, hd))
+    kc = _bf16(kc)
+    vc = _bf16(rng.normal(0, 1, (nkv, ctx, hd)))
+    # the construction, on the stored keys: within a period each chunk's top
+    # score is more than the slack above the previous chunk's
+    k64 = torch.from_numpy(kc.view(np.int16)).view(torch.bfloat16).double().numpy()
+    top = ((k64[g0, :n] @ qh) * scale)[: (n // ch) * ch].reshape(-1, ch).max(axis=1)
+    steps = np.diff(top)[(np.arange(len(top) - 1) + 1) % 8 != 0]
+    assert steps.min() > 8.0
+    kc_dev = torch.from_numpy(kc.view(np.int16)).cuda()
+    vc_dev = torch.from_numpy(vc.view(np.int16)).cuda()
+    o_dev = torch.full((nq * hd,), float("nan"), device="cuda")
+    dec.attention_noalloc(torch.from_numpy(q.ravel()).cuda(), kc_dev, vc_dev, nq, nkv, hd, ctx, n, o_dev)
+    dec.noalloc_sync_status()
+    got = o_dev.cpu().numpy().reshape(nq, hd)
+    for h in range(nq):
+        g = orc.kv_head_of(h, nq, nkv)
+        ref = orc.attention_head(q[h].astype(np.float64), kc[g, :n], vc[g, :n])
+        assert_close(got[h], ref, f"rising scores, hd {hd}, head {h}", max_abs=1e-4, rel_l2=1e-5)
