@@ -256,3 +256,82 @@ def test_paged_kv_matches_contiguous_and_oracle(name, mode):
     for s in range(w.steps):
         for l in range(w.n_layers):
             assert_close(got[s, l], ref[s, l], f"{name} {mode} paged step {s} layer {l}")
+
+
+def _rope_rows(h: np.ndarray, pos: int, d: int, theta: float) -> np.ndarray:
+    """Rotate-half RoPE of [heads][d] in double."""
+    half = d // 2
+    ang = pos * theta ** (-2.0 * np.arange(half) / d)
+    c, s = np.cos(ang), np.sin(ang)
+    a, b = h[:, :half], h[:, half:]
+    return np.concatenate([a * c - b * s, a * s + b * c], axis=1)
+
+
+@pytest.mark.parametrize("hd,nq,nkv", [(128, 2, 2), (64, 4, 2)])
+@pytest.mark.parametrize("mode", ["fused_graph", "headproj", "global_merge"])
+def test_attention_rising_scores_through_the_step(hd, nq, nkv, mode):
+    """The decoder's own attention (cluster kernels with records pushed or
+    exchanged, and the flat grid) on a prefilled context whose scores for query
+    head 0 climb by 20 per chunk over periods of 8 chunks: the online softmax's
+    reference max moves past its slack of 8 at almost every chunk each CTA
+    streams (~8 chunks a CTA), so the rescaling path keeps running.  One layer
+    with Wq = Wo = I, Wk = Wv = Wdown = 0 and unit norms gives
+    out = x + attention(RoPE(rmsnorm(x))); compared with the oracle's attention
+    head by head."""
+    from oracle import oracle as orc
+    eps, theta, one = 1e-6, 1e4, 0x3F80
+    H, F = nq * hd, 64
+    ch = 16384 // (2 * hd)                 # rows of one 16 KB K chunk
+    prefill = 128 * ch                     # 128 chunks a head: ~8 a CTA at 16 CTAs a head
+    max_ctx = prefill + 4
+    rng = np.random.default_rng(hd * 10 + nq)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).view(
+            torch.int16).numpy().view(np.uint16)
+
+    x = rng.normal(0, 1, H).astype(np.float32)
+    pos = prefill
+    n1 = x.astype(np.float64) / np.sqrt(np.mean(x.astype(np.float64) ** 2) + eps)
+    q = _rope_rows(n1.reshape(nq, hd), pos, hd, theta)
+    scale = 1.0 / np.sqrt(hd)
+    t = np.arange(prefill)
+    target = 20.0 * (t % (8 * ch)) / ch
+    g0 = orc.kv_head_of(0, nq, nkv)
+    kp = np.empty((nkv, prefill, hd), np.float32)
+    kp[g0] = (target / scale)[:, None] * (q[0] / (q[0] @ q[0]))[None, :]
+    for g in range(nkv):
+        if g != g0:
+            kp[g] = rng.normal(0, 1, (prefill, hd))
+    kp = bf16(kp)
+    vp = bf16(rng.normal(0, 1, (nkv, prefill, hd)))
+    k64 = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).double().numpy()
+    top = ((k64[g0] @ q[0]) * scale).reshape(-1, ch).max(axis=1)
+    steps = np.diff(top)[(np.arange(len(top) - 1) + 1) % 8 != 0]
+    assert steps.min() > 8.0               # the construction, on the stored keys
+
+    d = dec.Decoder(dec.Shape(1, H, nq, nkv, hd, F, max_ctx, eps, theta), **MODES[mode])
+    eye = np.where(np.eye(H, dtype=bool), one, 0).astype(np.uint16)
+    d.load_weights(0, dec.DEC_T_ATTN_NORM, np.full(H, one, np.uint16))
+    d.load_weights(0, dec.DEC_T_FFN_NORM, np.full(H, one, np.uint16))
+    d.load_weights(0, dec.DEC_T_WQ, eye)
+    d.load_weights(0, dec.DEC_T_WK, np.zeros((nkv * hd, H), np.uint16))
+    d.load_weights(0, dec.DEC_T_WV, np.zeros((nkv * hd, H), np.uint16))
+    d.load_weights(0, dec.DEC_T_WO, eye)
+    d.load_weights(0, dec.DEC_T_WGATE, bf16(rng.normal(0, 0.02, (F, H))))
+    d.load_weights(0, dec.DEC_T_WUP, bf16(rng.normal(0, 0.02, (F, H))))
+    d.load_weights(0, dec.DEC_T_WDOWN, np.zeros((H, F), np.uint16))
+    d.load_kv(0, kp, vp)
+    emb = torch.from_numpy(x).cuda()
+    out = torch.empty(H, device="cuda")
+    d.step(emb, pos, out)
+    d.sync_status()
+    got = out.cpu().numpy().astype(np.float64) - x      # out = x + attention
+    d.close()
+    kz = np.concatenate([kp, np.zeros((nkv, 1, hd), np.uint16)], axis=1)   # the appended row: k = v = 0
+    vz = np.concatenate([vp, np.zeros((nkv, 1, hd), np.uint16)], axis=1)
+    for h in range(nq):
+        g = orc.kv_head_of(h, nq, nkv)
+        ref = orc.attention_head(q[h], kz[g], vz[g])
+        assert_close(got[h * hd:(h + 1) * hd], ref, f"rising scores through the step, {mode}, hd {hd}, head {h}",
+                     max_abs=1e-3, rel_l2=1e-4)
