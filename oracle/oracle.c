@@ -58,6 +58,7 @@ enum {
   MUT_ROPE_PAIR_SWAP = 15,  /* interleaved RoPE rotating (2i+1, 2i) instead of (2i, 2i+1) */
   MUT_ARGMAX_LAST_TIE = 16, /* greedy choice keeps the last of equal logits */
   MUT_LM_NO_NORM = 17,      /* LM head without the final RMSNorm */
+  MUT_ATTN_NO_MAX = 18,     /* softmax weights exp(s) without the running max subtracted */
 };
 
 /* ---- storage formats ---------------------------------------------------- */
@@ -156,7 +157,7 @@ void orc_attention_head(const double* q, const uint16_t* K, const uint16_t* V, i
   }
   double z = 0.0;
   for (int t = 0; t < n; ++t) {
-    s[t] = exp(s[t] - m);
+    s[t] = exp(s[t] - (g_mutation == MUT_ATTN_NO_MAX ? 0.0 : m));
     z += s[t];
   }
   for (int i = 0; i < d; ++i) o[i] = 0.0;

@@ -28,7 +28,7 @@ MUTATIONS = {
     "attn_no_scale": 5, "attn_gqa_mod": 6, "silu_on_up": 7, "no_residual2": 8,
     "gemv_transpose": 9, "q4_no_offset": 10, "attn_skip_last": 11,
     "q4_stale_n1_codes": 12, "q4_o_tensor_scale": 13, "q4_a_no_dx": 14,
-    "rope_pair_swap": 15, "argmax_last_tie": 16, "lm_no_norm": 17,
+    "rope_pair_swap": 15, "argmax_last_tie": 16, "lm_no_norm": 17, "attn_no_max": 18,
 }
 
 # Tensor order of the layer struct's matrix slots.

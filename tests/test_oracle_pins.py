@@ -196,6 +196,21 @@ def pin_attention():
     qd[0] = 1.0
     Kd[-1, 0] = _bf16_bits_from_f32(np.array([200.0], np.float32))[0]
     _close(orc.attention_head(qd, Kd, V), _bf16_f64(V)[-1], 1e-12, "dominant score")
+    # softmax is shift invariant: scores near 1000 (exp overflows in fp64 past
+    # ~709) give exactly the output of the same scores moved near 0; keys
+    # 2000 + 16 j and 16 j are exact in bf16, q = 2 e0, scale 1/4: scores
+    # 1000 + 8 j and 8 j
+    Kb = _rand_bf16((n, d))
+    Ks = Kb.copy()
+    js = np.array([3, 0, 7, 5, 1, 6, 2, 4, 7])
+    Kb[:, 0] = _bf16_bits_from_f32((16.0 * js).astype(np.float32))
+    Ks[:, 0] = _bf16_bits_from_f32((2000.0 + 16.0 * js).astype(np.float32))
+    assert np.all(_bf16_f64(Ks)[:, 0] - _bf16_f64(Kb)[:, 0] == 2000.0)
+    q2 = 2.0 * qd
+    base = orc.attention_head(q2, Kb, V)
+    _close(orc.attention_head(q2, Ks, V), base, 1e-12, "shift invariance at scores ~1000")
+    w = np.exp(8.0 * js - 8.0 * js.max())
+    _close(base, (w / w.sum()) @ _bf16_f64(V), 1e-12, "softmax weights of the small scores")
     # library: torch SDPA (float64) with GQA
     nq, nkv, n = 8, 2, 23
     Q = RNG.normal(0, 1, (nq, d))
