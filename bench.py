@@ -292,15 +292,21 @@ def oracle_cores() -> int:
     return int(n) if n and n.isdigit() else (os.cpu_count() or 1)
 
 
-def time_oracle_tokens(w, host, budget_s: float, max_tokens: int):
-    """Whole oracle tokens from pos = prefill until the time budget is spent."""
-    st = oracle_for(w, host, w.prefill + max_tokens + 2)
+def time_oracle_tokens(w, host, budget_s: float, positions: int, max_tokens: int = 1 << 20):
+    """Whole oracle tokens at the positions the timed region decodes (prefill
+    to prefill + positions - 1, the cache rewound to the prefill at each wrap)
+    until the time budget is spent, so the sample's size does not hang on the
+    step count."""
+    st = oracle_for(w, host, w.prefill + positions + 2)
     from transformer_layer_decode_gb300 import synth
     n, t_total = 0, 0.0
     while n < max_tokens and (n == 0 or t_total < budget_s):
-        x = synth.step_input(w, n)
+        i = n % positions
+        if i == 0:
+            st.kv_len = w.prefill  # rewound: the rows past the prefill are written again
+        x = synth.step_input(w, i)
         t0 = time.perf_counter()
-        st.step(x, w.prefill + n)
+        st.step(x, w.prefill + i)
         t_total += time.perf_counter() - t0
         n += 1
     return n, t_total
@@ -536,11 +542,12 @@ def run_ours(args, w, rank, world, local_rank):
     if want_cpu:
         from oracle import oracle as orc
         orc.build()
-        n, t = time_oracle_tokens(w, host, budget_s=15.0, max_tokens=K)
+        n, t = time_oracle_tokens(w, host, budget_s=15.0, positions=K)
         result["cpu_baseline"] = {"value": n / t, "unit": "tok/s", "cores": oracle_cores(),
                                   "kind": "oracle",
-                                  "sample": f"{n} whole tokens from pos {w.prefill} "
-                                            f"({t:.1f} s of CPU work)"}
+                                  "sample": f"{n} whole tokens at the timed positions "
+                                            f"{w.prefill}..{w.prefill + K - 1} (the cache rewound "
+                                            f"at each wrap; {t:.1f} s of CPU work)"}
     return result if rank == 0 else None
 
 

@@ -69,3 +69,18 @@ def test_bench_reports_traffic_only_for_matching_sources(monkeypatch):
     assert bench.profiled_traffic(workload, kernel) == d["dram_bytes_per_launch"]
     monkeypatch.setattr(bench, "kernel_source_sha", lambda: "0" * 16)
     assert bench.profiled_traffic(workload, kernel) is None
+
+
+def test_cpu_baseline_sample_is_sized_by_time_and_wraps():
+    """The oracle sample beside the GPU line runs whole tokens at the timed
+    positions until its time budget is spent, rewinding the cache at each
+    wrap (the oracle itself insists on strictly sequential positions)."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from transformer_layer_decode_gb300 import synth
+    w = synth.WORKLOADS["layer_h512"]
+    host = bench.host_workload(w)
+    n, t = bench.time_oracle_tokens(w, host, budget_s=0.2, positions=3)
+    assert n > 3 and t >= 0.2            # wrapped at least once, sized by the budget
+    n, _ = bench.time_oracle_tokens(w, host, budget_s=10.0, positions=4, max_tokens=9)
+    assert n == 9                        # the token cap holds
