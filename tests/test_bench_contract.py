@@ -2,6 +2,7 @@
 contract's JSON line; it needs no GPU, so it runs here on a small workload."""
 import json
 import os
+import re
 import subprocess
 import sys
 
@@ -84,3 +85,20 @@ def test_cpu_baseline_sample_is_sized_by_time_and_wraps():
     assert n > 3 and t >= 0.2            # wrapped at least once, sized by the budget
     n, _ = bench.time_oracle_tokens(w, host, budget_s=10.0, positions=4, max_tokens=9)
     assert n == 9                        # the token cap holds
+
+
+def test_profile_summaries_name_safe_commands():
+    """Every ncu command a committed profile summary gives leaves the clocks
+    alone and runs committed files only (no scratch or machine paths)."""
+    prof = os.path.join(ROOT, "profiles")
+    seen = 0
+    for f in sorted(os.listdir(prof)):
+        text = open(os.path.join(prof, f)).read()
+        for line in text.splitlines():
+            if line.lstrip().startswith("#"):
+                continue  # a heading
+            if re.search(r"(^|\s|&&)ncu\s+--", line) and ("--metrics" in line or "--set" in line):
+                seen += 1
+                assert "--clock-control none" in line, (f, line)
+        assert "_work/" not in text and "/root/" not in text, f
+    assert seen > 0
